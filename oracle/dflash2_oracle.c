@@ -1,0 +1,162 @@
+/*
+ * DFlash2 draft-head oracle: plain, slow, fp64 CPU definitions of the hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or
+ * call this file; only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code with the CUDA library.
+ *
+ * Source of every formula: ggml-org/llama.cpp pull request #27342,
+ * "spec : add DFlash2 support (local convolution + candidate selector)",
+ * section "Overview" (the two printed formulas), together with the tensor names
+ * in the same thread's review ("selector_predecessor", "selector_successor",
+ * "selector_hidden") and the codebook-size exchange further down that thread.
+ *
+ * Readings taken where the page is silent (each is also listed in the design
+ * notes of the repository):
+ *   - taps t = 0..T-1, tap t multiplies x[i-t] (causal, not flipped);
+ *   - positions before the block come from a (T-1)-row history window, oldest
+ *     row first, so hist row T-1+j holds position j for j = -(T-1)..-1; a NULL
+ *     history means zeros;
+ *   - groups are contiguous: g(c) = c / (C/G);
+ *   - project(h) is a plain linear map u = h W^T with W stored [R, d];
+ *   - predecessors of position i are the K candidates of position i-1, so the
+ *     transitions of a block are i = 1..n-1;
+ *   - unary is per (position, candidate slot);
+ *   - the argmax keeps the lowest slot on ties (strict ">" scan).
+ *
+ * All arithmetic is IEEE double.  Inputs arrive as double arrays; callers that
+ * model bf16 data round to bf16 before converting, so both sides read the same
+ * values.  OpenMP only splits the outermost independent loop; it changes no
+ * arithmetic and no summation order.
+ */
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the OpenMP runtime will use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Grouped dynamic depthwise causal convolution (Overview, first formula):
+ *   out[s,i,c] = sum_{t=0}^{T-1} (base[t,c] + delta[s,i,t,g(c)]) * x~[s,i-t,c]
+ * with x~[s,j,c] = x[s,j,c] for j >= 0 and hist[s,T-1+j,c] for j < 0.
+ * Layouts (row-major): x, out [S,n,C]; hist [S,T-1,C] or NULL; base [T,C];
+ * delta [S,n,T,G].  Returns 0, or 1 when C is not a multiple of G.
+ */
+int oracle_dynconv(const double* x, const double* hist, const double* base,
+                   const double* delta, double* out,
+                   long S, long n, long C, long T, long G) {
+    if (C % G != 0) return 1;
+    const long cg = C / G;
+    long si;
+#pragma omp parallel for schedule(static)
+    for (si = 0; si < S * n; ++si) {
+        const long s = si / n, i = si % n;
+        for (long c = 0; c < C; ++c) {
+            const long g = c / cg;
+            double acc = 0.0;
+            for (long t = 0; t < T; ++t) {
+                const long j = i - t;
+                double xv;
+                if (j >= 0)
+                    xv = x[(s * n + j) * C + c];
+                else if (hist != NULL)
+                    xv = hist[(s * (T - 1) + (T - 1 + j)) * C + c];
+                else
+                    xv = 0.0;
+                const double w = base[t * C + c] + delta[((s * n + i) * T + t) * G + g];
+                acc += w * xv;
+            }
+            out[(s * n + i) * C + c] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * project(h): the dense d -> R map of each position's hidden state ("This
+ * position's hidden is projected ... to the same rank"; weight tensor
+ * "selector_hidden").  u[r,k] = sum_j h[r,j] * W[k,j].
+ * Layouts: h [P,d], W [R,d], u [P,R].
+ */
+void oracle_project(const double* h, const double* W, double* u,
+                    long P, long d, long R) {
+    long r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < P; ++r) {
+        for (long k = 0; k < R; ++k) {
+            double acc = 0.0;
+            for (long j = 0; j < d; ++j) acc += h[r * d + j] * W[k * d + j];
+            u[r * R + k] = acc;
+        }
+    }
+}
+
+/*
+ * Edge scores and the per-predecessor argmax (Overview, second formula):
+ *   edge(p -> c) = < A[p] (.) project(h), B[c] > + unary[c]
+ * For sequence s and position i in 1..n-1, predecessor slot p and candidate
+ * slot c:
+ *   e[s,i-1,p,c] = sum_r A[id_p,r] * u[s*n+i,r] * B[id_c,r] + unary[s,i,c],
+ *   id_p = cand_ids[s,i-1,p], id_c = cand_ids[s,i,c].
+ * The readout for (s,i-1,p) is the lowest slot c reaching max_c e, and that max.
+ * Layouts: cand_ids, unary [S,n,K]; u [S*n,R]; A, B [V,R];
+ * edges [S,n-1,K,K] or NULL; best_slot, best_score [S,n-1,K].
+ * Returns 0, or 1 if any candidate id lies outside [0,V) (nothing written for
+ * that transition's rows beyond what was computed before the check).
+ */
+int oracle_edges(const int32_t* cand_ids, const double* u, const double* A,
+                 const double* B, const double* unary,
+                 long S, long n, long K, long R, long V,
+                 double* edges, int32_t* best_slot, double* best_score) {
+    for (long q = 0; q < S * n * K; ++q)
+        if (cand_ids[q] < 0 || (long)cand_ids[q] >= V) return 1;
+    if (n < 2) return 0;
+    const long E = n - 1;
+    long se;
+#pragma omp parallel for schedule(static)
+    for (se = 0; se < S * E; ++se) {
+        const long s = se / E, i = se % E + 1;
+        const double* urow = u + (s * n + i) * R;
+        for (long p = 0; p < K; ++p) {
+            const long idp = cand_ids[(s * n + i - 1) * K + p];
+            double best = 0.0;
+            int32_t arg = 0;
+            for (long c = 0; c < K; ++c) {
+                const long idc = cand_ids[(s * n + i) * K + c];
+                double acc = 0.0;
+                for (long r = 0; r < R; ++r)
+                    acc += A[idp * R + r] * urow[r] * B[idc * R + r];
+                const double e = acc + unary[(s * n + i) * K + c];
+                if (edges != NULL) edges[((s * E + (i - 1)) * K + p) * K + c] = e;
+                if (c == 0 || e > best) {
+                    best = e;
+                    arg = (int32_t)c;
+                }
+            }
+            best_slot[(s * E + (i - 1)) * K + p] = arg;
+            best_score[(s * E + (i - 1)) * K + p] = best;
+        }
+    }
+    return 0;
+}
+
+/* The composite selector: project every position's hidden state, then score
+ * the edges and read out the argmax.  u [S*n,R] receives the projection. */
+int oracle_select(const double* h, const double* W, const int32_t* cand_ids,
+                  const double* A, const double* B, const double* unary,
+                  long S, long n, long d, long K, long R, long V,
+                  double* u, double* edges, int32_t* best_slot, double* best_score) {
+    oracle_project(h, W, u, S * n, d, R);
+    return oracle_edges(cand_ids, u, A, B, unary, S, n, K, R, V, edges, best_slot,
+                        best_score);
+}
