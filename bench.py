@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Throughput of the DFlash2 draft-head hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the grouped dynamic depthwise causal convolution, the projection of every
+position's hidden state, and the edge scores with the per-predecessor argmax.
+The default workload is the batched verification regime (256 sequences x 16
+positions, d = C = 5120, T = 4, G = 40, R = 128, V = 151936, K = 16).
+
+Prints ONE JSON line (rank 0).  The metric is draft positions per second
+(conv positions of all ranks / max-over-ranks time); the dominant kernel's
+achieved HBM bandwidth is reported against the measured peak.
+
+  python bench.py [--gpus N --steps K --warmup W --workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DFlash2 conv+selector draft positions/sec; achieved HBM GB/s vs GB300 peak"
+UNIT = "positions/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FLUSH_BYTES = 256 << 20
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
+# sha256 of the kernel source they were taken on (null when the source changed).
+TRAFFIC = {}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="dflash2", choices=["dflash2", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _workload(name):
+    from dflash2_draft_head_gb300.workloads import BENCH_WORKLOAD, BY_NAME
+    return BY_NAME[name] if name else BENCH_WORKLOAD
+
+
+def _config(w, world):
+    return {"workload": w.name, "S": w.S, "n": w.n, "C": w.C, "T": w.T, "G": w.G, "d": w.d,
+            "R": w.R, "V": w.V, "K": w.K, "selector_S": w.S_sel, "selector_n": w.n_sel,
+            "in_dtype": w.dtype, "out_dtype": w.dtype,
+            "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write)",
+            "parallelism": f"replicas x{world} (independent sequences per GPU)"}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def _bytes(w):
+    """Algorithmic bytes (each element streamed or gathered once, plus outputs)."""
+    b = 2 if w.dtype == "bf16" else 4
+    conv = (w.S * w.n * w.C * (b + b) + w.S * w.n * w.T * w.G * b + w.S * (w.T - 1) * w.C * b
+            + w.T * w.C * b)
+    P = w.S_sel * w.n_sel
+    proj = P * w.d * b + w.R * w.d * b + P * w.R * 4
+    proj_flops = 2.0 * P * w.d * w.R
+    E = w.S_sel * max(w.n_sel - 1, 0)
+    edges = E * (2 * w.K * w.R * b + 4 * w.R + 20 * w.K)
+    return conv, proj, proj_flops, edges
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+class OraclePool:
+    """Float64 copies of the workload's inputs, cut into units of up to 16 sequences."""
+
+    def __init__(self, w, max_units=16):
+        import numpy as np
+        from dflash2_draft_head_gb300 import synth
+        self.w = w
+        ub = min(w.S, 16)
+        self.ub = ub
+        self.units = []
+        n_conv = min(w.n, 4096)
+        self.n_conv = n_conv
+        base = synth.normal_whole(w.seed, "base", (w.T, w.C), math.sqrt(1.0 / w.T), w.dtype)
+        cb = synth.codebooks(w)
+        self.base = base.numpy().astype(np.float64)
+        self.W = cb["W"].numpy().astype(np.float64)
+        self.A = cb["A"].numpy().astype(np.float64)
+        self.B = cb["B"].numpy().astype(np.float64)
+        sel = synth.selector_inputs(w)
+        h = sel["h"].reshape(w.S_sel, w.n_sel, w.d)
+        for u0 in range(0, min(w.S, ub * max_units), ub):
+            ss = range(u0, min(w.S, u0 + ub))
+            x = np.stack([synth.normal_rows(w.seed, "x", s, 0, n_conv, (w.C,), 1.0, w.dtype,
+                                            w.n).numpy() for s in ss]).astype(np.float64)
+            hist = np.stack([synth.normal_rows(w.seed, "hist", s, 0, w.T - 1, (w.C,), 1.0,
+                                               w.dtype, w.T - 1).numpy() for s in ss]
+                            ).astype(np.float64)
+            delta = np.stack([synth.normal_rows(w.seed, "delta", s, 0, n_conv, (w.T, w.G),
+                                                math.sqrt(0.1 / w.T), w.dtype, w.n).numpy()
+                              for s in ss]).astype(np.float64)
+            s0, s1 = min(u0, w.S_sel), min(u0 + ub, w.S_sel)
+            self.units.append(dict(
+                x=x, hist=hist, delta=delta,
+                h=h[s0:s1].reshape(-1, w.d).numpy().astype(np.float64),
+                ids=sel["cand_ids"][s0:s1].numpy(),
+                unary=sel["unary"][s0:s1].numpy().astype(np.float64),
+                positions=len(ss) * n_conv))
+
+    def run(self, j):
+        import oracle
+        u = self.units[j % len(self.units)]
+        oracle.dynconv(u["x"], u["hist"], self.base, u["delta"])
+        if u["ids"].shape[0] > 0:
+            oracle.select(u["h"], self.W, u["ids"], self.A, self.B, u["unary"],
+                          want_edges=False)
+        return u["positions"]
+
+    def describe(self, reps):
+        w = self.w
+        return (f"{reps} oracle passes (dynconv + project + edges/argmax) over units of "
+                f"{self.ub} sequences x {self.n_conv} positions of {w.name} "
+                f"(selector on {w.n_sel} positions per sequence), fp64")
+
+
+def cpu_baseline(w, seconds):
+    import oracle
+    oracle.build()
+    pool = OraclePool(w)
+    pool.run(0)  # warm the code and pages
+    t0 = time.perf_counter()
+    pos = 0
+    reps = 0
+    while True:
+        pos += pool.run(reps)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 100000:
+            break
+    return {"value": pos / el, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": pool.describe(reps), "seconds": round(el, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = _env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = _workload(args.workload)
+    pool = OraclePool(w)
+    pool.run(0)
+    t0 = time.perf_counter()
+    pool.run(0)
+    t_unit = max(time.perf_counter() - t0, 1e-4)
+    total_budget = 120.0
+    units_per_step = max(1, int(total_budget / max(args.steps + args.warmup, 1) / t_unit))
+    for k in range(args.warmup):
+        for j in range(units_per_step):
+            pool.run(k * units_per_step + j)
+    pos = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        for j in range(units_per_step):
+            pos += pool.run(k * units_per_step + j)
+    el = time.perf_counter() - t0
+    v = pos / el
+    cores = oracle.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * el / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, world),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {units_per_step} units; "
+                                       + pool.describe(units_per_step * args.steps)},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.2)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = _env()
+    import ctypes
+
+    import torch
+    import torch.distributed as tdist
+
+    import dflash2_draft_head_gb300 as df2
+    from dflash2_draft_head_gb300 import synth
+
+    df2.build_library()
+    L = df2.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        tdist.init_process_group("nccl", device_id=dev)
+    w0 = _workload(args.workload)
+    w = dataclasses.replace(w0, seed=w0.seed + 1000 * rank)  # each rank its own sequences
+
+    bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ci = synth.conv_inputs(w)
+    cb = synth.codebooks(w0)
+    si = synth.selector_inputs(w)
+    host_in = {"x": ci["x"].to(bt), "hist": ci["hist"].to(bt), "delta": ci["delta"].to(bt),
+               "h": si["h"].to(bt), "cand_ids": si["cand_ids"], "unary": si["unary"]}
+    d_in = {k: v.to(dev).contiguous() for k, v in host_in.items()}
+    base = ci["base"].to(bt).to(dev)
+    Wt = cb["W"].to(bt).to(dev)
+    A = cb["A"].to(bt).to(dev)
+    B = cb["B"].to(bt).to(dev)
+    del ci, cb, si
+    out = torch.empty((w.S, w.n, w.C), dtype=bt, device=dev)
+    P = w.S_sel * w.n_sel
+    E = w.S_sel * max(w.n_sel - 1, 0)
+    u = torch.empty((P, w.R), dtype=torch.float32, device=dev)
+    best_slot = torch.empty((max(E, 1), w.K), dtype=torch.int32, device=dev)
+    best_score = torch.empty((max(E, 1), w.K), dtype=torch.float32, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    code = 1 if w.dtype == "bf16" else 0
+    vp = ctypes.c_void_p
+
+    def ptr(t):
+        return vp(t.data_ptr())
+
+    conv_args = (ptr(d_in["x"]), ptr(d_in["hist"]), ptr(base), ptr(d_in["delta"]), ptr(out),
+                 w.S, w.n, w.C, w.T, w.G, code, code, sp)
+    proj_args = (ptr(d_in["h"]), ptr(Wt), ptr(u), P, w.d, w.R, code, sp)
+    edge_args = (ptr(d_in["cand_ids"]), ptr(u), ptr(A), ptr(B), ptr(d_in["unary"]), w.S_sel,
+                 w.n_sel, w.K, w.R, w.V, code, None, ptr(best_slot), ptr(best_score), ptr(flag),
+                 sp)
+    f_conv, f_proj, f_edge = L.dflash2_dynconv, L.dflash2_project, L.dflash2_edges
+
+    def step():
+        r = f_conv(*conv_args) | f_proj(*proj_args) | f_edge(*edge_args)
+        if r:
+            raise RuntimeError(L.dflash2_last_error().decode())
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            tdist.barrier()
+
+    torch.cuda.set_stream(stream)
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    with ClockSampler(gpu_uuid) as clk:
+        barrier()
+        wall0 = time.perf_counter()
+        torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
+        for k in range(K):
+            flush.zero_()
+            e = ev[k]
+            e[0].record(stream)
+            if f_conv(*conv_args):
+                raise RuntimeError(L.dflash2_last_error().decode())
+            e[1].record(stream)
+            if f_proj(*proj_args):
+                raise RuntimeError(L.dflash2_last_error().decode())
+            e[2].record(stream)
+            if f_edge(*edge_args):
+                raise RuntimeError(L.dflash2_last_error().decode())
+            e[3].record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+    t_conv = [e[0].elapsed_time(e[1]) for e in ev]
+    t_proj = [e[1].elapsed_time(e[2]) for e in ev]
+    t_edge = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(t_step)
+    tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+    total_ms = float(tt.item())
+    if int(flag.item()) != 0 or df2.take_device_faults() != 0:
+        raise RuntimeError("device error flag set during the benchmark")
+
+    # end to end through the public API: pinned host inputs -> device -> readout -> host
+    pin = {k: v.pin_memory() for k, v in host_in.items()}
+    h_slot = torch.empty(best_slot.shape, dtype=torch.int32).pin_memory()
+    h_score = torch.empty(best_score.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = h_slot.numel() * 4 + h_score.numel() * 4
+
+    def e2e_step():
+        for k2, v in pin.items():
+            d_in[k2].copy_(v, non_blocking=True)
+        step()
+        h_slot.copy_(best_slot, non_blocking=True)
+        h_score.copy_(best_score, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    E2 = max(args.e2e_steps, 1)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E2):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        tdist.all_reduce(e2e_ms, op=tdist.ReduceOp.MAX)
+    e2e_ms = float(e2e_ms.item())
+
+    positions = w.S * w.n * world
+    value = positions * K / (total_ms / 1000.0)
+    conv_b, proj_b, proj_f, edge_b = _bytes(w)
+    hbm, tc, src = _peaks()
+    conv_us = 1000.0 * statistics.mean(t_conv)
+    proj_us = 1000.0 * statistics.mean(t_proj)
+    edge_us = 1000.0 * statistics.mean(t_edge)
+    achieved = conv_b / (conv_us * 1e-6) / 1e9
+    src_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
+                                               "dynconv.cu"), "rb").read()).hexdigest()
+    tr = TRAFFIC.get((w.name, "dynconv"))
+    traffic = tr["bytes"] if tr and tr["sha"] == src_sha else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": _config(w0, world),
+        "roofline": {"bound": "hbm", "kernel": "dflash2_dynconv", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "bytes_per_launch": conv_b, "peak_source": src},
+        "kernels": {
+            "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
+                        "frac_hbm": conv_b / conv_us / 1e3 / hbm},
+            "project": {"us": proj_us, "bytes": proj_b, "GB/s": proj_b / proj_us / 1e3,
+                        "TFLOP/s": proj_f / proj_us / 1e6,
+                        "frac_hbm": proj_b / proj_us / 1e3 / hbm,
+                        "frac_bf16_tc": proj_f / proj_us / 1e6 / tc},
+            "edges": {"us": edge_us, "bytes": edge_b, "GB/s": edge_b / edge_us / 1e3,
+                      "frac_hbm": edge_b / edge_us / 1e3 / hbm},
+        },
+        "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "cpu_baseline": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w0, args.cpu_seconds)
+    if world > 1:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

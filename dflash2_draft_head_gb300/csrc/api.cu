@@ -1,0 +1,278 @@
+// C ABI of the DFlash2 draft-head library: argument validation on the host,
+// then dispatch to the kernels.  Nothing here allocates device memory or
+// synchronises the host (except dflash2_take_device_faults, by contract).
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "dflash2.h"
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(DF2_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Buf {
+    const void* p;
+    size_t bytes;
+    const char* name;
+};
+
+bool overlap(const Buf& a, const Buf& b) {
+    if (a.p == nullptr || b.p == nullptr || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Every output must be disjoint from every other buffer.
+int check_disjoint(const Buf* outs, int nout, const Buf* ins, int nin) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlap(outs[i], ins[j]))
+                return fail(DF2_ERR_INVALID_ARG, "%s overlaps %s", outs[i].name, ins[j].name);
+        for (int j = i + 1; j < nout; ++j)
+            if (overlap(outs[i], outs[j]))
+                return fail(DF2_ERR_INVALID_ARG, "%s overlaps %s", outs[i].name, outs[j].name);
+    }
+    return DF2_OK;
+}
+
+int check_aligned(const Buf* bufs, int nb) {
+    for (int i = 0; i < nb; ++i)
+        if (bufs[i].p != nullptr && !aligned16(bufs[i].p))
+            return fail(DF2_ERR_INVALID_ARG, "%s is not 16-byte aligned", bufs[i].name);
+    return DF2_OK;
+}
+
+bool valid_dtype(int d) { return d == DF2_F32 || d == DF2_BF16; }
+size_t esize(int d) { return d == DF2_BF16 ? 2 : 4; }
+
+int num_sms_of_current_device() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    return sms;
+}
+
+int validate_project(const void* h, const void* W, const float* u, int P, int d, int R,
+                     int dtype) {
+    if (h == nullptr || W == nullptr || u == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "project: NULL h, W or u");
+    if (P <= 0 || d <= 0 || R <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "project: P=%d d=%d R=%d must be positive", P, d, R);
+    if (!valid_dtype(dtype)) return fail(DF2_ERR_INVALID_ARG, "project: bad dtype %d", dtype);
+    const size_t b = esize(dtype);
+    const Buf ins[2] = {{h, (size_t)P * d * b, "h"}, {W, (size_t)R * d * b, "W"}};
+    const Buf outs[1] = {{u, (size_t)P * R * 4, "u"}};
+    int st = check_aligned(ins, 2);
+    if (st == DF2_OK) st = check_aligned(outs, 1);
+    if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 2);
+    if (st != DF2_OK) return st;
+    if (R % 8 != 0 || R > 512)
+        return fail(DF2_ERR_UNSUPPORTED, "project: R=%d must be a multiple of 8 and <= 512", R);
+    if (dtype == DF2_BF16 && d % 8 != 0)
+        return fail(DF2_ERR_UNSUPPORTED, "project: bf16 needs d %% 8 == 0 (d=%d)", d);
+    if ((long long)P > 65535LL * 128)
+        return fail(DF2_ERR_UNSUPPORTED, "project: P=%d exceeds %d rows", P, 65535 * 128);
+    return DF2_OK;
+}
+
+int validate_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,
+                   const float* unary, int S, int n, int K, int R, int V, int dtype,
+                   const float* edges_out, const int32_t* best_slot, const float* best_score,
+                   const int32_t* err_flag) {
+    if (cand_ids == nullptr || u == nullptr || A == nullptr || B == nullptr || unary == nullptr ||
+        best_slot == nullptr || best_score == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "edges: NULL required pointer");
+    if (S <= 0 || n <= 0 || K <= 0 || R <= 0 || V <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "edges: S=%d n=%d K=%d R=%d V=%d must be positive", S, n,
+                    K, R, V);
+    if (!valid_dtype(dtype)) return fail(DF2_ERR_INVALID_ARG, "edges: bad dtype %d", dtype);
+    const size_t b = esize(dtype);
+    const size_t SnK = (size_t)S * n * K;
+    const size_t EK = (size_t)S * (n - 1) * K;
+    const Buf ins[5] = {{cand_ids, SnK * 4, "cand_ids"},
+                        {u, (size_t)S * n * R * 4, "u"},
+                        {A, (size_t)V * R * b, "A"},
+                        {B, (size_t)V * R * b, "B"},
+                        {unary, SnK * 4, "unary"}};
+    const Buf outs[4] = {{edges_out, EK * K * 4, "edges_out"},
+                         {best_slot, EK * 4, "best_slot"},
+                         {best_score, EK * 4, "best_score"},
+                         {err_flag, 4, "err_flag"}};
+    int st = check_aligned(ins, 5);
+    if (st == DF2_OK) st = check_aligned(outs, 3);
+    if (st == DF2_OK && err_flag != nullptr && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
+        st = fail(DF2_ERR_INVALID_ARG, "err_flag is not 4-byte aligned");
+    if (st == DF2_OK) st = check_disjoint(outs, 4, ins, 5);
+    if (st != DF2_OK) return st;
+    if (K > 256) return fail(DF2_ERR_UNSUPPORTED, "edges: K=%d > 256", K);
+    if (R % 8 != 0 || R > 512)
+        return fail(DF2_ERR_UNSUPPORTED, "edges: R=%d must be a multiple of 8 and <= 512", R);
+    if ((long long)S * (n - 1) > 0x7FFFFFFFLL)
+        return fail(DF2_ERR_UNSUPPORTED, "edges: too many transitions");
+    return DF2_OK;
+}
+
+int run_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,
+              const float* unary, int S, int n, int K, int R, int V, int dtype, float* edges_out,
+              int32_t* best_slot, float* best_score, int32_t* err_flag, cudaStream_t stream) {
+    if (n == 1) return DF2_OK;
+    df2::EdgesArgs a{cand_ids, u, A, B, unary, S, n, K, R, V, edges_out, best_slot, best_score,
+                     err_flag};
+    cudaError_t e;
+    if (dtype == DF2_BF16 && df2::edges_tc_supported(K, R))
+        e = df2::launch_edges_bf16_tc(a, stream);
+    else
+        e = df2::launch_edges_warp(a, dtype == DF2_BF16, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+    return DF2_OK;
+}
+
+int run_project(const void* h, const void* W, float* u, int P, int d, int R, int dtype,
+                cudaStream_t stream) {
+    df2::ProjectArgs a{h, W, u, P, d, R};
+    cudaError_t e = dtype == DF2_BF16
+                        ? df2::launch_project_bf16_tc(a, stream, num_sms_of_current_device())
+                        : df2::launch_project_f32(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "project launch");
+    return DF2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash2_version(void) { return 100; }
+
+const char* dflash2_status_string(int status) {
+    switch (status) {
+        case DF2_OK:
+            return "DF2_OK";
+        case DF2_ERR_INVALID_ARG:
+            return "DF2_ERR_INVALID_ARG";
+        case DF2_ERR_UNSUPPORTED:
+            return "DF2_ERR_UNSUPPORTED";
+        case DF2_ERR_CUDA:
+            return "DF2_ERR_CUDA";
+        default:
+            return "DF2_UNKNOWN_STATUS";
+    }
+}
+
+const char* dflash2_last_error(void) { return g_err; }
+
+int dflash2_dynconv(const void* x, const void* hist, const void* base, const void* delta,
+                    void* out, int S, int n, int C, int T, int G, int in_dtype, int out_dtype,
+                    void* stream) {
+    g_err[0] = 0;
+    if (x == nullptr || base == nullptr || delta == nullptr || out == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "dynconv: NULL x, base, delta or out");
+    if (S <= 0 || n <= 0 || C <= 0 || T <= 0 || G <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "dynconv: S=%d n=%d C=%d T=%d G=%d must be positive", S,
+                    n, C, T, G);
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+        return fail(DF2_ERR_INVALID_ARG, "dynconv: bad dtype");
+    if (C % G != 0) return fail(DF2_ERR_INVALID_ARG, "dynconv: C=%d not a multiple of G=%d", C, G);
+    const size_t bi = esize(in_dtype), bo = esize(out_dtype);
+    const Buf ins[4] = {{x, (size_t)S * n * C * bi, "x"},
+                        {hist, (size_t)S * (T - 1) * C * bi, "hist"},
+                        {base, (size_t)T * C * bi, "base"},
+                        {delta, (size_t)S * n * T * G * bi, "delta"}};
+    const Buf outs[1] = {{out, (size_t)S * n * C * bo, "out"}};
+    int st = check_aligned(ins, 4);
+    if (st == DF2_OK) st = check_aligned(outs, 1);
+    if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 4);
+    if (st != DF2_OK) return st;
+    if (C % 8 != 0 || (C / G) % 8 != 0)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv: needs C %% 8 == 0 and (C/G) %% 8 == 0");
+    if (T > 16) return fail(DF2_ERR_UNSUPPORTED, "dynconv: T=%d > 16", T);
+    if (in_dtype == DF2_F32 && out_dtype == DF2_BF16)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv: fp32 input with bf16 output");
+    df2::DynconvArgs a{x, T > 1 ? hist : nullptr, base, delta, out, S, n, C, T, G,
+                       in_dtype == DF2_BF16, out_dtype == DF2_BF16};
+    cudaError_t e = df2::launch_dynconv(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dynconv launch");
+    return DF2_OK;
+}
+
+int dflash2_project(const void* h, const void* W, float* u, int P, int d, int R, int in_dtype,
+                    void* stream) {
+    g_err[0] = 0;
+    int st = validate_project(h, W, u, P, d, R, in_dtype);
+    if (st != DF2_OK) return st;
+    return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,
+                  const float* unary, int S, int n, int K, int R, int V, int cb_dtype,
+                  float* edges_out, int32_t* best_slot, float* best_score, int32_t* err_flag,
+                  void* stream) {
+    g_err[0] = 0;
+    int st = validate_edges(cand_ids, u, A, B, unary, S, n, K, R, V, cb_dtype, edges_out,
+                            best_slot, best_score, err_flag);
+    if (st != DF2_OK) return st;
+    return run_edges(cand_ids, u, A, B, unary, S, n, K, R, V, cb_dtype, edges_out, best_slot,
+                     best_score, err_flag, static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const void* A,
+                   const void* B, const float* unary, int S, int n, int d, int K, int R, int V,
+                   int dtype, float* u_out, float* edges_out, int32_t* best_slot,
+                   float* best_score, int32_t* err_flag, void* stream) {
+    g_err[0] = 0;
+    if (S <= 0 || n <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "select: S=%d n=%d must be positive", S, n);
+    if ((long long)S * n > 0x7FFFFFFFLL) return fail(DF2_ERR_UNSUPPORTED, "select: S*n too large");
+    int st = validate_project(h, W, u_out, S * n, d, R, dtype);
+    if (st == DF2_OK)
+        st = validate_edges(cand_ids, u_out, A, B, unary, S, n, K, R, V, dtype, edges_out,
+                            best_slot, best_score, err_flag);
+    if (st != DF2_OK) return st;
+    // the projection output must not alias anything the selector reads or writes
+    const size_t b = esize(dtype);
+    const Buf uo[1] = {{u_out, (size_t)S * n * R * 4, "u_out"}};
+    const Buf others[8] = {{cand_ids, (size_t)S * n * K * 4, "cand_ids"},
+                           {A, (size_t)V * R * b, "A"},
+                           {B, (size_t)V * R * b, "B"},
+                           {unary, (size_t)S * n * K * 4, "unary"},
+                           {edges_out, (size_t)S * (n - 1) * K * K * 4, "edges_out"},
+                           {best_slot, (size_t)S * (n - 1) * K * 4, "best_slot"},
+                           {best_score, (size_t)S * (n - 1) * K * 4, "best_score"},
+                           {err_flag, 4, "err_flag"}};
+    st = check_disjoint(uo, 1, others, 8);
+    if (st != DF2_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = run_project(h, W, u_out, S * n, d, R, dtype, s);
+    if (st != DF2_OK) return st;
+    return run_edges(cand_ids, u_out, A, B, unary, S, n, K, R, V, dtype, edges_out, best_slot,
+                     best_score, err_flag, s);
+}
+
+int dflash2_take_device_faults(int32_t* flags_out) {
+    g_err[0] = 0;
+    if (flags_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "flags_out is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned v = 0;
+    if (e == cudaSuccess) e = df2::take_project_faults(&v);
+    if (e != cudaSuccess) return cuda_fail(e, "take_device_faults");
+    *flags_out = (int32_t)v;
+    return DF2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal declarations shared by the kernel translation units and the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace df2 {
+
+// Upper bound of polls of one bounded mbarrier wait before a kernel gives up.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+struct DynconvArgs {
+    const void* x;
+    const void* hist;
+    const void* base;
+    const void* delta;
+    void* out;
+    int S, n, C, T, G;
+    int in_bf16, out_bf16;
+};
+
+struct ProjectArgs {
+    const void* h;
+    const void* W;
+    float* u;
+    int P, d, R;
+};
+
+struct EdgesArgs {
+    const int32_t* cand_ids;
+    const float* u;
+    const void* A;
+    const void* B;
+    const float* unary;
+    int S, n, K, R, V;
+    float* edges_out;
+    int32_t* best_slot;
+    float* best_score;
+    int32_t* err_flag;
+};
+
+// Each launcher enqueues on `stream` and returns the launch's cudaError_t.
+cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream);
+cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
+cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
+// Reads and clears the projection kernel's device fault word (synchronous).
+cudaError_t take_project_faults(unsigned* flags);
+// Tensor-core tile path: bf16 codebooks, K a power of two <= 128, R <= 384.
+bool edges_tc_supported(int K, int R);
+cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, cudaStream_t stream);
+// Warp-per-predecessor path (any K <= 256, R <= 512; fp32 or bf16 codebooks).
+cudaError_t launch_edges_warp(const EdgesArgs& a, int cb_bf16, cudaStream_t stream);
+
+}  // namespace df2

@@ -1,0 +1,400 @@
+// Edge scores and per-predecessor argmax of the DFlash2 candidate selector
+// (ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local
+// convolution + candidate selector)", Overview, second formula):
+//   edge(p -> c) = < A[p] (.) project(h), B[c] > + unary[c]
+// For every transition into position i (predecessors = candidates of i-1):
+//   e[p,c] = sum_r A[id_p,r] u[i,r] B[id_c,r] + unary[i,c],  readout argmax_c.
+//
+// Tensor-core tile path (bf16 codebooks, K a power of two <= 128, R <= 384):
+//  - a CTA takes 128/K consecutive transitions, i.e. 128 predecessor rows and
+//    128 candidate rows;
+//  - 128 threads gather the rows by token id with 16-byte loads (a half-warp
+//    or a warp per 256/512-byte row, fully coalesced), form the gate
+//    G = A[id_p] (.) u in fp32, round it to bf16 and store G and B[id_c]
+//    straight into the 128-byte-swizzle K-major layout of the tensor core;
+//  - one thread issues tcgen05.mma (M=128, N=128, K=16 per instruction) over
+//    R into a 128x128 fp32 accumulator in tensor memory.  Only the K x K
+//    diagonal blocks (same transition) are read back; the rest of the tile
+//    is free work on an otherwise idle unit;
+//  - each thread owns one predecessor row: tcgen05.ld of its block, + unary,
+//    running argmax (lowest slot wins ties), writes best slot / score and,
+//    optionally, the K edge scores.
+//
+// Warp path (any K <= 256, R <= 512, fp32 or bf16 codebooks): one warp per
+// (transition, predecessor); lanes split R, the gate stays in registers, and
+// each candidate's dot product is reduced with warp shuffles.  This is the
+// exact-fp32 path.
+#include <cuda_bf16.h>
+
+#include "dflash2.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace df2 {
+namespace {
+
+struct EParams {
+    const int32_t* cand_ids;
+    const float* u;
+    const void* A;
+    const void* B;
+    const float* unary;
+    int S, n, K, R, V;
+    int E;  // transitions = S * (n - 1)
+    float* edges_out;
+    int32_t* best_slot;
+    float* best_score;
+    int32_t* err_flag;
+};
+
+__device__ __forceinline__ int checked_id(int id, int V, bool& bad) {
+    if (id < 0 || id >= V) {
+        bad = true;
+        return id < 0 ? 0 : V - 1;
+    }
+    return id;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// ------------------------------------------------------------------ tile path
+
+constexpr int TROWS = 128;
+constexpr int KB_BYTES = TROWS * 128;  // one 64-element k-block of 128 rows
+
+template <int KB>
+struct TileSmem {
+    static constexpr size_t op_bytes = (size_t)KB * KB_BYTES;
+    static constexpr size_t used = 1024 /*align*/ + 2 * op_bytes + TROWS * 4 * 2 /*ids*/ + 64;
+    // Never fewer than ~60 KB per CTA: at most 3 CTAs share an SM, so their
+    // 3 x 128 TMEM columns always fit in the SM's 512.
+    static constexpr size_t total = used < 61440 ? 61440 : used;
+};
+
+template <int KB>
+__global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* opA = smem;
+    uint8_t* opB = smem + TileSmem<KB>::op_bytes;
+    int32_t* ids_p = reinterpret_cast<int32_t*>(opB + TileSmem<KB>::op_bytes);
+    int32_t* ids_c = ids_p + TROWS;
+    const int K = p.K;
+    const int R = p.R;
+    const int TP = TROWS / K;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(ids_c + TROWS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int e0 = blockIdx.x * TP;
+    const int nm1 = p.n - 1;
+    bool bad = false;
+
+    // 1. ids of this tile's 128 predecessor rows and 128 candidate rows
+    {
+        const int e = e0 + tid / K;
+        const int slot = tid % K;
+        int idp = 0, idc = 0;
+        if (e < p.E) {
+            const int s = e / nm1;
+            const int i = e % nm1 + 1;
+            idp = checked_id(p.cand_ids[((size_t)s * p.n + i - 1) * K + slot], p.V, bad);
+            idc = checked_id(p.cand_ids[((size_t)s * p.n + i) * K + slot], p.V, bad);
+        }
+        ids_p[tid] = idp;
+        ids_c[tid] = idc;
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(mbar), 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // 2. gather rows into the swizzled operand tiles (gate on the A side)
+    constexpr int CPR = KB * 8;  // 16-byte chunks per (padded) row
+    const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
+    const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
+    const uint32_t sA = smem_u32(opA);
+    const uint32_t sB = smem_u32(opB);
+    constexpr int BATCH = 8;
+#pragma unroll 1
+    for (int j0 = 0; j0 < CPR; j0 += BATCH) {
+        uint4 av[BATCH], bv[BATCH];
+        float4 u0[BATCH], u1[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int slot = (j0 + j) * 128 + tid;
+            const int row = slot / CPR;
+            const int ch = slot % CPR;
+            const int e = e0 + row / K;
+            if (ch * 8 < R && e < p.E) {
+                const int s = e / nm1;
+                const int i = e % nm1 + 1;
+                const float4* ur =
+                    reinterpret_cast<const float4*>(p.u + ((size_t)s * p.n + i) * R + ch * 8);
+                av[j] = ldg_nc_v4(A + (size_t)ids_p[row] * R + ch * 8);
+                bv[j] = ldg_nc_v4(B + (size_t)ids_c[row] * R + ch * 8);
+                u0[j] = __ldg(ur);
+                u1[j] = __ldg(ur + 1);
+            } else {
+                av[j] = make_uint4(0, 0, 0, 0);
+                bv[j] = make_uint4(0, 0, 0, 0);
+                u0[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                u1[j] = u0[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int slot = (j0 + j) * 128 + tid;
+            const int row = slot / CPR;
+            const int ch = slot % CPR;
+            const uint32_t off = (uint32_t)((ch >> 3) * KB_BYTES + row * 128 +
+                                            (((ch & 7) ^ (row & 7)) << 4));
+            uint4 g;
+            {
+                const float2 a0 = bf16x2_to_f2(av[j].x), a1 = bf16x2_to_f2(av[j].y);
+                const float2 a2 = bf16x2_to_f2(av[j].z), a3 = bf16x2_to_f2(av[j].w);
+                g.x = f2_to_bf16x2(a0.x * u0[j].x, a0.y * u0[j].y);
+                g.y = f2_to_bf16x2(a1.x * u0[j].z, a1.y * u0[j].w);
+                g.z = f2_to_bf16x2(a2.x * u1[j].x, a2.y * u1[j].y);
+                g.w = f2_to_bf16x2(a3.x * u1[j].z, a3.y * u1[j].w);
+            }
+            st_shared_v4(sA + off, g);
+            st_shared_v4(sB + off, bv[j]);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // 3. one thread issues the contraction over R
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+        const int ksteps = (R + 15) / 16;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t koff = (uint32_t)((ks >> 2) * KB_BYTES + (ks & 3) * 32);
+            tc_mma_bf16(tmem, sw128_desc(sA + koff), sw128_desc(sB + koff), idesc,
+                        ks > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(mbar));
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(smem_u32(mbar), 0, kWaitPolls);
+    tc_fence_after();
+
+    // 4. epilogue: this thread's predecessor row, its transition's K columns
+    const int r = tid;
+    const int e = e0 + r / K;
+    const int pslot = r % K;
+    const int blk0 = K * (r / K);                       // first column of the block
+    const int colbase = K >= 32 ? blk0 : 32 * warp;     // warp-uniform
+    const int width = K >= 32 ? K : 32;
+    int s = 0, i = 1;
+    if (e < p.E) {
+        s = e / nm1;
+        i = e % nm1 + 1;
+    }
+    const float* un = p.unary + ((size_t)s * p.n + i) * K;
+    float* erow = p.edges_out != nullptr ? p.edges_out + ((size_t)e * K + pslot) * K : nullptr;
+    float best = 0.f;
+    int arg = 0;
+#pragma unroll 1
+    for (int cc = 0; cc < width; cc += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(colbase + cc), v);
+        tmem_ld_wait();
+        if (e < p.E) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int c = colbase + cc + j - blk0;
+                if (c >= 0 && c < K) {
+                    const float ev = __uint_as_float(v[j]) + un[c];
+                    if (erow != nullptr) erow[c] = ev;
+                    if (c == 0 || ev > best) {
+                        best = ev;
+                        arg = c;
+                    }
+                }
+            }
+        }
+    }
+    if (e < p.E) {
+        p.best_slot[(size_t)e * K + pslot] = arg;
+        p.best_score[(size_t)e * K + pslot] = best;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+    if (p.err_flag != nullptr) {
+        int flags = (bad ? DF2_FLAG_BAD_ID : 0) | (ok ? 0 : DF2_FLAG_TIMEOUT);
+        if (flags) atomicOr(p.err_flag, flags);
+    }
+}
+
+// ------------------------------------------------------------------ warp path
+
+template <typename TCB>
+__device__ __forceinline__ float cb_load(const TCB* p);
+template <>
+__device__ __forceinline__ float cb_load<float>(const float* p) {
+    return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float cb_load<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+}
+
+constexpr int WARP_MAXJ = 16;  // R <= 512
+
+template <typename TCB>
+__global__ void __launch_bounds__(256) edges_warp_kernel(const EParams p) {
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gw >= (long long)p.E * p.K) return;
+    const int K = p.K;
+    const int R = p.R;
+    const int e = (int)(gw / K);
+    const int pslot = (int)(gw % K);
+    const int nm1 = p.n - 1;
+    const int s = e / nm1;
+    const int i = e % nm1 + 1;
+    const TCB* A = static_cast<const TCB*>(p.A);
+    const TCB* B = static_cast<const TCB*>(p.B);
+    bool bad = false;
+    const int idp = checked_id(p.cand_ids[((size_t)s * p.n + i - 1) * K + pslot], p.V, bad);
+    const float* urow = p.u + ((size_t)s * p.n + i) * R;
+    float g[WARP_MAXJ];
+#pragma unroll
+    for (int j = 0; j < WARP_MAXJ; ++j) {
+        const int r = lane + 32 * j;
+        g[j] = r < R ? cb_load(A + (size_t)idp * R + r) * urow[r] : 0.f;
+    }
+    const int32_t* cands = p.cand_ids + ((size_t)s * p.n + i) * K;
+    const float* un = p.unary + ((size_t)s * p.n + i) * K;
+    float* erow = p.edges_out != nullptr ? p.edges_out + ((size_t)e * K + pslot) * K : nullptr;
+    float best = 0.f;
+    int arg = 0;
+    for (int c = 0; c < K; ++c) {
+        const int idc = checked_id(cands[c], p.V, bad);
+        const TCB* brow = B + (size_t)idc * R;
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < WARP_MAXJ; ++j) {
+            const int r = lane + 32 * j;
+            if (r < R) part = fmaf(g[j], cb_load(brow + r), part);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
+        const float ev = part + un[c];
+        if (erow != nullptr && lane == 0) erow[c] = ev;
+        if (c == 0 || ev > best) {
+            best = ev;
+            arg = c;
+        }
+    }
+    if (lane == 0) {
+        p.best_slot[(size_t)e * K + pslot] = arg;
+        p.best_score[(size_t)e * K + pslot] = best;
+        if (bad && p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_BAD_ID);
+    }
+}
+
+EParams make_params(const EdgesArgs& a) {
+    EParams p{};
+    p.cand_ids = a.cand_ids;
+    p.u = a.u;
+    p.A = a.A;
+    p.B = a.B;
+    p.unary = a.unary;
+    p.S = a.S;
+    p.n = a.n;
+    p.K = a.K;
+    p.R = a.R;
+    p.V = a.V;
+    p.E = a.S * (a.n - 1);
+    p.edges_out = a.edges_out;
+    p.best_slot = a.best_slot;
+    p.best_score = a.best_score;
+    p.err_flag = a.err_flag;
+    return p;
+}
+
+template <int KB>
+cudaError_t launch_tc(const EParams& p, cudaStream_t stream) {
+    const int TP = TROWS / p.K;
+    const size_t smem = TileSmem<KB>::total;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static unsigned set_mask[KB + 1] = {};
+    if (dev < 32 && !(set_mask[KB] & (1u << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(edges_tc_kernel<KB>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)TileSmem<KB>::total);
+        if (e != cudaSuccess) return e;
+        set_mask[KB] |= 1u << dev;
+    }
+    const int tiles = (p.E + TP - 1) / TP;
+    edges_tc_kernel<KB><<<tiles, 128, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool edges_tc_supported(int K, int R) {
+    return K >= 1 && K <= 128 && (K & (K - 1)) == 0 && R % 8 == 0 && R <= 384;
+}
+
+cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, cudaStream_t stream) {
+    const EParams p = make_params(a);
+    if (p.E <= 0) return cudaSuccess;
+    switch ((a.R + 63) / 64) {
+        case 1:
+            return launch_tc<1>(p, stream);
+        case 2:
+            return launch_tc<2>(p, stream);
+        case 3:
+            return launch_tc<3>(p, stream);
+        case 4:
+            return launch_tc<4>(p, stream);
+        case 5:
+            return launch_tc<5>(p, stream);
+        case 6:
+            return launch_tc<6>(p, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_edges_warp(const EdgesArgs& a, int cb_bf16, cudaStream_t stream) {
+    const EParams p = make_params(a);
+    if (p.E <= 0) return cudaSuccess;
+    const long long warps = (long long)p.E * p.K;
+    const long long blocks = (warps + 7) / 8;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+    if (cb_bf16)
+        edges_warp_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else
+        edges_warp_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace df2

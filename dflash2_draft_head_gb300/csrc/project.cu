@@ -1,0 +1,305 @@
+// project(h): u = h W^T, the dense d -> R projection of each position's hidden
+// state (ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local
+// convolution + candidate selector)", Overview: the position's hidden state is
+// projected to the codebook rank; weight tensor "selector_hidden").
+//
+// bf16 path (tcgen05, one GB300 SM per CTA):
+//  - output tile 128 (rows of h) x 128 (columns of u) accumulated in fp32 in
+//    tensor memory (128 TMEM columns);
+//  - K (= d) is split across the CTAs of a thread-block cluster (split-K);
+//    every CTA streams its K range through a 6-stage TMA pipeline of
+//    128x64 bf16 tiles of h and W, stored in the 128-byte-swizzle K-major
+//    layout that the tensor core reads directly;
+//  - one thread issues tcgen05.mma (M=128, N=128, K=16) and frees a stage with
+//    tcgen05.commit; one thread drives TMA;
+//  - epilogue: tcgen05.ld of the partial tile into the CTA's shared memory,
+//    a cluster barrier, then CTA r sums rows [r*128/split, (r+1)*128/split)
+//    over all CTAs of the cluster through distributed shared memory in a
+//    fixed order (deterministic) and writes fp32 u.  No global workspace.
+// The thin-N GEMM (R = 128..256) is HBM-bound on h when h is cold, so the
+// pipeline is sized for bandwidth, not for tensor throughput.
+//
+// fp32 path: a shared-memory tiled FFMA kernel (exact fp32, no TF32).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dflash2.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace df2 {
+
+// Device-side fault word of the projection kernel (one per device): DF2_FLAG_*
+// bits are ORed here when a bounded wait gives up.
+__device__ unsigned int g_fault_word = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int RED_STRIDE = BN + 4;  // padded fp32 row of the reduction buffer
+constexpr int NTHREADS = 128;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+static_assert((size_t)BM * RED_STRIDE * 4 <= (size_t)STAGES * STAGE_BYTES, "reduction buffer");
+
+struct ProjParams {
+    float* u;
+    int P, R;
+    int kblocks;
+    int splitk;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    project_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const ProjParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + STAGES);
+    const uint32_t accum = smem_u32(bars + 2 * STAGES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int m_tile = blockIdx.y;
+    const int n_tile = blockIdx.z;
+    const int kb0 = (int)((long long)rank * p.kblocks / p.splitk);
+    const int kb1 = (int)((long long)(rank + 1) * p.kblocks / p.splitk);
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(accum, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), BN);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = true;
+
+    if (warp == 0 && lane == 0) {
+        // TMA producer
+        for (int it = 0; it < nkb; ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitPolls)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = full0 + 8 * s;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t dst = smem_u32(stages + (size_t)s * STAGE_BYTES);
+            const int kx = (kb0 + it) * BK;
+            tma_load_2d(dst, &tmA, fb, kx, m_tile * BM);
+            tma_load_2d(dst + A_BYTES, &tmB, fb, kx, n_tile * BN);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        for (int it = 0; it < nkb; ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+            if (!mbar_wait_bounded(full0 + 8 * s, ph, kWaitPolls)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(stages + (size_t)s * STAGE_BYTES);
+            const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+                tc_mma_bf16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc,
+                            (it > 0 || k > 0) ? 1u : 0u);
+            tc_commit(empty0 + 8 * s);
+        }
+        tc_commit(accum);
+    }
+    __syncwarp();
+
+    // Epilogue: partial tile TMEM -> shared memory (stage buffers are free once
+    // the accumulator barrier fires: every issued load was consumed by an MMA).
+    if (!mbar_wait_bounded(accum, 0, kWaitPolls)) ok = false;
+    tc_fence_after();
+    float* red = reinterpret_cast<float*>(stages);
+    const int row = warp * 32 + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld_wait();
+        float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+    }
+    tc_fence_before();
+    cluster_sync();
+
+    // Deterministic split-K reduction across the cluster.
+    const int rows_per = BM / p.splitk;
+    const int r_base = (int)rank * rows_per;
+    const int nvec = rows_per * (BN / 4);
+    const uint32_t red_s = smem_u32(red);
+    for (int q = threadIdx.x; q < nvec; q += NTHREADS) {
+        const int rr = r_base + q / (BN / 4);
+        const int cc = (q % (BN / 4)) * 4;
+        const uint32_t off = red_s + (uint32_t)((rr * RED_STRIDE + cc) * 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int src = 0; src < p.splitk; ++src) {
+            const float4 v = ld_cluster_f4(map_cluster(off, (uint32_t)src));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const int grow = m_tile * BM + rr;
+        const int gcol = n_tile * BN + cc;
+        if (grow < p.P && gcol < p.R)
+            *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
+    }
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+    if (!ok) atomicOr(&g_fault_word, (unsigned)DF2_FLAG_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128 B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- fp32 path
+
+constexpr int FT = 16;  // 16x16 outputs per block, K chunks of 32
+
+__global__ void __launch_bounds__(256) project_f32_kernel(const float* __restrict__ h,
+                                                          const float* __restrict__ W,
+                                                          float* __restrict__ u, int P, int d,
+                                                          int R) {
+    __shared__ float hs[FT][33];
+    __shared__ float ws[FT][33];
+    const int tx = threadIdx.x % FT;  // output column within the tile
+    const int ty = threadIdx.x / FT;  // output row within the tile
+    const int r0 = blockIdx.y * FT;
+    const int k0 = blockIdx.x * FT;
+    float acc = 0.f;
+    for (int j0 = 0; j0 < d; j0 += 32) {
+        for (int q = threadIdx.x; q < FT * 32; q += 256) {
+            const int rr = q / 32, jj = q % 32;
+            const int j = j0 + jj;
+            hs[rr][jj] = (r0 + rr < P && j < d) ? h[(size_t)(r0 + rr) * d + j] : 0.f;
+            ws[rr][jj] = (k0 + rr < R && j < d) ? W[(size_t)(k0 + rr) * d + j] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) acc = fmaf(hs[ty][jj], ws[tx][jj], acc);
+        __syncthreads();
+    }
+    if (r0 + ty < P && k0 + tx < R) u[(size_t)(r0 + ty) * R + k0 + tx] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms) {
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, a.h, a.P, a.d, BM) || !make_map(&tmB, a.W, a.R, a.d, BN))
+        return cudaErrorInvalidValue;
+    const int kblocks = (a.d + BK - 1) / BK;
+    const int m_tiles = (a.P + BM - 1) / BM;
+    const int n_tiles = (a.R + BN - 1) / BN;
+    const int tiles = m_tiles * n_tiles;
+    // split-K factor: a power of two <= 8 (portable cluster size) that fills
+    // the SMs without exceeding them and leaves every CTA at least 2 k-blocks.
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= num_sms && kblocks >= split * 4) split *= 2;
+
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static unsigned attr_mask = 0;
+    if (dev >= 32 || !(attr_mask & (1u << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(project_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev < 32) attr_mask |= 1u << dev;
+    }
+    ProjParams p{a.u, a.P, a.R, kblocks, split};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)split, (unsigned)m_tiles, (unsigned)n_tiles);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, project_tc_kernel, tmA, tmB, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t take_project_faults(unsigned* flags) {
+    unsigned v = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(zero));
+    *flags = v;
+    return e;
+}
+
+cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream) {
+    dim3 grid((unsigned)((a.R + FT - 1) / FT), (unsigned)((a.P + FT - 1) / FT));
+    project_f32_kernel<<<grid, 256, 0, stream>>>(static_cast<const float*>(a.h),
+                                                 static_cast<const float*>(a.W), a.u, a.P, a.d,
+                                                 a.R);
+    return cudaGetLastError();
+}
+
+}  // namespace df2

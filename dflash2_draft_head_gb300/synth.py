@@ -96,15 +96,19 @@ def cand_rows(seed: int, s: int, lo: int, hi: int, K: int, V: int,
         rows_n = min(CHUNK, n_total - ch * CHUNK)
         ids = torch.randint(0, V, (rows_n, K), generator=g, dtype=torch.int64)
         gfix = _gen(seed, _TAG["cand_fix"], s, ch)
-        while True:
+        for attempt in range(9):
             srt, _ = torch.sort(ids, dim=1)
             dup = (srt[:, 1:] == srt[:, :-1]).any(dim=1) if K > 1 else \
                 torch.zeros(rows_n, dtype=torch.bool)
             rows = torch.nonzero(dup).flatten()
             if rows.numel() == 0:
                 break
-            ids[rows] = torch.randint(0, V, (rows.numel(), K), generator=gfix,
-                                      dtype=torch.int64)
+            if attempt < 8:
+                ids[rows] = torch.randint(0, V, (rows.numel(), K), generator=gfix,
+                                          dtype=torch.int64)
+            else:  # K close to V: draw the remaining rows without replacement
+                for r in rows.tolist():
+                    ids[r] = torch.randperm(V, generator=gfix)[:K]
         a = max(lo, ch * CHUNK) - ch * CHUNK
         b = min(hi, (ch + 1) * CHUNK) - ch * CHUNK
         parts.append(ids[a:b])

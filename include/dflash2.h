@@ -1,0 +1,161 @@
+/*
+ * dflash2.h: C ABI of the DFlash2 draft-head hot path on NVIDIA GB300 (sm_103a).
+ *
+ * The operations are the two formulas of ggml-org/llama.cpp pull request
+ * #27342, "spec : add DFlash2 support (local convolution + candidate
+ * selector)", section "Overview":
+ *
+ *   grouped dynamic depthwise causal convolution
+ *     out[i,c] = sum_t (base[t,c] + delta[i,t,g(c)]) * x[i-t,c]
+ *   candidate-selector edge score
+ *     edge(p->c) = < A[p] (.) project(h), B[c] > + unary[c]
+ *
+ * with the codebooks A ("selector_predecessor"), B ("selector_successor") and
+ * the projection weight ("selector_hidden") named in that thread's review.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *     16-byte aligned.  The caller allocates and owns them; the library never
+ *     allocates, frees or keeps a pointer past the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call only enqueues work on that stream and returns; it never
+ *     synchronises the host.
+ *   - Return value: a df2_status.  DF2_ERR_INVALID_ARG / DF2_ERR_UNSUPPORTED are
+ *     detected on the host before anything is enqueued (nothing is launched).
+ *     DF2_ERR_CUDA reports a launch error (cudaGetLastError); a fault inside a
+ *     kernel surfaces at the caller's next synchronisation as usual.
+ *   - dflash2_last_error() returns a thread-local text for the last non-OK
+ *     status of the calling thread.
+ *   - dtype codes: DF2_F32 (every float input fp32, fp32 accumulation and
+ *     output, no TF32 anywhere) or DF2_BF16 (bf16 inputs, fp32 accumulation).
+ */
+#ifndef DFLASH2_H_
+#define DFLASH2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DF2_OK = 0,
+    DF2_ERR_INVALID_ARG = 1,  /* bad size, NULL required pointer, misalignment, aliasing */
+    DF2_ERR_UNSUPPORTED = 2,  /* legal arguments outside what the kernels implement */
+    DF2_ERR_CUDA = 3          /* a CUDA runtime error at launch */
+} df2_status;
+
+typedef enum { DF2_F32 = 0, DF2_BF16 = 1 } df2_dtype;
+
+/* Bits a kernel ORs into a caller-provided device err_flag (int32). */
+#define DF2_FLAG_BAD_ID 1    /* a candidate id outside [0, V): it was clamped for the load */
+#define DF2_FLAG_TIMEOUT 2   /* a bounded on-chip wait gave up; outputs of that tile are undefined */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int dflash2_version(void);
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* dflash2_status_string(int status);
+
+/* Detail text for the calling thread's last non-OK status ("" if none). */
+const char* dflash2_last_error(void);
+
+/*
+ * Grouped dynamic depthwise causal convolution (PR #27342, Overview, first
+ * formula).  For s < S, i < n, c < C:
+ *   out[s,i,c] = sum_{t=0}^{T-1} (base[t,c] + delta[s,i,t,g(c)]) * xh[s,i-t,c]
+ * where g(c) = c / (C/G) (contiguous groups) and xh[s,j,c] = x[s,j,c] for
+ * j >= 0, hist[s,T-1+j,c] for -(T-1) <= j < 0 (oldest history row first; row
+ * T-2 is the position just before the block).
+ *
+ *   x      [S,n,C]    in_dtype
+ *   hist   [S,T-1,C]  in_dtype, or NULL for an all-zero history
+ *   base   [T,C]      in_dtype
+ *   delta  [S,n,T,G]  in_dtype
+ *   out    [S,n,C]    out_dtype; must not overlap x, hist, base or delta
+ *
+ * Accumulation is fp32; a bf16 output is rounded to nearest even once.
+ * INVALID_ARG: S,n,C,T,G <= 0; C % G != 0; NULL x/base/delta/out; pointer not
+ * 16-byte aligned; out overlapping an input.
+ * UNSUPPORTED: C % 8 != 0 or (C/G) % 8 != 0 (8-channel vectors); T > 16;
+ * in_dtype F32 with out_dtype BF16.
+ */
+int dflash2_dynconv(const void* x, const void* hist, const void* base, const void* delta,
+                    void* out, int S, int n, int C, int T, int G,
+                    int in_dtype, int out_dtype, void* stream);
+
+/*
+ * project(h): the dense d -> R map of each position's hidden state (PR
+ * #27342, Overview: the hidden state is projected to the codebook rank; its
+ * weight tensor is "selector_hidden").
+ *   u[r,k] = sum_j h[r,j] * W[k,j]          (u = h W^T)
+ *
+ *   h  [P,d]  in_dtype
+ *   W  [R,d]  in_dtype (K-major: each output column's weights are contiguous)
+ *   u  [P,R]  fp32
+ *
+ * BF16 runs on the tcgen05 tensor cores (TMA-fed, fp32 accumulation in tensor
+ * memory, split-K reduced deterministically through distributed shared memory
+ * within a thread-block cluster).  F32 runs on the FP32 pipes.
+ * INVALID_ARG: P,d,R <= 0; NULL pointer; misalignment.
+ * UNSUPPORTED: d % 8 != 0; R % 8 != 0 or R > 512.
+ */
+int dflash2_project(const void* h, const void* W, float* u, int P, int d, int R,
+                    int in_dtype, void* stream);
+
+/*
+ * Edge scores with the fused per-predecessor argmax (PR #27342, Overview,
+ * second formula).  For s < S, position i in 1..n-1 (the candidates of
+ * position i-1 are the predecessors), slots p, c < K:
+ *   e[s,i-1,p,c] = sum_r A[id_p,r] * u[s*n+i,r] * B[id_c,r] + unary[s,i,c]
+ *   id_p = cand_ids[s,i-1,p],  id_c = cand_ids[s,i,c]
+ *   best_slot[s,i-1,p]  = lowest c reaching max_c e[s,i-1,p,c]
+ *   best_score[s,i-1,p] = that maximum
+ *
+ *   cand_ids   [S,n,K]        int32 token ids in [0,V)
+ *   u          [S*n,R]        fp32 (the output of dflash2_project)
+ *   A, B       [V,R]          cb_dtype codebooks
+ *   unary      [S,n,K]        fp32
+ *   edges_out  [S,n-1,K,K]    fp32, or NULL to skip writing the edge matrix
+ *   best_slot  [S,n-1,K]      int32
+ *   best_score [S,n-1,K]      fp32
+ *   err_flag   one device int32 or NULL; DF2_FLAG_* bits are ORed into it
+ *              (the caller zeroes it and reads it after its own sync).
+ *
+ * n == 1 has no transitions: returns DF2_OK having launched nothing.
+ * An id outside [0,V) is clamped into range for the load and flagged
+ * (DF2_FLAG_BAD_ID); the kernel never traps.  In BF16 mode the gate
+ * A[id_p] (.) u is rounded to bf16 before the tensor-core contraction.
+ * INVALID_ARG: S,n,K,R,V <= 0; NULL required pointer; misalignment.
+ * UNSUPPORTED: K > 256; R % 8 != 0 or R > 512.
+ */
+int dflash2_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,
+                  const float* unary, int S, int n, int K, int R, int V, int cb_dtype,
+                  float* edges_out, int32_t* best_slot, float* best_score,
+                  int32_t* err_flag, void* stream);
+
+/*
+ * The composite selector: dflash2_project of every position's hidden state
+ * into u_out, then dflash2_edges, both enqueued on `stream`.
+ *   h [S*n,d], W [R,d] in `dtype`; A, B [V,R] in `dtype`; u_out [S*n,R] fp32
+ *   (caller-owned: it carries the projection between the two kernels).
+ * Other arguments and errors as for the two calls it makes.
+ */
+int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const void* A,
+                   const void* B, const float* unary, int S, int n, int d, int K, int R,
+                   int V, int dtype, float* u_out, float* edges_out, int32_t* best_slot,
+                   float* best_score, int32_t* err_flag, void* stream);
+
+/*
+ * Reads and clears the library's device-side fault word for the current
+ * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_project gave
+ * up).  Synchronises the current device.  Returns DF2_OK or DF2_ERR_CUDA.
+ */
+int dflash2_take_device_faults(int32_t* flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H_ */

@@ -1,0 +1,123 @@
+"""The C ABI library builds, loads and exports every declared entry point; host-side
+argument validation rejects bad calls before anything is launched (CPU only:
+every call here fails validation, so no CUDA work is issued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dflash2_draft_head_gb300 import binding, build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash2.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash2_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    return binding.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(L):
+    assert L.dflash2_version() >= 100
+    for code, name in [(0, b"DF2_OK"), (1, b"DF2_ERR_INVALID_ARG"), (2, b"DF2_ERR_UNSUPPORTED"),
+                       (3, b"DF2_ERR_CUDA")]:
+        assert L.dflash2_status_string(code) == name
+    assert L.dflash2_status_string(99) == b"DF2_UNKNOWN_STATUS"
+
+
+# fake, 16-byte aligned, non-overlapping addresses: only ever passed to calls
+# that must fail validation before any launch
+P = [ctypes.c_void_p(0x10000000 * (k + 1)) for k in range(12)]
+NULL = None
+
+
+def _dyn(L, x=P[0], hist=P[1], base=P[2], delta=P[3], out=P[4], S=2, n=8, C=64, T=4, G=4,
+         di=1, do=1):
+    return L.dflash2_dynconv(x, hist, base, delta, out, S, n, C, T, G, di, do, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=NULL), 1), (dict(out=NULL), 1), (dict(base=NULL), 1), (dict(delta=NULL), 1),
+    (dict(S=0), 1), (dict(n=-1), 1), (dict(C=0), 1), (dict(T=0), 1), (dict(G=0), 1),
+    (dict(C=64, G=5), 1), (dict(di=7), 1), (dict(x=ctypes.c_void_p(0x10000008)), 1),
+    (dict(out=P[0]), 1),                       # out aliases x
+    (dict(C=60, G=4), 2),                      # C % 8
+    (dict(C=64, G=16), 2),                     # C/G = 4
+    (dict(T=17), 2), (dict(di=0, do=1), 2),
+])
+def test_dynconv_validation(L, kw, code):
+    assert _dyn(L, **kw) == code
+    assert L.dflash2_last_error()
+
+
+def test_dynconv_hist_overlapping_out_is_rejected(L):
+    # hist [2,3,64] bf16 = 768 B placed 256 B before out: overlaps
+    out = ctypes.c_void_p(0x50000000)
+    hist = ctypes.c_void_p(0x50000000 - 256)
+    assert _dyn(L, hist=hist, out=out) == 1
+
+
+def _proj(L, h=P[0], W=P[1], u=P[2], Pn=16, d=64, R=16, dt=1):
+    return L.dflash2_project(h, W, u, Pn, d, R, dt, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=NULL), 1), (dict(u=NULL), 1), (dict(Pn=0), 1), (dict(d=0), 1), (dict(R=0), 1),
+    (dict(dt=3), 1), (dict(u=P[0]), 1), (dict(W=ctypes.c_void_p(0x20000004)), 1),
+    (dict(R=12), 2), (dict(R=520), 2), (dict(d=36), 2),
+])
+def test_project_validation(L, kw, code):
+    assert _proj(L, **kw) == code
+
+
+def _edges(L, ids=P[0], u=P[1], A=P[2], B=P[3], un=P[4], S=2, n=4, K=4, R=16, V=100, dt=1,
+           eo=P[5], bs=P[6], bsc=P[7], flag=P[8]):
+    return L.dflash2_edges(ids, u, A, B, un, S, n, K, R, V, dt, eo, bs, bsc, flag, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ids=NULL), 1), (dict(A=NULL), 1), (dict(bs=NULL), 1), (dict(bsc=NULL), 1),
+    (dict(S=0), 1), (dict(K=0), 1), (dict(V=0), 1), (dict(R=-8), 1), (dict(dt=2), 1),
+    (dict(bs=P[0]), 1), (dict(eo=P[2]), 1), (dict(bsc=P[6]), 1),
+    (dict(flag=ctypes.c_void_p(0x90000002)), 1),
+    (dict(K=257), 2), (dict(R=20), 2), (dict(R=528), 2),
+])
+def test_edges_validation(L, kw, code):
+    assert _edges(L, **kw) == code
+
+
+def test_select_validation(L):
+    args = [P[0], P[1], P[2], P[3], P[4], P[5], 2, 4, 64, 4, 16, 100, 1, P[6], P[7], P[8], P[9],
+            P[10], None]
+    a = list(args)
+    a[13] = P[0]  # u_out aliases h
+    assert L.dflash2_select(*a) == 1
+    a = list(args)
+    a[13] = P[3]  # u_out aliases A
+    assert L.dflash2_select(*a) == 1
+    a = list(args)
+    a[6] = 0
+    assert L.dflash2_select(*a) == 1
+    a = list(args)
+    a[10] = 12
+    assert L.dflash2_select(*a) == 2
+
+
+def test_take_device_faults_rejects_null(L):
+    assert L.dflash2_take_device_faults(None) == 1
