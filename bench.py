@@ -62,6 +62,22 @@ def _env():
     return rank, world, local
 
 
+def rank_workload(w0, rank):
+    """The workload a rank runs: same shapes, its own sequences (seed offset by rank)."""
+    return dataclasses.replace(w0, seed=w0.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a host float over all ranks (a measurement reduction, not a data path)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _workload(name):
     from dflash2_draft_head_gb300.workloads import BENCH_WORKLOAD, BY_NAME
     return BY_NAME[name] if name else BENCH_WORKLOAD
@@ -286,7 +302,7 @@ def main():
     if world > 1:
         tdist.init_process_group("nccl", device_id=dev)
     w0 = _workload(args.workload)
-    w = dataclasses.replace(w0, seed=w0.seed + 1000 * rank)  # each rank its own sequences
+    w = rank_workload(w0, rank)
 
     bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     ci = synth.conv_inputs(w)
@@ -366,11 +382,7 @@ def main():
     t_proj = [e[1].elapsed_time(e[2]) for e in ev]
     t_edge = [e[2].elapsed_time(e[3]) for e in ev]
     t_step = [e[0].elapsed_time(e[3]) for e in ev]
-    total_ms = sum(t_step)
-    tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-    total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
 
@@ -399,10 +411,7 @@ def main():
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        tdist.all_reduce(e2e_ms, op=tdist.ReduceOp.MAX)
-    e2e_ms = float(e2e_ms.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     positions = w.S * w.n * world
     value = positions * K / (total_ms / 1000.0)

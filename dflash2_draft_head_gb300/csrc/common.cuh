@@ -8,8 +8,8 @@
 
 namespace df2 {
 
-// Upper bound of polls of one bounded mbarrier wait before a kernel gives up.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Longest time one on-chip wait may take before a kernel gives up (200 ms).
+constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
 
 struct DynconvArgs {
     const void* x;

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
         tc_commit(smem_u32(mbar));
     }
     __syncwarp();
-    const bool ok = mbar_wait_bounded(smem_u32(mbar), 0, kWaitPolls);
+    const bool ok = mbar_wait_bounded(smem_u32(mbar), 0, kWaitNs);
     tc_fence_after();
 
     // 4. epilogue: this thread's predecessor row, its transition's K columns

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int it = 0; it < nkb; ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitPolls)) {
+            if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitNs)) {
                 ok = false;
                 break;
             }
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int it = 0; it < nkb; ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-            if (!mbar_wait_bounded(full0 + 8 * s, ph, kWaitPolls)) {
+            if (!mbar_wait_bounded(full0 + 8 * s, ph, kWaitNs)) {
                 ok = false;
                 break;
             }
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // Epilogue: partial tile TMEM -> shared memory (stage buffers are free once
     // the accumulator barrier fires: every issued load was consumed by an MMA).
-    if (!mbar_wait_bounded(accum, 0, kWaitPolls)) ok = false;
+    if (!mbar_wait_bounded(accum, 0, kWaitNs)) ok = false;
     tc_fence_after();
     float* red = reinterpret_cast<float*>(stages);
     const int row = warp * 32 + lane;
