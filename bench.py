@@ -52,6 +52,7 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     return ap.parse_args()
 
 
@@ -87,7 +88,8 @@ def _config(w, world):
     return {"workload": w.name, "S": w.S, "n": w.n, "C": w.C, "T": w.T, "G": w.G, "d": w.d,
             "R": w.R, "V": w.V, "K": w.K, "selector_S": w.S_sel, "selector_n": w.n_sel,
             "in_dtype": w.dtype, "out_dtype": w.dtype,
-            "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write)",
+            "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write, then "
+                  f"{FLUSH_BYTES >> 20} MiB read)",
             "parallelism": f"replicas x{world} (independent sequences per GPU)"}
 
 
@@ -282,6 +284,107 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 
+class L2Flush:
+    """Evicts L2 between timed steps: write one buffer larger than L2, then read
+    another, so that L2 ends full of clean lines (no write-back is left for the
+    next timed kernel to pay)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+def _event_record_external():
+    """cudaEventRecordWithFlags(..., cudaEventRecordExternal) of the CUDA runtime torch
+    loaded (timing events inside a captured graph), or None."""
+    import ctypes
+    path = None
+    try:
+        for line in open("/proc/self/maps"):
+            if "libcudart.so" in line:
+                path = line.split()[-1]
+                break
+    except OSError:
+        return None
+    if path is None:
+        return None
+    try:
+        f = ctypes.CDLL(path).cudaEventRecordWithFlags
+    except (OSError, AttributeError):
+        return None
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _call(f, a, L):
+    if f(*a):
+        raise RuntimeError(L.dflash2_last_error().decode())
+
+
+def _timed_graph(K, stream, flush, conv, proj, edge, record_ext, L, per_graph=50):
+    """K steps replayed from CUDA graphs: each step = L2 flush, then the three kernels
+    bracketed by timing events recorded as graph nodes.  Returns per-step kernel times."""
+    import ctypes
+
+    import torch
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    t_conv, t_proj, t_edge, t_step = [], [], [], []
+    done = 0
+    graphs = {}
+    while done < K:
+        M = min(per_graph, K - done)
+        if M not in graphs:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(M)]
+            for e4 in ev:
+                for e in e4:
+                    e.record(stream)  # materialise the event handles
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for m in range(M):
+                    flush.zero_()
+                    for j, (f, a) in enumerate((conv, proj, edge)):
+                        if record_ext(ctypes.c_void_p(ev[m][j].cuda_event), sp, 1):
+                            raise RuntimeError("event record in capture failed")
+                        _call(f, a, L)
+                    if record_ext(ctypes.c_void_p(ev[m][3].cuda_event), sp, 1):
+                        raise RuntimeError("event record in capture failed")
+            graphs[M] = (g, ev)
+        g, ev = graphs[M]
+        g.replay()
+        stream.synchronize()
+        for e in ev:
+            t_conv.append(e[0].elapsed_time(e[1]))
+            t_proj.append(e[1].elapsed_time(e[2]))
+            t_edge.append(e[2].elapsed_time(e[3]))
+            t_step.append(e[0].elapsed_time(e[3]))
+        done += M
+    return t_conv, t_proj, t_edge, t_step
+
+
+def _timed_eager(K, stream, flush, conv, proj, edge, L):
+    """K eagerly launched steps (fallback when graph timing events are unavailable)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
+    for k in range(K):
+        flush.zero_()
+        for j, (f, a) in enumerate((conv, proj, edge)):
+            ev[k][j].record(stream)
+            _call(f, a, L)
+        ev[k][3].record(stream)
+    stream.synchronize()
+    return ([e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev],
+            [e[2].elapsed_time(e[3]) for e in ev], [e[0].elapsed_time(e[3]) for e in ev])
+
+
 def main():
     args = _args()
     if args.impl == "reference":
@@ -323,7 +426,7 @@ def main():
     best_slot = torch.empty((max(E, 1), w.K), dtype=torch.int32, device=dev)
     best_score = torch.empty((max(E, 1), w.K), dtype=torch.float32, device=dev)
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.Stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
     code = 1 if w.dtype == "bf16" else 0
@@ -357,31 +460,23 @@ def main():
     barrier()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    record_ext = None if args.no_graph else _event_record_external()
     with ClockSampler(gpu_uuid) as clk:
         barrier()
         wall0 = time.perf_counter()
-        torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
-        for k in range(K):
-            flush.zero_()
-            e = ev[k]
-            e[0].record(stream)
-            if f_conv(*conv_args):
-                raise RuntimeError(L.dflash2_last_error().decode())
-            e[1].record(stream)
-            if f_proj(*proj_args):
-                raise RuntimeError(L.dflash2_last_error().decode())
-            e[2].record(stream)
-            if f_edge(*edge_args):
-                raise RuntimeError(L.dflash2_last_error().decode())
-            e[3].record(stream)
+        if record_ext is not None:
+            t_conv, t_proj, t_edge, t_step = _timed_graph(
+                K, stream, flush, (f_conv, conv_args), (f_proj, proj_args),
+                (f_edge, edge_args), record_ext, L)
+            mode = "cuda-graph"
+        else:
+            t_conv, t_proj, t_edge, t_step = _timed_eager(
+                K, stream, flush, (f_conv, conv_args), (f_proj, proj_args),
+                (f_edge, edge_args), L)
+            mode = "eager"
         barrier()
         wall = time.perf_counter() - wall0
-    t_conv = [e[0].elapsed_time(e[1]) for e in ev]
-    t_proj = [e[1].elapsed_time(e[2]) for e in ev]
-    t_edge = [e[2].elapsed_time(e[3]) for e in ev]
-    t_step = [e[0].elapsed_time(e[3]) for e in ev]
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -448,6 +543,7 @@ def main():
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
+        "launch_mode": mode,
         "cpu_baseline": None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

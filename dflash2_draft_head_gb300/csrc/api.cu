@@ -63,9 +63,12 @@ bool valid_dtype(int d) { return d == DF2_F32 || d == DF2_BF16; }
 size_t esize(int d) { return d == DF2_BF16 ? 2 : 4; }
 
 int num_sms_of_current_device() {
+    static int cached[64] = {0};
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64) cached[dev] = sms;
     return sms;
 }
 
@@ -96,9 +99,11 @@ int validate_edges(const int32_t* cand_ids, const float* u, const void* A, const
                    const float* unary, int S, int n, int K, int R, int V, int dtype,
                    const float* edges_out, const int32_t* best_slot, const float* best_score,
                    const int32_t* err_flag) {
-    if (cand_ids == nullptr || u == nullptr || A == nullptr || B == nullptr || unary == nullptr ||
-        best_slot == nullptr || best_score == nullptr)
+    if (cand_ids == nullptr || u == nullptr || A == nullptr || B == nullptr || unary == nullptr)
         return fail(DF2_ERR_INVALID_ARG, "edges: NULL required pointer");
+    // with a single position there are no transitions, so the outputs are empty
+    if (n > 1 && (best_slot == nullptr || best_score == nullptr))
+        return fail(DF2_ERR_INVALID_ARG, "edges: NULL best_slot or best_score");
     if (S <= 0 || n <= 0 || K <= 0 || R <= 0 || V <= 0)
         return fail(DF2_ERR_INVALID_ARG, "edges: S=%d n=%d K=%d R=%d V=%d must be positive", S, n,
                     K, R, V);
@@ -269,7 +274,10 @@ int dflash2_take_device_faults(int32_t* flags_out) {
     if (flags_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "flags_out is NULL");
     cudaError_t e = cudaDeviceSynchronize();
     unsigned v = 0;
+    unsigned v2 = 0;
     if (e == cudaSuccess) e = df2::take_project_faults(&v);
+    if (e == cudaSuccess) e = df2::take_dynconv_faults(&v2);
+    v |= v2;
     if (e != cudaSuccess) return cuda_fail(e, "take_device_faults");
     *flags_out = (int32_t)v;
     return DF2_OK;

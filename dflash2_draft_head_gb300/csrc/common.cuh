@@ -43,6 +43,8 @@ struct EdgesArgs {
 
 // Each launcher enqueues on `stream` and returns the launch's cudaError_t.
 cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream);
+// Reads and clears the convolution kernels' device fault word (synchronous).
+cudaError_t take_dynconv_faults(unsigned* flags);
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
 cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
 // Reads and clears the projection kernel's device fault word (synchronous).

@@ -17,6 +17,9 @@
 //  - the arithmetic is fp32, two channels per packed FFMA2 instruction.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
+#include "dflash2.h"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -189,6 +192,230 @@ __global__ void __launch_bounds__(256) dynconv_kernel(const DynParams p) {
     }
 }
 
+// ------------------------------------------------------------------ pipelined path
+//
+// Persistent CTAs: `nthr` compute threads (8 channels each, the CTA's channel
+// block) plus one producer warp.  Work items are (sequence, 8-position tile,
+// channel block), channel block fastest.  For every item one producer lane
+// stages into a ring of shared-memory buffers, with non-tensor bulk copies
+// completing on an mbarrier:
+//   - the T-1 halo rows (from x, or from the history window for the first tile
+//     of a sequence) and the tile's rows of x, each the CTA's channel segment;
+//   - the tile's whole delta block [l][t][G] (contiguous in HBM).
+// Compute threads consume a buffer (16-byte shared loads, a register sliding
+// window of T converted rows, packed FFMA2), store 16-byte outputs straight to
+// HBM and release the buffer with an mbarrier arrive.  The ring keeps several
+// tiles of loads in flight per SM without holding them in registers.
+
+constexpr int PL = 8;  // positions per work item
+
+// Device fault word of the convolution kernels: DF2_FLAG_TIMEOUT when a
+// bounded wait gives up.
+__device__ unsigned int g_dyn_fault = 0;
+
+struct PipeParams {
+    const __nv_bfloat16* x;
+    const __nv_bfloat16* hist;
+    const __nv_bfloat16* base;
+    const __nv_bfloat16* delta;
+    void* out;
+    int S, n, C, G, cg;
+    int nthr, n_cblk, n_ptile;
+    int n_items;
+    int stages;
+    uint32_t row_bytes;    // nthr * 16: one staged row segment
+    uint32_t stage_bytes;  // (T-1+PL) rows + PL*T*G bf16 of delta, 128-byte rounded
+};
+
+template <int T, typename TOut>
+__global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int nthr = p.nthr;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * p.stage_bytes);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = smem_u32(bars + p.stages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * p.stages);
+    const uint32_t smem0 = smem_u32(smem);
+    const int TG = T * p.G;
+
+    if (tid == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, (uint32_t)nthr);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (tid >= nthr) {
+        // ---------------- producer (one lane)
+        if (tid != nthr) return;
+        int it = 0;
+        for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+            const int st = it % p.stages;
+            const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+            if (*abort_flag) break;
+            if (!mbar_wait_bounded(empty0 + 8 * st, ph ^ 1u, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(&g_dyn_fault, (unsigned)DF2_FLAG_TIMEOUT);
+                break;
+            }
+            const int cblk = item % p.n_cblk;
+            const int rest = item / p.n_cblk;
+            const int ptile = rest % p.n_ptile;
+            const int s = rest / p.n_ptile;
+            const int i0 = ptile * PL;
+            const int c0 = cblk * nthr * 8;
+            const uint32_t seg = (uint32_t)min(nthr * 8, p.C - c0) * 2u;
+            const int nl = min(PL, p.n - i0);
+            const bool halo_from_hist = i0 == 0;
+            const int nhalo = (halo_from_hist && p.hist == nullptr) ? 0 : T - 1;
+            const uint32_t fb = full0 + 8 * st;
+            const uint32_t bytes = (uint32_t)(nhalo + nl) * seg + (uint32_t)(nl * TG) * 2u;
+            mbar_arrive_expect_tx(fb, bytes);
+            const uint32_t dst = smem0 + (uint32_t)st * p.stage_bytes;
+            for (int r = 0; r < nhalo; ++r) {
+                const __nv_bfloat16* src =
+                    halo_from_hist ? p.hist + ((size_t)s * (T - 1) + r) * p.C + c0
+                                   : p.x + ((size_t)s * p.n + i0 - (T - 1) + r) * p.C + c0;
+                bulk_g2s(dst + (uint32_t)r * p.row_bytes, src, seg, fb);
+            }
+            for (int l = 0; l < nl; ++l)
+                bulk_g2s(dst + (uint32_t)(T - 1 + l) * p.row_bytes,
+                         p.x + ((size_t)s * p.n + i0 + l) * p.C + c0, seg, fb);
+            bulk_g2s(dst + (uint32_t)(T - 1 + PL) * p.row_bytes,
+                     p.delta + ((size_t)s * p.n + i0) * TG, (uint32_t)(nl * TG) * 2u, fb);
+        }
+        return;
+    }
+
+    // ---------------- compute threads
+    int it = 0;
+    int cur_cblk = -1;
+    float2 bw[T][4];
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+        const int st = it % p.stages;
+        const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+        const int cblk = item % p.n_cblk;
+        const int rest = item / p.n_cblk;
+        const int ptile = rest % p.n_ptile;
+        const int s = rest / p.n_ptile;
+        const int i0 = ptile * PL;
+        const int cb0 = cblk * nthr * 8;
+        const int c = cb0 + tid * 8;
+        const bool active = c < p.C;
+        const int nl = min(PL, p.n - i0);
+        if (cblk != cur_cblk) {
+            cur_cblk = cblk;
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                uint4 v = active ? ldg_nc_v4(p.base + (size_t)t * p.C + c) : make_uint4(0, 0, 0, 0);
+                bw[t][0] = bf16x2_to_f2(v.x);
+                bw[t][1] = bf16x2_to_f2(v.y);
+                bw[t][2] = bf16x2_to_f2(v.z);
+                bw[t][3] = bf16x2_to_f2(v.w);
+            }
+        }
+        if (!*abort_flag && !mbar_wait_bounded(full0 + 8 * st, ph, kWaitNs)) {
+            *abort_flag = 1;
+            atomicOr(&g_dyn_fault, (unsigned)DF2_FLAG_TIMEOUT);
+        }
+        if (active && !*abort_flag) {
+            const uint32_t sb = smem0 + (uint32_t)st * p.stage_bytes + (uint32_t)tid * 16u;
+            const __nv_bfloat16* dl = reinterpret_cast<const __nv_bfloat16*>(
+                smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes);
+            const int g = c / p.cg;
+            const bool zero_halo = (i0 == 0 && p.hist == nullptr);
+            float2 xw[T][4];  // xw[t] multiplies tap t
+#pragma unroll
+            for (int k = 0; k < T; ++k)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < T - 1; ++r) {
+#pragma unroll
+                for (int k = T - 1; k > 0; --k)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
+                const uint4 v = zero_halo ? make_uint4(0, 0, 0, 0) : lds_v4(sb + (uint32_t)r * p.row_bytes);
+                xw[0][0] = bf16x2_to_f2(v.x);
+                xw[0][1] = bf16x2_to_f2(v.y);
+                xw[0][2] = bf16x2_to_f2(v.z);
+                xw[0][3] = bf16x2_to_f2(v.w);
+            }
+            TOut* op = static_cast<TOut*>(p.out) + ((size_t)s * p.n + i0) * p.C + c;
+#pragma unroll
+            for (int l = 0; l < PL; ++l) {
+                if (l < nl) {
+#pragma unroll
+                    for (int k = T - 1; k > 0; --k)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
+                    const uint4 v = lds_v4(sb + (uint32_t)(T - 1 + l) * p.row_bytes);
+                    xw[0][0] = bf16x2_to_f2(v.x);
+                    xw[0][1] = bf16x2_to_f2(v.y);
+                    xw[0][2] = bf16x2_to_f2(v.z);
+                    xw[0][3] = bf16x2_to_f2(v.w);
+                    float2 acc[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int t = 0; t < T; ++t) {
+                        const float dv = __bfloat162float(dl[(l * T + t) * p.G + g]);
+                        const float2 d2 = make_float2(dv, dv);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
+                    }
+                    store_row(op + (size_t)l * p.C, acc);
+                }
+            }
+        }
+        mbar_arrive(empty0 + 8 * st);
+    }
+    // On an abandoned pipeline, give copies still in flight a bounded time to
+    // land before the CTA's shared memory is released.
+    if (tid == 0 && *abort_flag) {
+        for (int i = 0; i < p.stages; ++i) mbar_wait_bounded(full0 + 8 * i, 0, kWaitNs / 4);
+    }
+}
+
+template <int T, typename TOut>
+cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
+    auto kern = dynconv_pipe_kernel<T, TOut>;
+    const size_t smem = (size_t)p.stages * p.stage_bytes + 2 * 8 * p.stages + 16;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, p.nthr + 32, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long grid = std::min<long long>((long long)sms * per_sm, p.n_items);
+    kern<<<(unsigned)grid, p.nthr + 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename TOut>
+cudaError_t launch_pipe(const PipeParams& p, int T, cudaStream_t stream) {
+    switch (T) {
+#define DF2_CASE(TT) \
+    case TT:         \
+        return launch_pipe_t<TT, TOut>(p, stream);
+        DF2_CASE(1) DF2_CASE(2) DF2_CASE(3) DF2_CASE(4) DF2_CASE(5) DF2_CASE(6) DF2_CASE(7)
+        DF2_CASE(8)
+#undef DF2_CASE
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
 template <typename TIn>
 constexpr int tile_len(int T) {
     return sizeof(TIn) == 4 ? (T <= 8 ? 4 : 2) : (T <= 8 ? 8 : (T <= 12 ? 4 : 2));
@@ -238,6 +465,15 @@ int pick_threads(int C) {
 
 }  // namespace
 
+cudaError_t take_dynconv_faults(unsigned* flags) {
+    unsigned v = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_dyn_fault, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_dyn_fault, &zero, sizeof(zero));
+    *flags = v;
+    return e;
+}
+
 cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream) {
     DynParams p{};
     p.x = a.x;
@@ -255,6 +491,33 @@ cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream) {
     // groups a window of nthr*8 consecutive channels can touch
     p.ng_max = (nthr * 8 - 1) / p.cg + 2;
     if (p.ng_max > a.G) p.ng_max = a.G;
+    if (a.in_bf16 && a.T <= 8 && (a.T * a.G) % 8 == 0 && nthr <= 128) {
+        PipeParams q{};
+        q.x = static_cast<const __nv_bfloat16*>(a.x);
+        q.hist = static_cast<const __nv_bfloat16*>(a.hist);
+        q.base = static_cast<const __nv_bfloat16*>(a.base);
+        q.delta = static_cast<const __nv_bfloat16*>(a.delta);
+        q.out = a.out;
+        q.S = a.S;
+        q.n = a.n;
+        q.C = a.C;
+        q.G = a.G;
+        q.cg = p.cg;
+        q.nthr = nthr;
+        q.n_cblk = p.n_cblk;
+        q.n_ptile = (a.n + PL - 1) / PL;
+        const long long items = (long long)a.S * q.n_ptile * q.n_cblk;
+        if (items <= 0x7FFFFFFFLL) {
+            q.n_items = (int)items;
+            q.row_bytes = (uint32_t)nthr * 16u;
+            const uint32_t raw = (uint32_t)(a.T - 1 + PL) * q.row_bytes +
+                                 (uint32_t)(PL * a.T * a.G) * 2u;
+            q.stage_bytes = (raw + 127u) & ~127u;
+            q.stages = 2;
+            return a.out_bf16 ? launch_pipe<__nv_bfloat16>(q, a.T, stream)
+                              : launch_pipe<float>(q, a.T, stream);
+        }
+    }
     if (a.in_bf16 && a.out_bf16)
         return launch_dtype<__nv_bfloat16, __nv_bfloat16>(p, a.T, nthr, stream);
     if (a.in_bf16)

@@ -123,7 +123,8 @@ int dflash2_project(const void* h, const void* W, float* u, int P, int d, int R,
  *   err_flag   one device int32 or NULL; DF2_FLAG_* bits are ORed into it
  *              (the caller zeroes it and reads it after its own sync).
  *
- * n == 1 has no transitions: returns DF2_OK having launched nothing.
+ * n == 1 has no transitions: returns DF2_OK having launched nothing (the three
+ * outputs are empty and may be NULL).
  * An id outside [0,V) is clamped into range for the load and flagged
  * (DF2_FLAG_BAD_ID); the kernel never traps.  In BF16 mode the gate
  * A[id_p] (.) u is rounded to bf16 before the tensor-core contraction.
