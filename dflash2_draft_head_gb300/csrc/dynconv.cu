@@ -227,6 +227,86 @@ struct PipeParams {
     uint32_t stage_bytes;  // (T-1+PL) rows + PL*T*G bf16 of delta, 128-byte rounded
 };
 
+
+// Converts one staged 8-channel bf16 row segment into four packed fp32 pairs.
+__device__ __forceinline__ void load_row_f2(uint32_t addr, float2 (&f)[4]) {
+    const uint4 v = lds_v4(addr);
+    f[0] = bf16x2_to_f2(v.x);
+    f[1] = bf16x2_to_f2(v.y);
+    f[2] = bf16x2_to_f2(v.z);
+    f[3] = bf16x2_to_f2(v.w);
+}
+
+// One output position: acc = sum_t (base_t + delta_t) * x_{i-t}; xw[t] holds x_{i-t}.
+template <int T>
+__device__ __forceinline__ void conv_point(const float2 (&bw)[T][4], const float2 (&xw)[T][4],
+                                           const __nv_bfloat16* dl, int G, float2 (&acc)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const float dv = __bfloat162float(dl[t * G]);
+        const float2 d2 = make_float2(dv, dv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
+    }
+}
+
+// A full tile of NL positions from a staged buffer: rows 0..T-2 are the halo,
+// row T-1+l holds position l; dl points at delta[l=0][t=0][g] (stride G per tap,
+// T*G per position).  Straight-line code: the window shifts are renames.
+template <int T, typename TOut, int NL>
+__device__ __forceinline__ void conv_tile(uint32_t sb, uint32_t row_bytes,
+                                          const __nv_bfloat16* dl, int G, bool zero_halo,
+                                          const float2 (&bw)[T][4], TOut* op, int C) {
+    float2 xw[T][4];
+#pragma unroll
+    for (int k = 0; k < T; ++k)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
+    if (!zero_halo) {
+#pragma unroll
+        for (int r = 0; r < T - 1; ++r) load_row_f2(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
+    }
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+#pragma unroll
+        for (int k = T - 1; k > 0; --k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
+        load_row_f2(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
+        float2 acc[4];
+        conv_point<T>(bw, xw, dl + l * T * G, G, acc);
+        store_row(op + (size_t)l * C, acc);
+    }
+}
+
+// The last, partial tile of a sequence (nl < PL positions).
+template <int T, typename TOut>
+__device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes,
+                                              const __nv_bfloat16* dl, int G, bool zero_halo,
+                                              const float2 (&bw)[T][4], TOut* op, int C, int nl) {
+    float2 xw[T][4];
+#pragma unroll
+    for (int k = 0; k < T; ++k)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
+    if (!zero_halo) {
+#pragma unroll
+        for (int r = 0; r < T - 1; ++r) load_row_f2(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
+    }
+    for (int l = 0; l < nl; ++l) {
+#pragma unroll
+        for (int k = T - 1; k > 0; --k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
+        load_row_f2(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
+        float2 acc[4];
+        conv_point<T>(bw, xw, dl + l * T * G, G, acc);
+        store_row(op + (size_t)l * C, acc);
+    }
+}
+
 template <int T, typename TOut>
 __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -325,53 +405,14 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
         if (active && !*abort_flag) {
             const uint32_t sb = smem0 + (uint32_t)st * p.stage_bytes + (uint32_t)tid * 16u;
             const __nv_bfloat16* dl = reinterpret_cast<const __nv_bfloat16*>(
-                smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes);
-            const int g = c / p.cg;
+                smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes) +
+                c / p.cg;
             const bool zero_halo = (i0 == 0 && p.hist == nullptr);
-            float2 xw[T][4];  // xw[t] multiplies tap t
-#pragma unroll
-            for (int k = 0; k < T; ++k)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < T - 1; ++r) {
-#pragma unroll
-                for (int k = T - 1; k > 0; --k)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
-                const uint4 v = zero_halo ? make_uint4(0, 0, 0, 0) : lds_v4(sb + (uint32_t)r * p.row_bytes);
-                xw[0][0] = bf16x2_to_f2(v.x);
-                xw[0][1] = bf16x2_to_f2(v.y);
-                xw[0][2] = bf16x2_to_f2(v.z);
-                xw[0][3] = bf16x2_to_f2(v.w);
-            }
             TOut* op = static_cast<TOut*>(p.out) + ((size_t)s * p.n + i0) * p.C + c;
-#pragma unroll
-            for (int l = 0; l < PL; ++l) {
-                if (l < nl) {
-#pragma unroll
-                    for (int k = T - 1; k > 0; --k)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
-                    const uint4 v = lds_v4(sb + (uint32_t)(T - 1 + l) * p.row_bytes);
-                    xw[0][0] = bf16x2_to_f2(v.x);
-                    xw[0][1] = bf16x2_to_f2(v.y);
-                    xw[0][2] = bf16x2_to_f2(v.z);
-                    xw[0][3] = bf16x2_to_f2(v.w);
-                    float2 acc[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        const float dv = __bfloat162float(dl[(l * T + t) * p.G + g]);
-                        const float2 d2 = make_float2(dv, dv);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
-                    }
-                    store_row(op + (size_t)l * p.C, acc);
-                }
-            }
+            if (nl == PL)
+                conv_tile<T, TOut, PL>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C);
+            else
+                conv_tile_ragged<T, TOut>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C, nl);
         }
         mbar_arrive(empty0 + 8 * st);
     }

@@ -69,28 +69,38 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
 constexpr int TROWS = 128;
 constexpr int KB_BYTES = TROWS * 128;  // one 64-element k-block of 128 rows
 
+// Shared memory of the tile kernel: two operand tiles (KB k-blocks of 128
+// rows x 128 bytes each), the tile's u rows when they fit, ids and offsets.
 template <int KB>
 struct TileSmem {
     static constexpr size_t op_bytes = (size_t)KB * KB_BYTES;
-    static constexpr size_t used = 1024 /*align*/ + 2 * op_bytes + TROWS * 4 * 2 /*ids*/ + 64;
-    // Never fewer than ~60 KB per CTA: at most 3 CTAs share an SM, so their
-    // 3 x 128 TMEM columns always fit in the SM's 512.
-    static constexpr size_t total = used < 61440 ? 61440 : used;
+    static constexpr size_t fixed = 1024 /*align*/ + 2 * op_bytes + TROWS * 4 * 2 /*ids*/ +
+                                    TROWS * 4 /*u row offsets*/ + 64;
+    static constexpr size_t max_u = 32768;
+    static size_t total(size_t u_bytes) {
+        size_t t = fixed + u_bytes;
+        // Never fewer than ~60 KB per CTA: at most 3 CTAs share an SM, so their
+        // 3 x 128 TMEM columns always fit in the SM's 512.
+        return t < 61440 ? 61440 : t;
+    }
 };
 
 template <int KB>
-__global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
+__global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p, const int log2K,
+                                                       const int stage_u) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int K = p.K;
+    const int R = p.R;
+    const int TP = TROWS >> log2K;
     uint8_t* opA = smem;
     uint8_t* opB = smem + TileSmem<KB>::op_bytes;
     int32_t* ids_p = reinterpret_cast<int32_t*>(opB + TileSmem<KB>::op_bytes);
     int32_t* ids_c = ids_p + TROWS;
-    const int K = p.K;
-    const int R = p.R;
-    const int TP = TROWS / K;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(ids_c + TROWS);
+    int32_t* urow = ids_c + TROWS;                             // [TP] row index of u
+    float* us = reinterpret_cast<float*>(urow + TROWS);        // [TP][R] when staged
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(us + (stage_u ? (size_t)TP * R : 0));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
 
     const int tid = threadIdx.x;
@@ -99,16 +109,20 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
     const int nm1 = p.n - 1;
     bool bad = false;
 
-    // 1. ids of this tile's 128 predecessor rows and 128 candidate rows
+    // 1. ids of this tile's 128 predecessor rows and 128 candidate rows, and
+    //    the u row of each of its transitions
     {
-        const int e = e0 + tid / K;
-        const int slot = tid % K;
+        const int e = e0 + (tid >> log2K);
+        const int slot = tid & (K - 1);
         int idp = 0, idc = 0;
         if (e < p.E) {
             const int s = e / nm1;
             const int i = e % nm1 + 1;
             idp = checked_id(p.cand_ids[((size_t)s * p.n + i - 1) * K + slot], p.V, bad);
             idc = checked_id(p.cand_ids[((size_t)s * p.n + i) * K + slot], p.V, bad);
+            if (slot == 0) urow[tid >> log2K] = s * p.n + i;
+        } else if (slot == 0) {
+            urow[tid >> log2K] = -1;
         }
         ids_p[tid] = idp;
         ids_c[tid] = idc;
@@ -126,57 +140,77 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // 2. gather rows into the swizzled operand tiles (gate on the A side)
+    // 2. asynchronous gathers: raw rows of A and B straight into the
+    //    128-byte-swizzle K-major operand layout, and the u rows
     constexpr int CPR = KB * 8;  // 16-byte chunks per (padded) row
     const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
     const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
     const uint32_t sA = smem_u32(opA);
     const uint32_t sB = smem_u32(opB);
-    constexpr int BATCH = 8;
-#pragma unroll 1
-    for (int j0 = 0; j0 < CPR; j0 += BATCH) {
-        uint4 av[BATCH], bv[BATCH];
-        float4 u0[BATCH], u1[BATCH];
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j) {
-            const int slot = (j0 + j) * 128 + tid;
-            const int row = slot / CPR;
-            const int ch = slot % CPR;
-            const int e = e0 + row / K;
-            if (ch * 8 < R && e < p.E) {
-                const int s = e / nm1;
-                const int i = e % nm1 + 1;
-                const float4* ur =
-                    reinterpret_cast<const float4*>(p.u + ((size_t)s * p.n + i) * R + ch * 8);
-                av[j] = ldg_nc_v4(A + (size_t)ids_p[row] * R + ch * 8);
-                bv[j] = ldg_nc_v4(B + (size_t)ids_c[row] * R + ch * 8);
-                u0[j] = __ldg(ur);
-                u1[j] = __ldg(ur + 1);
-            } else {
-                av[j] = make_uint4(0, 0, 0, 0);
-                bv[j] = make_uint4(0, 0, 0, 0);
-                u0[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                u1[j] = u0[j];
-            }
+#pragma unroll 4
+    for (int j = 0; j < CPR; ++j) {
+        const int slot = j * 128 + tid;
+        const int row = slot / CPR;
+        const int ch = slot % CPR;
+        const uint32_t off =
+            (uint32_t)((ch >> 3) * KB_BYTES + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+        if (ch * 8 < R) {
+            cp_async16(sA + off, A + (size_t)ids_p[row] * R + ch * 8);
+            cp_async16(sB + off, B + (size_t)ids_c[row] * R + ch * 8);
+        } else {
+            st_shared_v4(sA + off, make_uint4(0, 0, 0, 0));
+            st_shared_v4(sB + off, make_uint4(0, 0, 0, 0));
         }
-#pragma unroll
-        for (int j = 0; j < BATCH; ++j) {
-            const int slot = (j0 + j) * 128 + tid;
-            const int row = slot / CPR;
-            const int ch = slot % CPR;
-            const uint32_t off = (uint32_t)((ch >> 3) * KB_BYTES + row * 128 +
-                                            (((ch & 7) ^ (row & 7)) << 4));
-            uint4 g;
-            {
-                const float2 a0 = bf16x2_to_f2(av[j].x), a1 = bf16x2_to_f2(av[j].y);
-                const float2 a2 = bf16x2_to_f2(av[j].z), a3 = bf16x2_to_f2(av[j].w);
-                g.x = f2_to_bf16x2(a0.x * u0[j].x, a0.y * u0[j].y);
-                g.y = f2_to_bf16x2(a1.x * u0[j].z, a1.y * u0[j].w);
-                g.z = f2_to_bf16x2(a2.x * u1[j].x, a2.y * u1[j].y);
-                g.w = f2_to_bf16x2(a3.x * u1[j].z, a3.y * u1[j].w);
+    }
+    if (stage_u) {
+        const uint32_t su = smem_u32(us);
+        const int c4 = R >> 2;
+        for (int q = tid; q < TP * c4; q += 128) {
+            const int tt = q / c4;
+            const int r4 = q - tt * c4;
+            const int ur = urow[tt];
+            if (ur >= 0)
+                cp_async16(su + (uint32_t)q * 16u, p.u + (size_t)ur * R + r4 * 4);
+            else
+                st_shared_v4(su + (uint32_t)q * 16u, make_uint4(0, 0, 0, 0));
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // 3. gate in place: A chunk (.) u, rounded to bf16
+#pragma unroll 4
+    for (int j = 0; j < CPR; ++j) {
+        const int slot = j * 128 + tid;
+        const int row = slot / CPR;
+        const int ch = slot % CPR;
+        if (ch * 8 < R) {
+            const uint32_t off =
+                (uint32_t)((ch >> 3) * KB_BYTES + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+            const int tt = row >> log2K;
+            float4 u0, u1;
+            if (stage_u) {
+                const float4* ur = reinterpret_cast<const float4*>(us + (size_t)tt * R + ch * 8);
+                u0 = ur[0];
+                u1 = ur[1];
+            } else if (urow[tt] >= 0) {
+                const float4* ur =
+                    reinterpret_cast<const float4*>(p.u + (size_t)urow[tt] * R + ch * 8);
+                u0 = __ldg(ur);
+                u1 = __ldg(ur + 1);
+            } else {
+                u0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                u1 = u0;
             }
+            const uint4 a = lds_v4(sA + off);
+            const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
+            const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
+            uint4 g;
+            g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
+            g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
+            g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
+            g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
             st_shared_v4(sA + off, g);
-            st_shared_v4(sB + off, bv[j]);
         }
     }
     fence_proxy_async_smem();
@@ -200,9 +234,9 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p) {
 
     // 4. epilogue: this thread's predecessor row, its transition's K columns
     const int r = tid;
-    const int e = e0 + r / K;
-    const int pslot = r % K;
-    const int blk0 = K * (r / K);                       // first column of the block
+    const int e = e0 + (r >> log2K);
+    const int pslot = r & (K - 1);
+    const int blk0 = r & ~(K - 1);                      // first column of the block
     const int colbase = K >= 32 ? blk0 : 32 * warp;     // warp-uniform
     const int width = K >= 32 ? K : 32;
     int s = 0, i = 1;
@@ -340,20 +374,18 @@ EParams make_params(const EdgesArgs& a) {
 
 template <int KB>
 cudaError_t launch_tc(const EParams& p, cudaStream_t stream) {
-    const int TP = TROWS / p.K;
-    const size_t smem = TileSmem<KB>::total;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static unsigned set_mask[KB + 1] = {};
-    if (dev < 32 && !(set_mask[KB] & (1u << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(edges_tc_kernel<KB>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)TileSmem<KB>::total);
-        if (e != cudaSuccess) return e;
-        set_mask[KB] |= 1u << dev;
-    }
+    int log2K = 0;
+    while ((1 << log2K) < p.K) ++log2K;
+    const int TP = TROWS >> log2K;
+    const size_t u_bytes = (size_t)TP * p.R * 4;
+    const int stage_u = u_bytes <= TileSmem<KB>::max_u &&
+                        TileSmem<KB>::fixed + u_bytes <= 220 * 1024;
+    const size_t smem = TileSmem<KB>::total(stage_u ? u_bytes : 0);
+    cudaError_t e = cudaFuncSetAttribute(edges_tc_kernel<KB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int tiles = (p.E + TP - 1) / TP;
-    edges_tc_kernel<KB><<<tiles, 128, smem, stream>>>(p);
+    edges_tc_kernel<KB><<<tiles, 128, smem, stream>>>(p, log2K, stage_u);
     return cudaGetLastError();
 }
 
