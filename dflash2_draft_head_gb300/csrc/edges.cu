@@ -284,6 +284,291 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p, const in
     }
 }
 
+// ------------------------------------------------------------------ pipelined tile path
+//
+// Persistent CTAs (one per SM), warp-specialised, for K a power of two in
+// [4, 128]:
+//   warps 9-16  gather:   per tile, the 256 candidate ids (prefetched one tile
+//                         ahead) and the u-row index of each transition; then,
+//                         per 64-rank k-block, cp.async of
+//                         the 128 A rows and 128 B rows (128 bytes each) straight
+//                         into the 128-byte-swizzle operand layout, and of the
+//                         tile's u slice; completion tracked on full[stage];
+//   warps 4-7   gate:     A (.) u in place (fp32 product, bf16 rounding), then a
+//                         proxy fence; arrive on gated[stage];
+//   warp 8      MMA:      tcgen05.mma M=N=128 over the k-block into one of two
+//                         TMEM accumulators; commit frees the stage, and after
+//                         the last k-block signals tmem_full;
+//   warps 0-3   epilogue: one thread per predecessor row: tcgen05.ld of its own
+//                         transition's K columns, + unary, running argmax,
+//                         stores; then releases the accumulator.
+// A ring of EP_STAGES k-block stages keeps several tiles of gathers in flight
+// while the previous tile is contracted and read out.
+
+constexpr int EP_STAGES = 5;
+constexpr int EP_OP = TROWS * 128;               // one operand k-block: 16 KB
+constexpr int EP_U = 32 * 64 * 4;                // u slice: TP <= 32 rows x 64 ranks fp32
+constexpr int EP_STAGE = 2 * EP_OP + EP_U;       // 40 KB
+constexpr int EP_THREADS = 17 * 32;  // 4 epilogue, 4 gate, 1 MMA, 8 gather warps
+constexpr size_t EP_SMEM = 1024 + (size_t)EP_STAGES * EP_STAGE + 3 * TROWS * 4 +
+                           (3 * EP_STAGES + 4) * 8 + 16;
+
+__global__ void __launch_bounds__(EP_THREADS, 1)
+    edges_pipe_kernel(const EParams p, const int log2K, const int n_tiles, const int nkb,
+                      const int zero_pad) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int K = p.K;
+    const int R = p.R;
+    const int TP = TROWS >> log2K;
+    const int nm1 = p.n - 1;
+    int32_t* ids_p = reinterpret_cast<int32_t*>(smem + (size_t)EP_STAGES * EP_STAGE);
+    int32_t* ids_c = ids_p + TROWS;
+    int32_t* urow = ids_c + TROWS;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(urow + TROWS);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t gated0 = full0 + 8 * EP_STAGES;
+    const uint32_t empty0 = gated0 + 8 * EP_STAGES;
+    const uint32_t tfull0 = empty0 + 8 * EP_STAGES;
+    const uint32_t tempty0 = tfull0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * EP_STAGES + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t st0 = smem_u32(smem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+
+    if (zero_pad) {  // k-block columns past R stay zero for the whole kernel
+        for (int q = tid; q < EP_STAGES * EP_STAGE / 16; q += EP_THREADS)
+            st_shared_v4(st0 + (uint32_t)q * 16u, make_uint4(0, 0, 0, 0));
+        fence_proxy_async_smem();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < EP_STAGES; ++i) {
+            mbar_init(full0 + 8 * i, 256);
+            mbar_init(gated0 + 8 * i, 128);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 128);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait_bounded(bar, parity, kWaitNs)) *abort_flag = 1;
+    };
+
+    if (warp >= 9) {
+        // ------------------------------------------------ gather (8 warps)
+        const int gtid = tid - 9 * 32;  // 0..255: one id per thread and tile
+        const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
+        const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
+        bool bad = false;
+        // id of this thread's row (pred rows 0..127, cand rows 128..255) of a tile
+        auto load_id = [&](int tile, int& id, int& ur) {
+            const int r = gtid & (TROWS - 1);
+            const int e = tile * TP + (r >> log2K);
+            const int slot = r & (K - 1);
+            id = 0;
+            ur = 0;
+            if (tile < n_tiles && e < p.E) {
+                const int s = e / nm1;
+                const int i = e % nm1 + 1;
+                const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
+                id = checked_id(p.cand_ids[(size_t)pos * K + slot], p.V, bad);
+                ur = s * p.n + i;
+            }
+        };
+        int id_next, ur_next;
+        load_id(blockIdx.x, id_next, ur_next);
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            named_bar_sync(1, 256);  // every copy of the previous tile has been issued
+            if (gtid < TROWS) {
+                ids_p[gtid] = id_next;
+                if ((gtid & (K - 1)) == 0) urow[gtid >> log2K] = ur_next;
+            } else {
+                ids_c[gtid - TROWS] = id_next;
+            }
+            named_bar_sync(1, 256);
+            load_id(tile + gridDim.x, id_next, ur_next);  // prefetch the next tile's id
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int st = it % EP_STAGES;
+                wait(empty0 + 8 * st, (((uint32_t)(it / EP_STAGES)) & 1u) ^ 1u);
+                const uint32_t sA = st0 + (uint32_t)st * EP_STAGE;
+                const uint32_t sB = sA + EP_OP;
+                const uint32_t sU = sB + EP_OP;
+                if (!*abort_flag) {
+#pragma unroll
+                    for (int j = 0; j < (TROWS * 8) / 256; ++j) {
+                        const int q = j * 256 + gtid;
+                        const int row = q >> 3;
+                        const int ch = q & 7;
+                        const int col = kb * 64 + ch * 8;
+                        if (col < R) {
+                            const uint32_t off =
+                                (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
+                            cp_async16(sA + off, A + (size_t)ids_p[row] * R + col);
+                            cp_async16(sB + off, B + (size_t)ids_c[row] * R + col);
+                        }
+                    }
+                    for (int q = gtid; q < TP * 16; q += 256) {
+                        const int col = kb * 64 + (q & 15) * 4;
+                        if (col < R)
+                            cp_async16(sU + (uint32_t)q * 16u, p.u + (size_t)urow[q >> 4] * R + col);
+                    }
+                }
+                cp_async_mbar_arrive_noinc(full0 + 8 * st);
+            }
+        }
+        if (bad && p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_BAD_ID);
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------ gate
+        const int gt = tid - 128;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int st = it % EP_STAGES;
+                wait(full0 + 8 * st, ((uint32_t)(it / EP_STAGES)) & 1u);
+                const uint32_t sA = st0 + (uint32_t)st * EP_STAGE;
+                const float* us = reinterpret_cast<const float*>(smem + (size_t)st * EP_STAGE +
+                                                                 2 * EP_OP);
+                if (!*abort_flag) {
+#pragma unroll 4
+                    for (int q = gt; q < TROWS * 8; q += 128) {
+                        const int row = q >> 3;
+                        const int ch = q & 7;
+                        if (kb * 64 + ch * 8 < R) {
+                            const uint32_t off =
+                                (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
+                            const float4* ur = reinterpret_cast<const float4*>(
+                                us + (row >> log2K) * 64 + ch * 8);
+                            const float4 u0 = ur[0];
+                            const float4 u1 = ur[1];
+                            const uint4 a = lds_v4(sA + off);
+                            const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
+                            const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
+                            uint4 g;
+                            g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
+                            g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
+                            g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
+                            g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
+                            st_shared_v4(sA + off, g);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(gated0 + 8 * st);
+            }
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------ MMA issue
+        if ((tid & 31) == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+            int it = 0, tl = 0;
+            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+                const int buf = tl & 1;
+                wait(tempty0 + 8 * buf, (((uint32_t)(tl >> 1)) & 1u) ^ 1u);
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * 128);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int st = it % EP_STAGES;
+                    wait(gated0 + 8 * st, ((uint32_t)(it / EP_STAGES)) & 1u);
+                    tc_fence_after();
+                    const uint32_t sA = st0 + (uint32_t)st * EP_STAGE;
+                    const uint32_t sB = sA + EP_OP;
+                    const int kst = min(4, (R - kb * 64 + 15) / 16);
+                    for (int k = 0; k < kst; ++k)
+                        tc_mma_bf16(d, sw128_desc(sA + 32 * k), sw128_desc(sB + 32 * k), idesc,
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(empty0 + 8 * st);
+                }
+                tc_commit(tfull0 + 8 * buf);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 0-3)
+        const int r = tid;
+        const int pslot = r & (K - 1);
+        const int blk0 = r & ~(K - 1);
+        const int colbase = K >= 32 ? blk0 : 32 * warp;  // warp-uniform
+        const int width = K >= 32 ? K : 32;
+        int tl = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            const int e = tile * TP + (r >> log2K);
+            const bool valid = e < p.E;
+            int s = 0, i = 1;
+            if (valid) {
+                s = e / nm1;
+                i = e % nm1 + 1;
+            }
+            const float* un = p.unary + ((size_t)s * p.n + i) * K;
+            float* erow =
+                (p.edges_out != nullptr && valid) ? p.edges_out + ((size_t)e * K + pslot) * K : nullptr;
+            float best = 0.f;
+            int arg = 0;
+            wait(tfull0 + 8 * buf, ((uint32_t)(tl >> 1)) & 1u);
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < width; cc += 32) {
+                float ua[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int c = colbase + cc + j - blk0;
+                    ua[j] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
+                }
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(
+                    tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * 128 + colbase + cc), v);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int c = colbase + cc + j - blk0;
+                        if (c >= 0 && c < K) {
+                            const float ev = __uint_as_float(v[j]) + ua[j];
+                            if (erow != nullptr) erow[c] = ev;
+                            if (c == 0 || ev > best) {
+                                best = ev;
+                                arg = c;
+                            }
+                        }
+                    }
+                }
+            }
+            if (valid) {
+                p.best_slot[(size_t)e * K + pslot] = arg;
+                p.best_score[(size_t)e * K + pslot] = best;
+            }
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * buf);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+    if (tid == 0 && *abort_flag && p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_TIMEOUT);
+}
+
 // ------------------------------------------------------------------ warp path
 
 template <typename TCB>
@@ -392,12 +677,33 @@ cudaError_t launch_tc(const EParams& p, cudaStream_t stream) {
 }  // namespace
 
 bool edges_tc_supported(int K, int R) {
-    return K >= 1 && K <= 128 && (K & (K - 1)) == 0 && R % 8 == 0 && R <= 384;
+    if (K < 1 || K > 128 || (K & (K - 1)) != 0 || R % 8 != 0) return false;
+    return K >= 4 ? R <= 512 : R <= 384;
+}
+
+cudaError_t launch_edges_pipe(const EParams& p, cudaStream_t stream) {
+    int log2K = 0;
+    while ((1 << log2K) < p.K) ++log2K;
+    const int TP = TROWS >> log2K;
+    const int n_tiles = (p.E + TP - 1) / TP;
+    const int nkb = (p.R + 63) / 64;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(edges_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)EP_SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = n_tiles < sms ? n_tiles : sms;
+    edges_pipe_kernel<<<grid, EP_THREADS, EP_SMEM, stream>>>(p, log2K, n_tiles, nkb,
+                                                             p.R % 64 != 0);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, cudaStream_t stream) {
     const EParams p = make_params(a);
     if (p.E <= 0) return cudaSuccess;
+    if (p.K >= 4 && p.K <= 128) return launch_edges_pipe(p, stream);
     switch ((a.R + 63) / 64) {
         case 1:
             return launch_tc<1>(p, stream);
