@@ -328,20 +328,22 @@ def _call(f, a, L):
         raise RuntimeError(L.dflash2_last_error().decode())
 
 
-def _timed_graph(K, stream, flush, conv, proj, edge, record_ext, L, per_graph=50):
-    """K steps replayed from CUDA graphs: each step = L2 flush, then the three kernels
-    bracketed by timing events recorded as graph nodes.  Returns per-step kernel times."""
+def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
+    """K steps replayed from CUDA graphs.  Each step: L2 flush, then the calls in
+    order, with a timing event (recorded as a graph node) before the first call
+    and after every call.  Returns, per call, the list of per-step times (ms)."""
     import ctypes
 
     import torch
     sp = ctypes.c_void_p(stream.cuda_stream)
-    t_conv, t_proj, t_edge, t_step = [], [], [], []
+    nc = len(calls)
+    times = [[] for _ in range(nc)]
     done = 0
     graphs = {}
     while done < K:
         M = min(per_graph, K - done)
         if M not in graphs:
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(M)]
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(M)]
             for e4 in ev:
                 for e in e4:
                     e.record(stream)  # materialise the event handles
@@ -350,23 +352,124 @@ def _timed_graph(K, stream, flush, conv, proj, edge, record_ext, L, per_graph=50
             with torch.cuda.graph(g, stream=stream):
                 for m in range(M):
                     flush.zero_()
-                    for j, (f, a) in enumerate((conv, proj, edge)):
+                    for j, (f, a) in enumerate(calls):
                         if record_ext(ctypes.c_void_p(ev[m][j].cuda_event), sp, 1):
                             raise RuntimeError("event record in capture failed")
                         _call(f, a, L)
-                    if record_ext(ctypes.c_void_p(ev[m][3].cuda_event), sp, 1):
+                    if record_ext(ctypes.c_void_p(ev[m][nc].cuda_event), sp, 1):
                         raise RuntimeError("event record in capture failed")
             graphs[M] = (g, ev)
         g, ev = graphs[M]
         g.replay()
         stream.synchronize()
         for e in ev:
-            t_conv.append(e[0].elapsed_time(e[1]))
-            t_proj.append(e[1].elapsed_time(e[2]))
-            t_edge.append(e[2].elapsed_time(e[3]))
-            t_step.append(e[0].elapsed_time(e[3]))
+            for j in range(nc):
+                times[j].append(e[j].elapsed_time(e[j + 1]))
         done += M
-    return t_conv, t_proj, t_edge, t_step
+    return times
+
+
+def _timed_eager(K, stream, flush, calls, L):
+    """K eagerly launched steps (fallback when graph timing events are unavailable)."""
+    import torch
+    nc = len(calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(K)]
+    torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
+    for k in range(K):
+        flush.zero_()
+        for j, (f, a) in enumerate(calls):
+            ev[k][j].record(stream)
+            _call(f, a, L)
+        ev[k][nc].record(stream)
+    stream.synchronize()
+    return [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nc)]
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class L2Flush:
+    """Evicts L2 between timed steps: write one buffer larger than L2, then read
+    another, so that L2 ends full of clean lines (no write-back is left for the
+    next timed kernel to pay)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+def _event_record_external():
+    """cudaEventRecordWithFlags(..., cudaEventRecordExternal) of the CUDA runtime torch
+    loaded (timing events inside a captured graph), or None."""
+    import ctypes
+    path = None
+    try:
+        for line in open("/proc/self/maps"):
+            if "libcudart.so" in line:
+                path = line.split()[-1]
+                break
+    except OSError:
+        return None
+    if path is None:
+        return None
+    try:
+        f = ctypes.CDLL(path).cudaEventRecordWithFlags
+    except (OSError, AttributeError):
+        return None
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _call(f, a, L):
+    if f(*a):
+        raise RuntimeError(L.dflash2_last_error().decode())
+
+
+def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
+    """K steps replayed from CUDA graphs.  Each step: L2 flush, then the calls in
+    order, with a timing event (recorded as a graph node) before the first call
+    and after every call.  Returns, per call, the list of per-step times (ms)."""
+    import ctypes
+
+    import torch
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    nc = len(calls)
+    times = [[] for _ in range(nc)]
+    done = 0
+    graphs = {}
+    while done < K:
+        M = min(per_graph, K - done)
+        if M not in graphs:
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(M)]
+            for e4 in ev:
+                for e in e4:
+                    e.record(stream)  # materialise the event handles
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for m in range(M):
+                    flush.zero_()
+                    for j, (f, a) in enumerate(calls):
+                        if record_ext(ctypes.c_void_p(ev[m][j].cuda_event), sp, 1):
+                            raise RuntimeError("event record in capture failed")
+                        _call(f, a, L)
+                    if record_ext(ctypes.c_void_p(ev[m][nc].cuda_event), sp, 1):
+                        raise RuntimeError("event record in capture failed")
+            graphs[M] = (g, ev)
+        g, ev = graphs[M]
+        g.replay()
+        stream.synchronize()
+        for e in ev:
+            for j in range(nc):
+                times[j].append(e[j].elapsed_time(e[j + 1]))
+        done += M
+    return times
 
 
 def _timed_eager(K, stream, flush, conv, proj, edge, L):
@@ -441,10 +544,14 @@ def main():
     edge_args = (ptr(d_in["cand_ids"]), ptr(u), ptr(A), ptr(B), ptr(d_in["unary"]), w.S_sel,
                  w.n_sel, w.K, w.R, w.V, code, None, ptr(best_slot), ptr(best_score), ptr(flag),
                  sp)
+    sel_args = (ptr(d_in["h"]), ptr(Wt), ptr(d_in["cand_ids"]), ptr(A), ptr(B),
+                ptr(d_in["unary"]), w.S_sel, w.n_sel, w.d, w.K, w.R, w.V, code, ptr(u), None,
+                ptr(best_slot), ptr(best_score), ptr(flag), sp)
     f_conv, f_proj, f_edge = L.dflash2_dynconv, L.dflash2_project, L.dflash2_edges
+    f_sel = L.dflash2_select
 
     def step():
-        r = f_conv(*conv_args) | f_proj(*proj_args) | f_edge(*edge_args)
+        r = f_conv(*conv_args) | f_sel(*sel_args)
         if r:
             raise RuntimeError(L.dflash2_last_error().decode())
 
@@ -465,18 +572,25 @@ def main():
     with ClockSampler(gpu_uuid) as clk:
         barrier()
         wall0 = time.perf_counter()
+        calls = [(f_conv, conv_args), (f_sel, sel_args)]
         if record_ext is not None:
-            t_conv, t_proj, t_edge, t_step = _timed_graph(
-                K, stream, flush, (f_conv, conv_args), (f_proj, proj_args),
-                (f_edge, edge_args), record_ext, L)
+            t_conv, t_sel = _timed_graph(K, stream, flush, calls, record_ext, L)
             mode = "cuda-graph"
         else:
-            t_conv, t_proj, t_edge, t_step = _timed_eager(
-                K, stream, flush, (f_conv, conv_args), (f_proj, proj_args),
-                (f_edge, edge_args), L)
+            t_conv, t_sel = _timed_eager(K, stream, flush, calls, L)
             mode = "eager"
         barrier()
         wall = time.perf_counter() - wall0
+    t_step = [a + b for a, b in zip(t_conv, t_sel)]
+    # per-kernel breakdown of the selector (separate, smaller loop: project and
+    # edges each bracketed by events, so the programmatic overlap between them
+    # inside the composite call is absent here)
+    K_iso = max(min(K, 200), 1)
+    iso_calls = [(f_proj, proj_args), (f_edge, edge_args)]
+    if record_ext is not None:
+        t_proj, t_edge = _timed_graph(K_iso, stream, flush, iso_calls, record_ext, L)
+    else:
+        t_proj, t_edge = _timed_eager(K_iso, stream, flush, iso_calls, L)
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -513,6 +627,7 @@ def main():
     conv_b, proj_b, proj_f, edge_b = _bytes(w)
     hbm, tc, src = _peaks()
     conv_us = 1000.0 * statistics.mean(t_conv)
+    sel_us = 1000.0 * statistics.mean(t_sel)
     proj_us = 1000.0 * statistics.mean(t_proj)
     edge_us = 1000.0 * statistics.mean(t_edge)
     achieved = conv_b / (conv_us * 1e-6) / 1e9
@@ -531,16 +646,22 @@ def main():
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
                         "frac_hbm": conv_b / conv_us / 1e3 / hbm},
-            "project": {"us": proj_us, "bytes": proj_b, "GB/s": proj_b / proj_us / 1e3,
+            "select": {"us": sel_us, "bytes": proj_b + edge_b,
+                       "GB/s": (proj_b + edge_b) / sel_us / 1e3,
+                       "frac_hbm": (proj_b + edge_b) / sel_us / 1e3 / hbm,
+                       "note": "project + edges in one dflash2_select call (timed region)"},
+            "project": {"isolated": True, "steps": K_iso, "us": proj_us, "bytes": proj_b,
+                        "GB/s": proj_b / proj_us / 1e3,
                         "TFLOP/s": proj_f / proj_us / 1e6,
                         "frac_hbm": proj_b / proj_us / 1e3 / hbm,
                         "frac_bf16_tc": proj_f / proj_us / 1e6 / tc},
-            "edges": {"us": edge_us, "bytes": edge_b, "GB/s": edge_b / edge_us / 1e3,
+            "edges": {"isolated": True, "steps": K_iso, "us": edge_us, "bytes": edge_b,
+                      "GB/s": edge_b / edge_us / 1e3,
                       "frac_hbm": edge_b / edge_us / 1e3 / hbm},
         },
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 3 * K,  # dynconv + project + edges per timed step
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
         "launch_mode": mode,

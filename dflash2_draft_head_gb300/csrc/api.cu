@@ -136,13 +136,14 @@ int validate_edges(const int32_t* cand_ids, const float* u, const void* A, const
 
 int run_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,
               const float* unary, int S, int n, int K, int R, int V, int dtype, float* edges_out,
-              int32_t* best_slot, float* best_score, int32_t* err_flag, cudaStream_t stream) {
+              int32_t* best_slot, float* best_score, int32_t* err_flag, cudaStream_t stream,
+              int u_only_dependency) {
     if (n == 1) return DF2_OK;
     df2::EdgesArgs a{cand_ids, u, A, B, unary, S, n, K, R, V, edges_out, best_slot, best_score,
                      err_flag};
     cudaError_t e;
     if (dtype == DF2_BF16 && df2::edges_tc_supported(K, R))
-        e = df2::launch_edges_bf16_tc(a, stream);
+        e = df2::launch_edges_bf16_tc(a, u_only_dependency, stream);
     else
         e = df2::launch_edges_warp(a, dtype == DF2_BF16, stream);
     if (e != cudaSuccess) return cuda_fail(e, "edges launch");
@@ -233,7 +234,7 @@ int dflash2_edges(const int32_t* cand_ids, const float* u, const void* A, const 
                             best_slot, best_score, err_flag);
     if (st != DF2_OK) return st;
     return run_edges(cand_ids, u, A, B, unary, S, n, K, R, V, cb_dtype, edges_out, best_slot,
-                     best_score, err_flag, static_cast<cudaStream_t>(stream));
+                     best_score, err_flag, static_cast<cudaStream_t>(stream), 0);
 }
 
 int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const void* A,
@@ -265,8 +266,9 @@ int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     st = run_project(h, W, u_out, S * n, d, R, dtype, s);
     if (st != DF2_OK) return st;
+    // the projection only produces u_out and waited for everything before it
     return run_edges(cand_ids, u_out, A, B, unary, S, n, K, R, V, dtype, edges_out, best_slot,
-                     best_score, err_flag, s);
+                     best_score, err_flag, s, dtype == DF2_BF16 ? 1 : 0);
 }
 
 int dflash2_take_device_faults(int32_t* flags_out) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernel translation units and the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -41,6 +42,10 @@ struct EdgesArgs {
     int32_t* err_flag;
 };
 
+// 2-D bf16 tensor map over a row-major [rows, cols] array with a box of
+// box_rows x 64 columns and 128-byte swizzle (out-of-range elements read as 0).
+bool make_tmap_rows_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
+
 // Each launcher enqueues on `stream` and returns the launch's cudaError_t.
 cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream);
 // Reads and clears the convolution kernels' device fault word (synchronous).
@@ -51,7 +56,10 @@ cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
 cudaError_t take_project_faults(unsigned* flags);
 // Tensor-core tile path: bf16 codebooks, K a power of two <= 128, R <= 384.
 bool edges_tc_supported(int K, int R);
-cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, cudaStream_t stream);
+// u_only_dependency: the preceding kernel in the stream only produces u (and
+// has itself waited for everything before it), so the kernel may read ids,
+// codebooks and unary before that kernel completes.
+cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, int u_only_dependency, cudaStream_t stream);
 // Warp-per-predecessor path (any K <= 256, R <= 512; fp32 or bf16 codebooks).
 cudaError_t launch_edges_warp(const EdgesArgs& a, int cb_bf16, cudaStream_t stream);
 

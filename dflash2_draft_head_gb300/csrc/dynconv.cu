@@ -328,6 +328,10 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
         fence_mbar_init();
     }
     __syncthreads();
+    // Launched as a programmatic dependent: everything above overlapped the
+    // previous kernel; no input is read before it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (tid >= nthr) {
         // ---------------- producer (one lane)
@@ -439,7 +443,18 @@ cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const long long grid = std::min<long long>((long long)sms * per_sm, p.n_items);
-    kern<<<(unsigned)grid, p.nthr + 32, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)(p.nthr + 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

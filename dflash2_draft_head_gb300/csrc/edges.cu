@@ -24,7 +24,10 @@
 // (transition, predecessor); lanes split R, the gate stays in registers, and
 // each candidate's dot product is reduced with warp shuffles.  This is the
 // exact-fp32 path.
+#include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "dflash2.h"
 #include "common.cuh"
@@ -286,42 +289,59 @@ __global__ void __launch_bounds__(128) edges_tc_kernel(const EParams p, const in
 
 // ------------------------------------------------------------------ pipelined tile path
 //
-// Persistent CTAs (one per SM), warp-specialised, for K a power of two in
-// [4, 128]:
-//   warps 9-16  gather:   per tile, the 256 candidate ids (prefetched one tile
-//                         ahead) and the u-row index of each transition; then,
-//                         per 64-rank k-block, cp.async of
-//                         the 128 A rows and 128 B rows (128 bytes each) straight
-//                         into the 128-byte-swizzle operand layout, and of the
-//                         tile's u slice; completion tracked on full[stage];
-//   warps 4-7   gate:     A (.) u in place (fp32 product, bf16 rounding), then a
-//                         proxy fence; arrive on gated[stage];
+// Persistent CTAs (at most one per SM), warp-specialised, for K a power of two
+// in [4, 128].  Work is a list of tiles of up to TP = 128/K transitions: whole
+// tiles round-robin over the CTAs, then the leftover transitions cut into
+// equal small pieces, one more per CTA, so the last round is not a partial
+// wave of whole tiles.  Per tile and 64-rank k-block:
+//   warps 9+    gather:   the tile's 256 candidate ids into shared memory, then
+//                         16-byte cp.async copies of the 128 A rows and 128 B
+//                         rows (128 bytes of each) straight into the
+//                         128-byte-swizzle K-major operand layout, and of the u
+//                         slice, completion tracked on full[stage].  Sixteen
+//                         warps spread the outstanding requests over all four
+//                         SM sub-partitions;
+//   warps 4-7   gate:     A (.) u in place (fp32 product, bf16 rounding), proxy
+//                         fence, arrive on gated[stage];
 //   warp 8      MMA:      tcgen05.mma M=N=128 over the k-block into one of two
-//                         TMEM accumulators; commit frees the stage, and after
-//                         the last k-block signals tmem_full;
-//   warps 0-3   epilogue: one thread per predecessor row: tcgen05.ld of its own
-//                         transition's K columns, + unary, running argmax,
-//                         stores; then releases the accumulator.
-// A ring of EP_STAGES k-block stages keeps several tiles of gathers in flight
-// while the previous tile is contracted and read out.
+//                         TMEM accumulators; commit frees the stage and, after
+//                         the last k-block, signals tmem_full;
+//   warps 0-3   epilogue: one thread per predecessor row: unary prefetched,
+//                         tcgen05.ld of its own transition's K columns, running
+//                         argmax, stores; then releases the accumulator.
 
 constexpr int EP_STAGES = 5;
 constexpr int EP_OP = TROWS * 128;               // one operand k-block: 16 KB
 constexpr int EP_U = 32 * 64 * 4;                // u slice: TP <= 32 rows x 64 ranks fp32
 constexpr int EP_STAGE = 2 * EP_OP + EP_U;       // 40 KB
-constexpr int EP_THREADS = 17 * 32;  // 4 epilogue, 4 gate, 1 MMA, 8 gather warps
+constexpr int EP_GWARPS = 16;                    // gather warps (four per SM sub-partition)
+constexpr int EP_GTHREADS = EP_GWARPS * 32;
+constexpr int EP_THREADS = (9 + EP_GWARPS) * 32;  // 4 epilogue, 4 gate, 1 MMA, gather warps
 constexpr size_t EP_SMEM = 1024 + (size_t)EP_STAGES * EP_STAGE + 3 * TROWS * 4 +
                            (3 * EP_STAGES + 4) * 8 + 16;
 
+struct TileList {
+    int TP, rounds_tiles, piece, n_items, E;
+    // item -> first transition and transition count
+    __device__ __forceinline__ void at(int idx, int& e0, int& cnt) const {
+        if (idx < rounds_tiles) {
+            e0 = idx * TP;
+            cnt = TP;
+        } else {
+            e0 = rounds_tiles * TP + (idx - rounds_tiles) * piece;
+            cnt = min(piece, E - e0);
+        }
+    }
+};
+
 __global__ void __launch_bounds__(EP_THREADS, 1)
-    edges_pipe_kernel(const EParams p, const int log2K, const int n_tiles, const int nkb,
-                      const int zero_pad) {
+    edges_pipe_kernel(const EParams p, const int log2K, const TileList tl_list, const int nkb,
+                      const int zero_pad, const int u_only_dependency) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int K = p.K;
     const int R = p.R;
-    const int TP = TROWS >> log2K;
     const int nm1 = p.n - 1;
     int32_t* ids_p = reinterpret_cast<int32_t*>(smem + (size_t)EP_STAGES * EP_STAGE);
     int32_t* ids_c = ids_p + TROWS;
@@ -338,6 +358,7 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int lane = tid & 31;
 
     if (zero_pad) {  // k-block columns past R stay zero for the whole kernel
         for (int q = tid; q < EP_STAGES * EP_STAGE / 16; q += EP_THREADS)
@@ -346,7 +367,7 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < EP_STAGES; ++i) {
-            mbar_init(full0 + 8 * i, 256);
+            mbar_init(full0 + 8 * i, EP_GTHREADS);
             mbar_init(gated0 + 8 * i, 128);
             mbar_init(empty0 + 8 * i, 1);
         }
@@ -365,6 +386,12 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent.  When the previous grid only
+    // produces u (the projection of the composite selector, which itself waited
+    // for everything before it), ids, codebooks and unary may be read at once
+    // and only the u copies wait; otherwise every thread waits here.
+    if (!u_only_dependency) griddep_wait();
+    griddep_launch_dependents();
 
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (*abort_flag) return;
@@ -372,39 +399,38 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
     };
 
     if (warp >= 9) {
-        // ------------------------------------------------ gather (8 warps)
-        const int gtid = tid - 9 * 32;  // 0..255: one id per thread and tile
+        // ------------------------------------------------ gather (EP_GWARPS warps)
+        const int gtid = tid - 9 * 32;
         const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
         const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
         bool bad = false;
-        // id of this thread's row (pred rows 0..127, cand rows 128..255) of a tile
-        auto load_id = [&](int tile, int& id, int& ur) {
-            const int r = gtid & (TROWS - 1);
-            const int e = tile * TP + (r >> log2K);
-            const int slot = r & (K - 1);
-            id = 0;
-            ur = 0;
-            if (tile < n_tiles && e < p.E) {
-                const int s = e / nm1;
-                const int i = e % nm1 + 1;
-                const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
-                id = checked_id(p.cand_ids[(size_t)pos * K + slot], p.V, bad);
-                ur = s * p.n + i;
-            }
-        };
-        int id_next, ur_next;
-        load_id(blockIdx.x, id_next, ur_next);
         int it = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            named_bar_sync(1, 256);  // every copy of the previous tile has been issued
-            if (gtid < TROWS) {
-                ids_p[gtid] = id_next;
-                if ((gtid & (K - 1)) == 0) urow[gtid >> log2K] = ur_next;
-            } else {
-                ids_c[gtid - TROWS] = id_next;
+        for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x) {
+            int e0, cnt;
+            tl_list.at(idx, e0, cnt);
+            const int rows = cnt << log2K;
+            named_bar_sync(1, EP_GTHREADS);  // the previous tile's copies are all issued
+            if (gtid < 2 * TROWS) {
+                const int r = gtid & (TROWS - 1);
+                const int tt = r >> log2K;
+                const int slot = r & (K - 1);
+                int id = 0, ur = 0;
+                if (tt < cnt) {
+                    const int e = e0 + tt;
+                    const int s = e / nm1;
+                    const int i = e % nm1 + 1;
+                    const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
+                    id = checked_id(p.cand_ids[(size_t)pos * K + slot], p.V, bad);
+                    ur = s * p.n + i;
+                }
+                if (gtid < TROWS) {
+                    ids_p[r] = id;
+                    if (slot == 0) urow[tt] = ur;
+                } else {
+                    ids_c[r] = id;
+                }
             }
-            named_bar_sync(1, 256);
-            load_id(tile + gridDim.x, id_next, ur_next);  // prefetch the next tile's id
+            named_bar_sync(1, EP_GTHREADS);
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = it % EP_STAGES;
                 wait(empty0 + 8 * st, (((uint32_t)(it / EP_STAGES)) & 1u) ^ 1u);
@@ -413,19 +439,20 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
                 const uint32_t sU = sB + EP_OP;
                 if (!*abort_flag) {
 #pragma unroll
-                    for (int j = 0; j < (TROWS * 8) / 256; ++j) {
-                        const int q = j * 256 + gtid;
+                    for (int j = 0; j < (TROWS * 8) / EP_GTHREADS; ++j) {
+                        const int q = j * EP_GTHREADS + gtid;
                         const int row = q >> 3;
                         const int ch = q & 7;
                         const int col = kb * 64 + ch * 8;
-                        if (col < R) {
+                        if (row < rows && col < R) {
                             const uint32_t off =
                                 (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
                             cp_async16(sA + off, A + (size_t)ids_p[row] * R + col);
                             cp_async16(sB + off, B + (size_t)ids_c[row] * R + col);
                         }
                     }
-                    for (int q = gtid; q < TP * 16; q += 256) {
+                    if (u_only_dependency && it == 0) griddep_wait();
+                    for (int q = gtid; q < cnt * 16; q += EP_GTHREADS) {
                         const int col = kb * 64 + (q & 15) * 4;
                         if (col < R)
                             cp_async16(sU + (uint32_t)q * 16u, p.u + (size_t)urow[q >> 4] * R + col);
@@ -439,7 +466,10 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
         // ------------------------------------------------ gate
         const int gt = tid - 128;
         int it = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x) {
+            int e0, cnt;
+            tl_list.at(idx, e0, cnt);
+            const int rows = cnt << log2K;
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = it % EP_STAGES;
                 wait(full0 + 8 * st, ((uint32_t)(it / EP_STAGES)) & 1u);
@@ -451,7 +481,7 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
                     for (int q = gt; q < TROWS * 8; q += 128) {
                         const int row = q >> 3;
                         const int ch = q & 7;
-                        if (kb * 64 + ch * 8 < R) {
+                        if (row < rows && kb * 64 + ch * 8 < R) {
                             const uint32_t off =
                                 (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
                             const float4* ur = reinterpret_cast<const float4*>(
@@ -476,10 +506,10 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
         }
     } else if (warp == 8) {
         // ------------------------------------------------ MMA issue
-        if ((tid & 31) == 0) {
+        if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             int it = 0, tl = 0;
-            for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+            for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x, ++tl) {
                 const int buf = tl & 1;
                 wait(tempty0 + 8 * buf, (((uint32_t)(tl >> 1)) & 1u) ^ 1u);
                 tc_fence_after();
@@ -508,10 +538,12 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
         const int colbase = K >= 32 ? blk0 : 32 * warp;  // warp-uniform
         const int width = K >= 32 ? K : 32;
         int tl = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+        for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x, ++tl) {
+            int e0, cnt;
+            tl_list.at(idx, e0, cnt);
             const int buf = tl & 1;
-            const int e = tile * TP + (r >> log2K);
-            const bool valid = e < p.E;
+            const bool valid = (r >> log2K) < cnt;
+            const int e = e0 + (r >> log2K);
             int s = 0, i = 1;
             if (valid) {
                 s = e / nm1;
@@ -522,15 +554,22 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
                 (p.edges_out != nullptr && valid) ? p.edges_out + ((size_t)e * K + pslot) * K : nullptr;
             float best = 0.f;
             int arg = 0;
+            float ua[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {  // first column chunk's unary, before the wait
+                const int c = colbase + j - blk0;
+                ua[j] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
+            }
             wait(tfull0 + 8 * buf, ((uint32_t)(tl >> 1)) & 1u);
             tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < width; cc += 32) {
-                float ua[32];
+                if (cc > 0) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int c = colbase + cc + j - blk0;
-                    ua[j] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
+                    for (int j = 0; j < 32; ++j) {
+                        const int c = colbase + cc + j - blk0;
+                        ua[j] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
+                    }
                 }
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(
@@ -681,11 +720,10 @@ bool edges_tc_supported(int K, int R) {
     return K >= 4 ? R <= 512 : R <= 384;
 }
 
-cudaError_t launch_edges_pipe(const EParams& p, cudaStream_t stream) {
+cudaError_t launch_edges_pipe(const EParams& p, int u_only_dependency, cudaStream_t stream) {
     int log2K = 0;
     while ((1 << log2K) < p.K) ++log2K;
     const int TP = TROWS >> log2K;
-    const int n_tiles = (p.E + TP - 1) / TP;
     const int nkb = (p.R + 63) / 64;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -694,16 +732,36 @@ cudaError_t launch_edges_pipe(const EParams& p, cudaStream_t stream) {
         e = cudaFuncSetAttribute(edges_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)EP_SMEM);
     if (e != cudaSuccess) return e;
-    const int grid = n_tiles < sms ? n_tiles : sms;
-    edges_pipe_kernel<<<grid, EP_THREADS, EP_SMEM, stream>>>(p, log2K, n_tiles, nkb,
-                                                             p.R % 64 != 0);
+    // whole tiles round-robin, then the leftover transitions in equal pieces
+    const int G = p.E < sms ? p.E : sms;
+    TileList tl{};
+    tl.TP = TP;
+    tl.E = p.E;
+    tl.rounds_tiles = (p.E / TP / G) * G;
+    const int rem = p.E - tl.rounds_tiles * TP;
+    tl.piece = rem > 0 ? std::min(TP, (rem + G - 1) / G) : TP;
+    const int n_pieces = rem > 0 ? (rem + tl.piece - 1) / tl.piece : 0;
+    tl.n_items = tl.rounds_tiles + n_pieces;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(EP_THREADS);
+    cfg.dynamicSmemBytes = EP_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, edges_pipe_kernel, p, log2K, tl, nkb, (int)(p.R % 64 != 0),
+                           u_only_dependency);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, cudaStream_t stream) {
+cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, int u_only_dependency, cudaStream_t stream) {
     const EParams p = make_params(a);
     if (p.E <= 0) return cudaSuccess;
-    if (p.K >= 4 && p.K <= 128) return launch_edges_pipe(p, stream);
+    if (p.K >= 4 && p.K <= 128) return launch_edges_pipe(p, u_only_dependency, stream);
     switch ((a.R + 63) / 64) {
         case 1:
             return launch_tc<1>(p, stream);

@@ -54,6 +54,7 @@ struct ProjParams {
     int splitk;
 };
 
+template <int SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const ProjParams p) {
@@ -72,8 +73,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const int m_tile = blockIdx.y;
     const int n_tile = blockIdx.z;
-    const int kb0 = (int)((long long)rank * p.kblocks / p.splitk);
-    const int kb1 = (int)((long long)(rank + 1) * p.kblocks / p.splitk);
+    const int kb0 = (int)((long long)rank * p.kblocks / SPLIT);
+    const int kb1 = (int)((long long)(rank + 1) * p.kblocks / SPLIT);
     const int nkb = kb1 - kb0;
 
     if (threadIdx.x == 0) {
@@ -95,6 +96,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    // Launched as a programmatic dependent: the set-up above overlapped the
+    // previous kernel; h and W are read only after it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0 && lane == 0) {
         // TMA producer
@@ -135,52 +140,93 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     __syncwarp();
 
-    // Epilogue: partial tile TMEM -> shared memory (stage buffers are free once
-    // the accumulator barrier fires: every issued load was consumed by an MMA).
+    // Epilogue.  The accumulator barrier fires once every issued load has been
+    // consumed by an MMA, so the stage buffers are free for the reduction.
     if (!mbar_wait_bounded(accum, 0, kWaitNs)) ok = false;
     tc_fence_after();
-    float* red = reinterpret_cast<float*>(stages);
     const int row = warp * 32 + lane;
+    if constexpr (SPLIT == 1) {
+        // no split: each thread writes its own row straight from TMEM
+        const int grow = m_tile * BM + row;
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-        tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld_wait();
+            const int gcol = n_tile * BN + c0;
+            if (grow < p.P) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-    }
-    tc_fence_before();
-    cluster_sync();
-
-    // Deterministic split-K reduction across the cluster.
-    const int rows_per = BM / p.splitk;
-    const int r_base = (int)rank * rows_per;
-    const int nvec = rows_per * (BN / 4);
-    const uint32_t red_s = smem_u32(red);
-    for (int q = threadIdx.x; q < nvec; q += NTHREADS) {
-        const int rr = r_base + q / (BN / 4);
-        const int cc = (q % (BN / 4)) * 4;
-        const uint32_t off = red_s + (uint32_t)((rr * RED_STRIDE + cc) * 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int src = 0; src < p.splitk; ++src) {
-            const float4 v = ld_cluster_f4(map_cluster(off, (uint32_t)src));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+                for (int j = 0; j < 8; ++j)
+                    if (gcol + 4 * j < p.R)
+                        *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol + 4 * j) =
+                            make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            }
         }
-        const int grow = m_tile * BM + rr;
-        const int gcol = n_tile * BN + cc;
-        if (grow < p.P && gcol < p.R)
-            *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
-    }
-    cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, BN);
+        }
+    } else {
+        // partial tile TMEM -> this CTA's shared memory
+        float* red = reinterpret_cast<float*>(stages);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+        tc_fence_before();
+        cluster_sync();
+
+        // Deterministic split-K reduction across the cluster: CTA r owns rows
+        // [r*128/SPLIT, (r+1)*128/SPLIT); every remote load of a thread's
+        // elements is issued before the fixed-order sums.
+        constexpr int NV = (BM / SPLIT) * (BN / 4) / NTHREADS;  // float4 per thread
+        const int r_base = (int)rank * (BM / SPLIT);
+        const uint32_t red_s = smem_u32(red);
+        uint32_t off[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int q = j * NTHREADS + threadIdx.x;
+            off[j] = red_s + (uint32_t)(((r_base + q / (BN / 4)) * RED_STRIDE + (q % (BN / 4)) * 4) * 4);
+        }
+        float4 acc[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) acc[j] = ld_cluster_f4(map_cluster(off[j], 0));
+#pragma unroll
+        for (int src = 1; src < SPLIT; ++src) {
+            float4 v[NV];
+#pragma unroll
+            for (int j = 0; j < NV; ++j) v[j] = ld_cluster_f4(map_cluster(off[j], (uint32_t)src));
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                acc[j].x += v[j].x;
+                acc[j].y += v[j].y;
+                acc[j].z += v[j].z;
+                acc[j].w += v[j].w;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int q = j * NTHREADS + threadIdx.x;
+            const int grow = m_tile * BM + r_base + q / (BN / 4);
+            const int gcol = n_tile * BN + (q % (BN / 4)) * 4;
+            if (grow < p.P && gcol < p.R)
+                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc[j];
+        }
+        cluster_sync();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, BN);
+        }
     }
     if (!ok) atomicOr(&g_fault_word, (unsigned)DF2_FLAG_TIMEOUT);
 }
@@ -198,8 +244,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+}  // namespace
+
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128 B swizzle.
-bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+bool make_tmap_rows_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -211,6 +259,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- fp32 path
 
@@ -246,7 +296,7 @@ __global__ void __launch_bounds__(256) project_f32_kernel(const float* __restric
 
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms) {
     CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, a.h, a.P, a.d, BM) || !make_map(&tmB, a.W, a.R, a.d, BN))
+    if (!make_tmap_rows_bf16(&tmA, a.h, a.P, a.d, BM) || !make_tmap_rows_bf16(&tmB, a.W, a.R, a.d, BN))
         return cudaErrorInvalidValue;
     const int kblocks = (a.d + BK - 1) / BK;
     const int m_tiles = (a.P + BM - 1) / BM;
@@ -257,30 +307,29 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
     int split = 1;
     while (split < 8 && tiles * split * 2 <= num_sms && kblocks >= split * 4) split *= 2;
 
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static unsigned attr_mask = 0;
-    if (dev >= 32 || !(attr_mask & (1u << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(project_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        if (dev < 32) attr_mask |= 1u << dev;
-    }
+    auto kern = split == 1 ? project_tc_kernel<1>
+                : split == 2 ? project_tc_kernel<2>
+                : split == 4 ? project_tc_kernel<4>
+                             : project_tc_kernel<8>;
+    cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)SMEM_BYTES);
+    if (e0 != cudaSuccess) return e0;
     ProjParams p{a.u, a.P, a.R, kblocks, split};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)split, (unsigned)m_tiles, (unsigned)n_tiles);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)split;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, project_tc_kernel, tmA, tmB, p);
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -111,6 +111,18 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     return v;
 }
 
+// TMA gather of four rows: columns [x, x + box width) of rows y0..y3 of a 2-D
+// tensor map whose box is one row high, written as four consecutive box rows
+// at dst (with the map's swizzle), completing on the mbarrier.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int x,
+                                            int y0, int y1, int y2, int y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -230,13 +242,29 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// Distributed-shared-memory load.  Not volatile: ordering against the writers
+// comes from the cluster barrier (which is volatile and clobbers memory), so
+// independent loads can be issued back to back.
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
     float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+    asm("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(addr));
     return v;
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Waits until the preceding grid in the stream has completed and its memory is
+// visible (a no-op when the kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid in the stream (if launched as a programmatic dependent)
+// start being scheduled once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ loads
