@@ -39,7 +39,12 @@ FLUSH_BYTES = 256 << 20
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
 # sha256 of the kernel source they were taken on (null when the source changed).
-TRAFFIC = {}
+TRAFFIC = {
+    ("batched_256x16_d5120", "dynconv"): {
+        "sha": "f3a5fc7a13c94f99d3a6206d2720691540fd7637aedcc006619d5ae729de77ce",
+        "bytes": 51189504 + 3214592,  # dram__bytes_read.sum + dram__bytes_write.sum
+    },
+}
 
 
 def _args():
@@ -387,107 +392,6 @@ def _timed_eager(K, stream, flush, calls, L):
 
 # ---------------------------------------------------------------- GPU arm
 
-class L2Flush:
-    """Evicts L2 between timed steps: write one buffer larger than L2, then read
-    another, so that L2 ends full of clean lines (no write-back is left for the
-    next timed kernel to pay)."""
-
-    def __init__(self, dev):
-        import torch
-        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        self.sink = torch.empty((), dtype=torch.float32, device=dev)
-
-    def zero_(self):
-        import torch
-        self.w.zero_()
-        torch.sum(self.r, dim=0, out=self.sink)
-
-def _event_record_external():
-    """cudaEventRecordWithFlags(..., cudaEventRecordExternal) of the CUDA runtime torch
-    loaded (timing events inside a captured graph), or None."""
-    import ctypes
-    path = None
-    try:
-        for line in open("/proc/self/maps"):
-            if "libcudart.so" in line:
-                path = line.split()[-1]
-                break
-    except OSError:
-        return None
-    if path is None:
-        return None
-    try:
-        f = ctypes.CDLL(path).cudaEventRecordWithFlags
-    except (OSError, AttributeError):
-        return None
-    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
-    f.restype = ctypes.c_int
-    return f
-
-
-def _call(f, a, L):
-    if f(*a):
-        raise RuntimeError(L.dflash2_last_error().decode())
-
-
-def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
-    """K steps replayed from CUDA graphs.  Each step: L2 flush, then the calls in
-    order, with a timing event (recorded as a graph node) before the first call
-    and after every call.  Returns, per call, the list of per-step times (ms)."""
-    import ctypes
-
-    import torch
-    sp = ctypes.c_void_p(stream.cuda_stream)
-    nc = len(calls)
-    times = [[] for _ in range(nc)]
-    done = 0
-    graphs = {}
-    while done < K:
-        M = min(per_graph, K - done)
-        if M not in graphs:
-            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(M)]
-            for e4 in ev:
-                for e in e4:
-                    e.record(stream)  # materialise the event handles
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for m in range(M):
-                    flush.zero_()
-                    for j, (f, a) in enumerate(calls):
-                        if record_ext(ctypes.c_void_p(ev[m][j].cuda_event), sp, 1):
-                            raise RuntimeError("event record in capture failed")
-                        _call(f, a, L)
-                    if record_ext(ctypes.c_void_p(ev[m][nc].cuda_event), sp, 1):
-                        raise RuntimeError("event record in capture failed")
-            graphs[M] = (g, ev)
-        g, ev = graphs[M]
-        g.replay()
-        stream.synchronize()
-        for e in ev:
-            for j in range(nc):
-                times[j].append(e[j].elapsed_time(e[j + 1]))
-        done += M
-    return times
-
-
-def _timed_eager(K, stream, flush, conv, proj, edge, L):
-    """K eagerly launched steps (fallback when graph timing events are unavailable)."""
-    import torch
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
-    for k in range(K):
-        flush.zero_()
-        for j, (f, a) in enumerate((conv, proj, edge)):
-            ev[k][j].record(stream)
-            _call(f, a, L)
-        ev[k][3].record(stream)
-    stream.synchronize()
-    return ([e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev],
-            [e[2].elapsed_time(e[3]) for e in ev], [e[0].elapsed_time(e[3]) for e in ev])
-
-
 def main():
     args = _args()
     if args.impl == "reference":
@@ -643,6 +547,17 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "dflash2_dynconv", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "bytes_per_launch": conv_b, "peak_source": src},
+        "roofline_all": {
+            "dynconv": {"bound": "hbm", "achieved": conv_b / conv_us / 1e3, "peak": hbm,
+                        "unit": "GB/s", "frac": conv_b / conv_us / 1e3 / hbm},
+            "project": {"bound": "hbm", "achieved": proj_b / proj_us / 1e3, "peak": hbm,
+                        "unit": "GB/s", "frac": proj_b / proj_us / 1e3 / hbm,
+                        "tensor_TFLOP/s": proj_f / proj_us / 1e6, "tensor_peak": tc,
+                        "tensor_frac": proj_f / proj_us / 1e6 / tc, "timing": "isolated loop"},
+            "edges": {"bound": "hbm", "achieved": edge_b / edge_us / 1e3, "peak": hbm,
+                      "unit": "GB/s", "frac": edge_b / edge_us / 1e3 / hbm,
+                      "timing": "isolated loop"},
+        },
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
                         "frac_hbm": conv_b / conv_us / 1e3 / hbm},

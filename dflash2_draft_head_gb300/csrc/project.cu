@@ -45,7 +45,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int RED_STRIDE = BN + 4;  // padded fp32 row of the reduction buffer
 constexpr int NTHREADS = 128;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
-static_assert((size_t)BM * RED_STRIDE * 4 <= (size_t)STAGES * STAGE_BYTES, "reduction buffer");
+// partial tile plus up to 7 receive slots of 16 rows (split 8) or 1 slot of 64 rows (split 2)
+static_assert((size_t)BM * RED_STRIDE * 4 * 2 <= (size_t)STAGES * STAGE_BYTES, "reduction buffer");
 
 struct ProjParams {
     float* u;
@@ -63,10 +64,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)STAGES * STAGE_BYTES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = smem_u32(bars + STAGES);
     const uint32_t accum = smem_u32(bars + 2 * STAGES);
+    const uint32_t recv = smem_u32(bars + 2 * STAGES + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -85,6 +87,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(accum, 1);
+        mbar_init(recv, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -170,8 +173,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_dealloc(tmem, BN);
         }
     } else {
-        // partial tile TMEM -> this CTA's shared memory
+        // Split-K reduction through distributed shared memory.  CTA r of the
+        // cluster owns rows [r*RP, (r+1)*RP), RP = 128/SPLIT.  Every CTA writes
+        // its partial tile (padded rows) to its own shared memory, then pushes
+        // each owner's row slice into that owner's receive slot with one bulk
+        // shared-to-shared copy; each owner sums the SPLIT slices in rank order
+        // (deterministic) and stores its rows of u.
+        constexpr int RP = BM / SPLIT;
+        constexpr uint32_t SLICE = (uint32_t)RP * RED_STRIDE * 4;
         float* red = reinterpret_cast<float*>(stages);
+        const uint32_t red_s = smem_u32(red);
+        const uint32_t recv_s = red_s + (uint32_t)BM * RED_STRIDE * 4;  // SPLIT-1 slots
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(recv, (SPLIT - 1) * SLICE);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
             uint32_t v[32];
@@ -183,46 +196,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                      __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
+        fence_proxy_async_smem();  // partial tile -> visible to the copy engine
         tc_fence_before();
-        cluster_sync();
+        cluster_sync();            // every CTA's mainloop is done: receive slots are free
+        if (threadIdx.x < SPLIT && threadIdx.x != rank) {
+            const uint32_t dst_rank = threadIdx.x;
+            const uint32_t slot = rank < dst_rank ? rank : rank - 1;
+            bulk_s2cluster(map_cluster(recv_s + slot * SLICE, dst_rank),
+                           red_s + dst_rank * SLICE, SLICE, map_cluster(recv, dst_rank));
+        }
+        if (!mbar_wait_bounded(recv, 0, kWaitNs)) ok = false;
 
-        // Deterministic split-K reduction across the cluster: CTA r owns rows
-        // [r*128/SPLIT, (r+1)*128/SPLIT); every remote load of a thread's
-        // elements is issued before the fixed-order sums.
-        constexpr int NV = (BM / SPLIT) * (BN / 4) / NTHREADS;  // float4 per thread
-        const int r_base = (int)rank * (BM / SPLIT);
-        const uint32_t red_s = smem_u32(red);
-        uint32_t off[NV];
+        const int r_base = (int)rank * RP;
+        for (int q = threadIdx.x; q < RP * (BN / 4); q += NTHREADS) {
+            const int rr = q / (BN / 4);
+            const int cc = (q % (BN / 4)) * 4;
+            const uint32_t eoff = (uint32_t)((rr * RED_STRIDE + cc) * 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int q = j * NTHREADS + threadIdx.x;
-            off[j] = red_s + (uint32_t)(((r_base + q / (BN / 4)) * RED_STRIDE + (q % (BN / 4)) * 4) * 4);
-        }
-        float4 acc[NV];
-#pragma unroll
-        for (int j = 0; j < NV; ++j) acc[j] = ld_cluster_f4(map_cluster(off[j], 0));
-#pragma unroll
-        for (int src = 1; src < SPLIT; ++src) {
-            float4 v[NV];
-#pragma unroll
-            for (int j = 0; j < NV; ++j) v[j] = ld_cluster_f4(map_cluster(off[j], (uint32_t)src));
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                acc[j].x += v[j].x;
-                acc[j].y += v[j].y;
-                acc[j].z += v[j].z;
-                acc[j].w += v[j].w;
+            for (int src = 0; src < SPLIT; ++src) {
+                const uint32_t a = src == (int)rank
+                                       ? red_s + (uint32_t)r_base * RED_STRIDE * 4 + eoff
+                                       : recv_s + (uint32_t)(src < (int)rank ? src : src - 1) * SLICE + eoff;
+                float4 v;
+                asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                             : "r"(a));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
             }
-        }
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            const int q = j * NTHREADS + threadIdx.x;
-            const int grow = m_tile * BM + r_base + q / (BN / 4);
-            const int gcol = n_tile * BN + (q % (BN / 4)) * 4;
+            const int grow = m_tile * BM + r_base + rr;
+            const int gcol = n_tile * BN + cc;
             if (grow < p.P && gcol < p.R)
-                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc[j];
+                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
         }
-        cluster_sync();
+        cluster_sync();  // the slices this CTA sent have all been received
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, BN);
