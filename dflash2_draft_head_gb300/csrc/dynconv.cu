@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(256) dynconv_kernel(const DynParams p) {
 // HBM and release the buffer with an mbarrier arrive.  The ring keeps several
 // tiles of loads in flight per SM without holding them in registers.
 
-constexpr int PL = 8;  // positions per work item
 
 // Device fault word of the convolution kernels: DF2_FLAG_TIMEOUT when a
 // bounded wait gives up.
@@ -228,87 +227,130 @@ struct PipeParams {
 };
 
 
-// Converts one staged 8-channel bf16 row segment into four packed fp32 pairs.
-__device__ __forceinline__ void load_row_f2(uint32_t addr, float2 (&f)[4]) {
-    const uint4 v = lds_v4(addr);
-    f[0] = bf16x2_to_f2(v.x);
-    f[1] = bf16x2_to_f2(v.y);
-    f[2] = bf16x2_to_f2(v.z);
-    f[3] = bf16x2_to_f2(v.w);
+// A thread's staged row segment: NP packed bf16 pairs (NP = 4: 8 channels in
+// 16 bytes; NP = 2: 4 channels in 8 bytes), converted to fp32 pairs.
+template <int NP>
+__device__ __forceinline__ void load_row_f2(uint32_t addr, float2 (&f)[NP]) {
+    if constexpr (NP == 4) {
+        const uint4 v = lds_v4(addr);
+        f[0] = bf16x2_to_f2(v.x);
+        f[1] = bf16x2_to_f2(v.y);
+        f[2] = bf16x2_to_f2(v.z);
+        f[3] = bf16x2_to_f2(v.w);
+    } else {
+        const uint2 v = lds_v2(addr);
+        f[0] = bf16x2_to_f2(v.x);
+        f[1] = bf16x2_to_f2(v.y);
+    }
+}
+
+template <int NP>
+__device__ __forceinline__ void load_base_f2(const __nv_bfloat16* p, bool active, float2 (&f)[NP]) {
+    if constexpr (NP == 4) {
+        const uint4 v = active ? ldg_nc_v4(p) : make_uint4(0, 0, 0, 0);
+        f[0] = bf16x2_to_f2(v.x);
+        f[1] = bf16x2_to_f2(v.y);
+        f[2] = bf16x2_to_f2(v.z);
+        f[3] = bf16x2_to_f2(v.w);
+    } else {
+        const uint2 v = active ? __ldg(reinterpret_cast<const uint2*>(p)) : make_uint2(0, 0);
+        f[0] = bf16x2_to_f2(v.x);
+        f[1] = bf16x2_to_f2(v.y);
+    }
+}
+
+__device__ __forceinline__ void store_pairs(__nv_bfloat16* p, const float2 (&acc)[4]) {
+    store_row(p, acc);
+}
+__device__ __forceinline__ void store_pairs(float* p, const float2 (&acc)[4]) { store_row(p, acc); }
+__device__ __forceinline__ void store_pairs(__nv_bfloat16* p, const float2 (&acc)[2]) {
+    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0].x, acc[0].y);
+    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[1].x, acc[1].y);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&b0);
+    v.y = *reinterpret_cast<uint32_t*>(&b1);
+    *reinterpret_cast<uint2*>(p) = v;
+}
+__device__ __forceinline__ void store_pairs(float* p, const float2 (&acc)[2]) {
+    *reinterpret_cast<float4*>(p) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
 }
 
 // One output position: acc = sum_t (base_t + delta_t) * x_{i-t}; xw[t] holds x_{i-t}.
-template <int T>
-__device__ __forceinline__ void conv_point(const float2 (&bw)[T][4], const float2 (&xw)[T][4],
-                                           const __nv_bfloat16* dl, int G, float2 (&acc)[4]) {
+template <int T, int NP>
+__device__ __forceinline__ void conv_point(const float2 (&bw)[T][NP], const float2 (&xw)[T][NP],
+                                           const __nv_bfloat16* dl, int G, float2 (&acc)[NP]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int q = 0; q < NP; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
         const float dv = __bfloat162float(dl[t * G]);
         const float2 d2 = make_float2(dv, dv);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
+        for (int q = 0; q < NP; ++q)
+            acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
     }
 }
 
-// A full tile of NL positions from a staged buffer: rows 0..T-2 are the halo,
-// row T-1+l holds position l; dl points at delta[l=0][t=0][g] (stride G per tap,
-// T*G per position).  Straight-line code: the window shifts are renames.
-template <int T, typename TOut, int NL>
+// A full tile of NL positions from a staged buffer: rows 0..T-2 are the halo
+// (all zero for the first tile of a block that has no history), row T-1+l
+// holds position l; dl points at delta[l=0][t=0][g] (stride G per tap, T*G per
+// position).  Straight-line code: the window shifts are renames.
+template <int T, int NP, typename TOut, int NL>
 __device__ __forceinline__ void conv_tile(uint32_t sb, uint32_t row_bytes,
                                           const __nv_bfloat16* dl, int G, bool zero_halo,
-                                          const float2 (&bw)[T][4], TOut* op, int C) {
-    float2 xw[T][4];
+                                          const float2 (&bw)[T][NP], TOut* op, int C) {
+    float2 xw[T][NP];
 #pragma unroll
     for (int k = 0; k < T; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
+        for (int q = 0; q < NP; ++q) xw[k][q] = make_float2(0.f, 0.f);
     if (!zero_halo) {
 #pragma unroll
-        for (int r = 0; r < T - 1; ++r) load_row_f2(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
+        for (int r = 0; r < T - 1; ++r) load_row_f2<NP>(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
     }
 #pragma unroll
     for (int l = 0; l < NL; ++l) {
 #pragma unroll
         for (int k = T - 1; k > 0; --k)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
-        load_row_f2(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
-        float2 acc[4];
-        conv_point<T>(bw, xw, dl + l * T * G, G, acc);
-        store_row(op + (size_t)l * C, acc);
+            for (int q = 0; q < NP; ++q) xw[k][q] = xw[k - 1][q];
+        load_row_f2<NP>(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
+        float2 acc[NP];
+        conv_point<T, NP>(bw, xw, dl + l * T * G, G, acc);
+        store_pairs(op + (size_t)l * C, acc);
     }
 }
 
 // The last, partial tile of a sequence (nl < PL positions).
-template <int T, typename TOut>
+template <int T, int NP, typename TOut>
 __device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes,
-                                              const __nv_bfloat16* dl, int G, bool zero_halo,
-                                              const float2 (&bw)[T][4], TOut* op, int C, int nl) {
-    float2 xw[T][4];
+                                                 const __nv_bfloat16* dl, int G, bool zero_halo,
+                                                 const float2 (&bw)[T][NP], TOut* op, int C,
+                                                 int nl) {
+    float2 xw[T][NP];
 #pragma unroll
     for (int k = 0; k < T; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) xw[k][q] = make_float2(0.f, 0.f);
+        for (int q = 0; q < NP; ++q) xw[k][q] = make_float2(0.f, 0.f);
     if (!zero_halo) {
 #pragma unroll
-        for (int r = 0; r < T - 1; ++r) load_row_f2(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
+        for (int r = 0; r < T - 1; ++r) load_row_f2<NP>(sb + (uint32_t)r * row_bytes, xw[T - 2 - r]);
     }
     for (int l = 0; l < nl; ++l) {
 #pragma unroll
         for (int k = T - 1; k > 0; --k)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) xw[k][q] = xw[k - 1][q];
-        load_row_f2(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
-        float2 acc[4];
-        conv_point<T>(bw, xw, dl + l * T * G, G, acc);
-        store_row(op + (size_t)l * C, acc);
+            for (int q = 0; q < NP; ++q) xw[k][q] = xw[k - 1][q];
+        load_row_f2<NP>(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
+        float2 acc[NP];
+        conv_point<T, NP>(bw, xw, dl + l * T * G, G, acc);
+        store_pairs(op + (size_t)l * C, acc);
     }
 }
 
-template <int T, typename TOut>
-__global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
+template <int T, int PL, int NP, typename TOut>
+__global__ void __launch_bounds__(288) dynconv_pipe_kernel(const PipeParams p) {
+    constexpr int VEC = 2 * NP;  // channels per compute thread
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int nthr = p.nthr;
@@ -351,19 +393,26 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
             const int ptile = rest % p.n_ptile;
             const int s = rest / p.n_ptile;
             const int i0 = ptile * PL;
-            const int c0 = cblk * nthr * 8;
-            const uint32_t seg = (uint32_t)min(nthr * 8, p.C - c0) * 2u;
+            const int c0 = cblk * nthr * VEC;
+            const uint32_t seg = (uint32_t)min(nthr * VEC, p.C - c0) * 2u;
             const int nl = min(PL, p.n - i0);
-            const bool halo_from_hist = i0 == 0;
-            const int nhalo = (halo_from_hist && p.hist == nullptr) ? 0 : T - 1;
+            // halo row r holds position j = i0-(T-1)+r: from x when j >= 0, else from
+            // the history window (or nothing: zeros when there is no history)
+            const int nneg = max(0, (T - 1) - i0);  // halo rows before the block
+            const int nhalo = p.hist == nullptr ? (T - 1) - nneg : T - 1;
             const uint32_t fb = full0 + 8 * st;
             const uint32_t bytes = (uint32_t)(nhalo + nl) * seg + (uint32_t)(nl * TG) * 2u;
             mbar_arrive_expect_tx(fb, bytes);
             const uint32_t dst = smem0 + (uint32_t)st * p.stage_bytes;
-            for (int r = 0; r < nhalo; ++r) {
-                const __nv_bfloat16* src =
-                    halo_from_hist ? p.hist + ((size_t)s * (T - 1) + r) * p.C + c0
-                                   : p.x + ((size_t)s * p.n + i0 - (T - 1) + r) * p.C + c0;
+            for (int r = 0; r < T - 1; ++r) {
+                const int j = i0 - (T - 1) + r;
+                const __nv_bfloat16* src;
+                if (j >= 0)
+                    src = p.x + ((size_t)s * p.n + j) * p.C + c0;
+                else if (p.hist != nullptr)
+                    src = p.hist + ((size_t)s * (T - 1) + (T - 1 + j)) * p.C + c0;
+                else
+                    continue;
                 bulk_g2s(dst + (uint32_t)r * p.row_bytes, src, seg, fb);
             }
             for (int l = 0; l < nl; ++l)
@@ -378,7 +427,7 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
     // ---------------- compute threads
     int it = 0;
     int cur_cblk = -1;
-    float2 bw[T][4];
+    float2 bw[T][NP];
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
         const int st = it % p.stages;
         const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
@@ -387,36 +436,31 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
         const int ptile = rest % p.n_ptile;
         const int s = rest / p.n_ptile;
         const int i0 = ptile * PL;
-        const int cb0 = cblk * nthr * 8;
-        const int c = cb0 + tid * 8;
+        const int cb0 = cblk * nthr * VEC;
+        const int c = cb0 + tid * VEC;
         const bool active = c < p.C;
         const int nl = min(PL, p.n - i0);
         if (cblk != cur_cblk) {
             cur_cblk = cblk;
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
-                uint4 v = active ? ldg_nc_v4(p.base + (size_t)t * p.C + c) : make_uint4(0, 0, 0, 0);
-                bw[t][0] = bf16x2_to_f2(v.x);
-                bw[t][1] = bf16x2_to_f2(v.y);
-                bw[t][2] = bf16x2_to_f2(v.z);
-                bw[t][3] = bf16x2_to_f2(v.w);
-            }
+            for (int t = 0; t < T; ++t) load_base_f2<NP>(p.base + (size_t)t * p.C + c, active, bw[t]);
         }
         if (!*abort_flag && !mbar_wait_bounded(full0 + 8 * st, ph, kWaitNs)) {
             *abort_flag = 1;
             atomicOr(&g_dyn_fault, (unsigned)DF2_FLAG_TIMEOUT);
         }
         if (active && !*abort_flag) {
-            const uint32_t sb = smem0 + (uint32_t)st * p.stage_bytes + (uint32_t)tid * 16u;
+            const uint32_t sb = smem0 + (uint32_t)st * p.stage_bytes + (uint32_t)tid * (2u * VEC);
             const __nv_bfloat16* dl = reinterpret_cast<const __nv_bfloat16*>(
                 smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes) +
                 c / p.cg;
+            static_assert(PL >= T - 1, "a tile's halo must lie entirely before or inside the block");
             const bool zero_halo = (i0 == 0 && p.hist == nullptr);
             TOut* op = static_cast<TOut*>(p.out) + ((size_t)s * p.n + i0) * p.C + c;
             if (nl == PL)
-                conv_tile<T, TOut, PL>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C);
+                conv_tile<T, NP, TOut, PL>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C);
             else
-                conv_tile_ragged<T, TOut>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C, nl);
+                conv_tile_ragged<T, NP, TOut>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C, nl);
         }
         mbar_arrive(empty0 + 8 * st);
     }
@@ -427,9 +471,14 @@ __global__ void __launch_bounds__(160) dynconv_pipe_kernel(const PipeParams p) {
     }
 }
 
-template <int T, typename TOut>
+template <int T, int PL, typename TOut>
 cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
-    auto kern = dynconv_pipe_kernel<T, TOut>;
+    // 8 channels per thread up to T = 4; 4 channels (half the registers for the
+    // window and the taps, twice the threads) for longer filters
+    constexpr int NP = T <= 4 ? 4 : 2;
+    p.nthr = p.nthr * 4 / NP;  // nthr arrives as the 8-channel thread count
+    p.row_bytes = (uint32_t)p.nthr * (4u * NP);
+    auto kern = dynconv_pipe_kernel<T, PL, NP, TOut>;
     const size_t smem = (size_t)p.stages * p.stage_bytes + 2 * 8 * p.stages + 16;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -458,12 +507,12 @@ cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <typename TOut>
+template <int PL, typename TOut>
 cudaError_t launch_pipe(const PipeParams& p, int T, cudaStream_t stream) {
     switch (T) {
 #define DF2_CASE(TT) \
     case TT:         \
-        return launch_pipe_t<TT, TOut>(p, stream);
+        return launch_pipe_t<TT, PL, TOut>(p, stream);
         DF2_CASE(1) DF2_CASE(2) DF2_CASE(3) DF2_CASE(4) DF2_CASE(5) DF2_CASE(6) DF2_CASE(7)
         DF2_CASE(8)
 #undef DF2_CASE
@@ -561,17 +610,21 @@ cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream) {
         q.cg = p.cg;
         q.nthr = nthr;
         q.n_cblk = p.n_cblk;
-        q.n_ptile = (a.n + PL - 1) / PL;
+        // Tiles of 8 positions (>= T-1, so a tile's halo is either all history
+        // or all x).  Shorter tiles balance the last round better but cost more
+        // in halo copies and conversions than they gain (measured).
+        constexpr int PLsel = 8;
+        q.n_ptile = (a.n + PLsel - 1) / PLsel;
         const long long items = (long long)a.S * q.n_ptile * q.n_cblk;
         if (items <= 0x7FFFFFFFLL) {
             q.n_items = (int)items;
             q.row_bytes = (uint32_t)nthr * 16u;
-            const uint32_t raw = (uint32_t)(a.T - 1 + PL) * q.row_bytes +
-                                 (uint32_t)(PL * a.T * a.G) * 2u;
+            const uint32_t raw = (uint32_t)(a.T - 1 + PLsel) * q.row_bytes +
+                                 (uint32_t)(PLsel * a.T * a.G) * 2u;
             q.stage_bytes = (raw + 127u) & ~127u;
             q.stages = 2;
-            return a.out_bf16 ? launch_pipe<__nv_bfloat16>(q, a.T, stream)
-                              : launch_pipe<float>(q, a.T, stream);
+            return a.out_bf16 ? launch_pipe<PLsel, __nv_bfloat16>(q, a.T, stream)
+                              : launch_pipe<PLsel, float>(q, a.T, stream);
         }
     }
     if (a.in_bf16 && a.out_bf16)

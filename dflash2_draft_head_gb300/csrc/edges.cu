@@ -317,7 +317,7 @@ constexpr int EP_STAGE = 2 * EP_OP + EP_U;       // 40 KB
 constexpr int EP_GWARPS = 16;                    // gather warps (four per SM sub-partition)
 constexpr int EP_GTHREADS = EP_GWARPS * 32;
 constexpr int EP_THREADS = (9 + EP_GWARPS) * 32;  // 4 epilogue, 4 gate, 1 MMA, gather warps
-constexpr size_t EP_SMEM = 1024 + (size_t)EP_STAGES * EP_STAGE + 3 * TROWS * 4 +
+constexpr size_t EP_SMEM = 1024 + (size_t)EP_STAGES * EP_STAGE + 6 * TROWS * 4 +
                            (3 * EP_STAGES + 4) * 8 + 16;
 
 struct TileList {
@@ -343,10 +343,9 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
     const int K = p.K;
     const int R = p.R;
     const int nm1 = p.n - 1;
-    int32_t* ids_p = reinterpret_cast<int32_t*>(smem + (size_t)EP_STAGES * EP_STAGE);
-    int32_t* ids_c = ids_p + TROWS;
-    int32_t* urow = ids_c + TROWS;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(urow + TROWS);
+    int32_t* ids_p = reinterpret_cast<int32_t*>(smem + (size_t)EP_STAGES * EP_STAGE);  // [2][256]
+    int32_t* urow = ids_p + 4 * TROWS;                                                 // [2][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(urow + 2 * TROWS);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t gated0 = full0 + 8 * EP_STAGES;
     const uint32_t empty0 = gated0 + 8 * EP_STAGES;
@@ -400,37 +399,50 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
 
     if (warp >= 9) {
         // ------------------------------------------------ gather (EP_GWARPS warps)
+        // ids and u-row indices are double-buffered by tile parity and the next
+        // tile's ids are prefetched into registers while this tile is issued.
         const int gtid = tid - 9 * 32;
         const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
         const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
         bool bad = false;
-        int it = 0;
-        for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x) {
+        auto load_id = [&](int idx, int& id, int& ur) {  // thread gtid < 256: one id
+            id = 0;
+            ur = 0;
+            if (idx >= tl_list.n_items || gtid >= 2 * TROWS) return;
+            int e0, cnt;
+            tl_list.at(idx, e0, cnt);
+            const int r = gtid & (TROWS - 1);
+            const int tt = r >> log2K;
+            if (tt < cnt) {
+                const int e = e0 + tt;
+                const int s = e / nm1;
+                const int i = e % nm1 + 1;
+                const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
+                id = checked_id(p.cand_ids[(size_t)pos * K + (r & (K - 1))], p.V, bad);
+                ur = s * p.n + i;
+            }
+        };
+        int id_next, ur_next;
+        load_id(blockIdx.x, id_next, ur_next);
+        int it = 0, tl = 0;
+        for (int idx = blockIdx.x; idx < tl_list.n_items; idx += gridDim.x, ++tl) {
             int e0, cnt;
             tl_list.at(idx, e0, cnt);
             const int rows = cnt << log2K;
-            named_bar_sync(1, EP_GTHREADS);  // the previous tile's copies are all issued
-            if (gtid < 2 * TROWS) {
-                const int r = gtid & (TROWS - 1);
-                const int tt = r >> log2K;
-                const int slot = r & (K - 1);
-                int id = 0, ur = 0;
-                if (tt < cnt) {
-                    const int e = e0 + tt;
-                    const int s = e / nm1;
-                    const int i = e % nm1 + 1;
-                    const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
-                    id = checked_id(p.cand_ids[(size_t)pos * K + slot], p.V, bad);
-                    ur = s * p.n + i;
-                }
-                if (gtid < TROWS) {
-                    ids_p[r] = id;
-                    if (slot == 0) urow[tt] = ur;
-                } else {
-                    ids_c[r] = id;
-                }
+            int32_t* idp = ids_p + (tl & 1) * 2 * TROWS;  // [pred 128 | cand 128] per parity
+            int32_t* idc = idp + TROWS;
+            int32_t* urw = urow + (tl & 1) * TROWS;
+            // slot tl&1 was last read while issuing tile tl-2; every gather warp
+            // finished that before the barrier of tile tl-1 below, which this
+            // warp has passed, so the slot is free without another barrier
+            if (gtid < TROWS) {
+                idp[gtid] = id_next;
+                if ((gtid & (K - 1)) == 0) urw[gtid >> log2K] = ur_next;
+            } else if (gtid < 2 * TROWS) {
+                idc[gtid - TROWS] = id_next;
             }
             named_bar_sync(1, EP_GTHREADS);
+            load_id(idx + gridDim.x, id_next, ur_next);  // prefetch the next tile's id
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = it % EP_STAGES;
                 wait(empty0 + 8 * st, (((uint32_t)(it / EP_STAGES)) & 1u) ^ 1u);
@@ -447,15 +459,15 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
                         if (row < rows && col < R) {
                             const uint32_t off =
                                 (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
-                            cp_async16(sA + off, A + (size_t)ids_p[row] * R + col);
-                            cp_async16(sB + off, B + (size_t)ids_c[row] * R + col);
+                            cp_async16(sA + off, A + (size_t)idp[row] * R + col);
+                            cp_async16(sB + off, B + (size_t)idc[row] * R + col);
                         }
                     }
                     if (u_only_dependency && it == 0) griddep_wait();
                     for (int q = gtid; q < cnt * 16; q += EP_GTHREADS) {
                         const int col = kb * 64 + (q & 15) * 4;
                         if (col < R)
-                            cp_async16(sU + (uint32_t)q * 16u, p.u + (size_t)urow[q >> 4] * R + col);
+                            cp_async16(sU + (uint32_t)q * 16u, p.u + (size_t)urw[q >> 4] * R + col);
                     }
                 }
                 cp_async_mbar_arrive_noinc(full0 + 8 * st);

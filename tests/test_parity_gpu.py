@@ -72,6 +72,8 @@ def test_dynconv_workloads_fp32_out(name):
     dict(S=1, n=20, C=5376, T=4, G=1),     # one group; C/8 = 672 channel vectors
     dict(S=5, n=17, C=1040, T=3, G=130),   # cg = 8, many groups per block
     dict(S=2, n=40, C=2048, T=12, G=16),   # long taps, tile of 4
+    dict(S=3, n=21, C=1024, T=8, G=16),    # 4-position tiles whose halo mixes history and x
+    dict(S=1, n=7, C=1024, T=6, G=8),      # T-1 > tile length: halo spans two tiles
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_dynconv_edge_shapes(kw, dtype):
@@ -79,8 +81,9 @@ def test_dynconv_edge_shapes(kw, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_dynconv_null_history(dtype):
-    check_dynconv(W_(S=3, n=6, C=128, T=4, G=8, dtype=dtype), with_hist=False)
+@pytest.mark.parametrize("T", [4, 8])
+def test_dynconv_null_history(dtype, T):
+    check_dynconv(W_(S=3, n=13, C=128, T=T, G=8, dtype=dtype), with_hist=False)
 
 
 def test_dynconv_block_split_matches_one_run():
