@@ -221,6 +221,7 @@ struct PipeParams {
     int S, n, C, G, cg;
     int nthr, n_cblk, n_ptile;
     int n_items;
+    int ng_max;            // groups a channel block can span
     int stages;
     uint32_t row_bytes;    // nthr * 16: one staged row segment
     uint32_t stage_bytes;  // (T-1+PL) rows + PL*T*G bf16 of delta, 128-byte rounded
@@ -275,30 +276,54 @@ __device__ __forceinline__ void store_pairs(float* p, const float2 (&acc)[2]) {
     *reinterpret_cast<float4*>(p) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
 }
 
-// One output position: acc = sum_t (base_t + delta_t) * x_{i-t}; xw[t] holds x_{i-t}.
+// One output position: acc = sum_t (base_t + delta_t) * x_{i-t}; xw[t] holds
+// x_{i-t}; dtl[t] is delta_t of this thread's group (fp32, contiguous).
+// Tuning switches of the pipelined kernel, chosen by measurement on GB300
+// (long streams and the 256 x 16 batch, T = 4 and T = 8):
+//   kSplitTaps:  for T <= 4, even and odd taps accumulate separately (two FMA
+//                chains; 3 % faster at T = 4, slower at T = 8);
+//   kLanesOverGroups: the delta transpose maps lanes to groups (contiguous
+//                reads; measured slower, so off).
+constexpr bool kSplitTaps = true;
+constexpr bool kLanesOverGroups = false;
+
+// Even and odd taps may accumulate separately (two independent FMA chains per
+// channel pair), then add.
 template <int T, int NP>
 __device__ __forceinline__ void conv_point(const float2 (&bw)[T][NP], const float2 (&xw)[T][NP],
-                                           const __nv_bfloat16* dl, int G, float2 (&acc)[NP]) {
+                                           const float* dtl, float2 (&acc)[NP]) {
+    float2 odd[NP];
 #pragma unroll
-    for (int q = 0; q < NP; ++q) acc[q] = make_float2(0.f, 0.f);
+    for (int q = 0; q < NP; ++q) {
+        acc[q] = make_float2(0.f, 0.f);
+        odd[q] = make_float2(0.f, 0.f);
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        const float dv = __bfloat162float(dl[t * G]);
+        const float dv = dtl[t];
         const float2 d2 = make_float2(dv, dv);
 #pragma unroll
-        for (int q = 0; q < NP; ++q)
-            acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
+        for (int q = 0; q < NP; ++q) {
+            if (kSplitTaps && T <= 4 && (t & 1))
+                odd[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], odd[q]);
+            else
+                acc[q] = __ffma2_rn(__fadd2_rn(bw[t][q], d2), xw[t][q], acc[q]);
+        }
+    }
+    if constexpr (kSplitTaps && T > 1 && T <= 4) {
+#pragma unroll
+        for (int q = 0; q < NP; ++q) acc[q] = __fadd2_rn(acc[q], odd[q]);
     }
 }
 
 // A full tile of NL positions from a staged buffer: rows 0..T-2 are the halo
 // (all zero for the first tile of a block that has no history), row T-1+l
-// holds position l; dl points at delta[l=0][t=0][g] (stride G per tap, T*G per
-// position).  Straight-line code: the window shifts are renames.
+// holds position l; dt[l*T + t] is delta of this thread's group (fp32).
+// Straight-line code: the window shifts are renames, tap offsets immediates.
 template <int T, int NP, typename TOut, int NL>
-__device__ __forceinline__ void conv_tile(uint32_t sb, uint32_t row_bytes,
-                                          const __nv_bfloat16* dl, int G, bool zero_halo,
-                                          const float2 (&bw)[T][NP], TOut* op, int C) {
+__device__ __forceinline__ void conv_tile(uint32_t sb, uint32_t row_bytes, const float* dt,
+                                          bool zero_halo, const float2 (&bw)[T][NP], TOut* op,
+                                          int C) {
     float2 xw[T][NP];
 #pragma unroll
     for (int k = 0; k < T; ++k)
@@ -316,17 +341,16 @@ __device__ __forceinline__ void conv_tile(uint32_t sb, uint32_t row_bytes,
             for (int q = 0; q < NP; ++q) xw[k][q] = xw[k - 1][q];
         load_row_f2<NP>(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
         float2 acc[NP];
-        conv_point<T, NP>(bw, xw, dl + l * T * G, G, acc);
+        conv_point<T, NP>(bw, xw, dt + l * T, acc);
         store_pairs(op + (size_t)l * C, acc);
     }
 }
 
 // The last, partial tile of a sequence (nl < PL positions).
 template <int T, int NP, typename TOut>
-__device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes,
-                                                 const __nv_bfloat16* dl, int G, bool zero_halo,
-                                                 const float2 (&bw)[T][NP], TOut* op, int C,
-                                                 int nl) {
+__device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes, const float* dt,
+                                                 bool zero_halo, const float2 (&bw)[T][NP],
+                                                 TOut* op, int C, int nl) {
     float2 xw[T][NP];
 #pragma unroll
     for (int k = 0; k < T; ++k)
@@ -343,13 +367,16 @@ __device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes
             for (int q = 0; q < NP; ++q) xw[k][q] = xw[k - 1][q];
         load_row_f2<NP>(sb + (uint32_t)(T - 1 + l) * row_bytes, xw[0]);
         float2 acc[NP];
-        conv_point<T, NP>(bw, xw, dl + l * T * G, G, acc);
+        conv_point<T, NP>(bw, xw, dt + l * T, acc);
         store_pairs(op + (size_t)l * C, acc);
     }
 }
 
+// Register budget: 4 CTAs of 160 threads (8-channel threads) or 2 CTAs of 288
+// threads (4-channel threads) per SM.
 template <int T, int PL, int NP, typename TOut>
-__global__ void __launch_bounds__(288) dynconv_pipe_kernel(const PipeParams p) {
+__global__ void __launch_bounds__(NP == 4 ? 160 : 288, NP == 4 ? 4 : 2)
+    dynconv_pipe_kernel(const PipeParams p) {
     constexpr int VEC = 2 * NP;  // channels per compute thread
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
@@ -375,11 +402,19 @@ __global__ void __launch_bounds__(288) dynconv_pipe_kernel(const PipeParams p) {
     griddep_wait();
     griddep_launch_dependents();
 
+    // Each CTA keeps one channel block (its base taps stay in registers) and
+    // walks the (sequence, tile) pairs pt = blockIdx.x / n_cblk + k * step.
+    const int cblk = blockIdx.x % p.n_cblk;
+    const int step = gridDim.x / p.n_cblk;
+    const int n_pt = p.S * p.n_ptile;
+    const int c0 = cblk * nthr * VEC;
+
     if (tid >= nthr) {
         // ---------------- producer (one lane)
         if (tid != nthr) return;
+        const uint32_t seg = (uint32_t)min(nthr * VEC, p.C - c0) * 2u;
         int it = 0;
-        for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+        for (int pt = blockIdx.x / p.n_cblk; pt < n_pt; pt += step, ++it) {
             const int st = it % p.stages;
             const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
             if (*abort_flag) break;
@@ -388,13 +423,8 @@ __global__ void __launch_bounds__(288) dynconv_pipe_kernel(const PipeParams p) {
                 atomicOr(&g_dyn_fault, (unsigned)DF2_FLAG_TIMEOUT);
                 break;
             }
-            const int cblk = item % p.n_cblk;
-            const int rest = item / p.n_cblk;
-            const int ptile = rest % p.n_ptile;
-            const int s = rest / p.n_ptile;
-            const int i0 = ptile * PL;
-            const int c0 = cblk * nthr * VEC;
-            const uint32_t seg = (uint32_t)min(nthr * VEC, p.C - c0) * 2u;
+            const int s = pt / p.n_ptile;
+            const int i0 = (pt - s * p.n_ptile) * PL;
             const int nl = min(PL, p.n - i0);
             // halo row r holds position j = i0-(T-1)+r: from x when j >= 0, else from
             // the history window (or nothing: zeros when there is no history)
@@ -425,42 +455,65 @@ __global__ void __launch_bounds__(288) dynconv_pipe_kernel(const PipeParams p) {
     }
 
     // ---------------- compute threads
-    int it = 0;
-    int cur_cblk = -1;
+    const int c = c0 + tid * VEC;
+    const bool active = c < p.C;
+    const int c_end = min(c0 + nthr * VEC, p.C);
+    const int g_lo = c0 / p.cg;
+    const int ng = (c_end - 1) / p.cg - g_lo + 1;  // groups of this channel block
+    const int gl = active ? c / p.cg - g_lo : 0;
+    float* dt0 = reinterpret_cast<float*>(smem + (size_t)p.stages * p.stage_bytes + 256);
     float2 bw[T][NP];
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) load_base_f2<NP>(p.base + (size_t)t * p.C + c, active, bw[t]);
+    static_assert(PL >= T - 1, "a tile's halo must lie entirely before or inside the block");
+    int it = 0;
+    for (int pt = blockIdx.x / p.n_cblk; pt < n_pt; pt += step, ++it) {
         const int st = it % p.stages;
         const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
-        const int cblk = item % p.n_cblk;
-        const int rest = item / p.n_cblk;
-        const int ptile = rest % p.n_ptile;
-        const int s = rest / p.n_ptile;
-        const int i0 = ptile * PL;
-        const int cb0 = cblk * nthr * VEC;
-        const int c = cb0 + tid * VEC;
-        const bool active = c < p.C;
+        const int s = pt / p.n_ptile;
+        const int i0 = (pt - s * p.n_ptile) * PL;
         const int nl = min(PL, p.n - i0);
-        if (cblk != cur_cblk) {
-            cur_cblk = cblk;
-#pragma unroll
-            for (int t = 0; t < T; ++t) load_base_f2<NP>(p.base + (size_t)t * p.C + c, active, bw[t]);
-        }
         if (!*abort_flag && !mbar_wait_bounded(full0 + 8 * st, ph, kWaitNs)) {
             *abort_flag = 1;
             atomicOr(&g_dyn_fault, (unsigned)DF2_FLAG_TIMEOUT);
         }
+        // delta of this block's groups -> fp32 [group][l][t], groups DSTR floats
+        // apart (padded so the groups a warp reads fall in different banks),
+        // double-buffered by item
+        constexpr int DSTR = PL * T + 4;
+        float* dt = dt0 + (size_t)(it & 1) * p.ng_max * DSTR;
+        {
+            const __nv_bfloat16* dsrc = reinterpret_cast<const __nv_bfloat16*>(
+                smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes);
+            if constexpr (kLanesOverGroups) {
+                // lanes walk groups (contiguous in the staged [l][t][G] block),
+                // warps walk (l, t)
+                const int lane = tid & 31;
+                for (int lt = tid >> 5; lt < PL * T; lt += nthr >> 5) {
+                    const bool in = (lt / T) < nl;
+                    for (int gg = lane; gg < ng; gg += 32)
+                        dt[gg * DSTR + lt] =
+                            in ? __bfloat162float(dsrc[lt * p.G + g_lo + gg]) : 0.f;
+                }
+            } else {
+                for (int q = tid; q < ng * PL * T; q += nthr) {
+                    const int lt = q % (PL * T);
+                    const int gg = q / (PL * T);
+                    dt[gg * DSTR + lt] =
+                        (lt / T) < nl ? __bfloat162float(dsrc[lt * p.G + g_lo + gg]) : 0.f;
+                }
+            }
+        }
+        named_bar_sync(1, (uint32_t)nthr);
         if (active && !*abort_flag) {
             const uint32_t sb = smem0 + (uint32_t)st * p.stage_bytes + (uint32_t)tid * (2u * VEC);
-            const __nv_bfloat16* dl = reinterpret_cast<const __nv_bfloat16*>(
-                smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes) +
-                c / p.cg;
-            static_assert(PL >= T - 1, "a tile's halo must lie entirely before or inside the block");
+            const float* dtg = dt + (size_t)gl * DSTR;
             const bool zero_halo = (i0 == 0 && p.hist == nullptr);
             TOut* op = static_cast<TOut*>(p.out) + ((size_t)s * p.n + i0) * p.C + c;
             if (nl == PL)
-                conv_tile<T, NP, TOut, PL>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C);
+                conv_tile<T, NP, TOut, PL>(sb, p.row_bytes, dtg, zero_halo, bw, op, p.C);
             else
-                conv_tile_ragged<T, NP, TOut>(sb, p.row_bytes, dl, p.G, zero_halo, bw, op, p.C, nl);
+                conv_tile_ragged<T, NP, TOut>(sb, p.row_bytes, dtg, zero_halo, bw, op, p.C, nl);
         }
         mbar_arrive(empty0 + 8 * st);
     }
@@ -479,7 +532,10 @@ cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
     p.nthr = p.nthr * 4 / NP;  // nthr arrives as the 8-channel thread count
     p.row_bytes = (uint32_t)p.nthr * (4u * NP);
     auto kern = dynconv_pipe_kernel<T, PL, NP, TOut>;
-    const size_t smem = (size_t)p.stages * p.stage_bytes + 2 * 8 * p.stages + 16;
+    p.ng_max = (p.nthr * 2 * NP - 1) / p.cg + 2;
+    // stages, then the mbarriers (<= 256 bytes), then two transposed delta buffers
+    const size_t smem = (size_t)p.stages * p.stage_bytes + 256 +
+                        2 * (size_t)p.ng_max * (PL * T + 4) * sizeof(float);
     int dev = 0;
     cudaGetDevice(&dev);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -491,7 +547,11 @@ cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const long long grid = std::min<long long>((long long)sms * per_sm, p.n_items);
+    // a multiple of n_cblk: every CTA keeps one channel block
+    const long long n_pt = (long long)p.S * p.n_ptile;
+    const long long per_cblk = std::max<long long>(
+        1, std::min<long long>((long long)sms * per_sm / p.n_cblk, n_pt));
+    const long long grid = per_cblk * p.n_cblk;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)(p.nthr + 32));
