@@ -6,6 +6,6 @@ grouped dynamic depthwise causal convolution and the candidate selector
 ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local convolution
 + candidate selector)".  This package is the thin Python binding over it.
 """
-from .binding import (Dflash2Error, dynconv, edges, lib, project, select,  # noqa: F401
-                      take_device_faults, version)
+from .binding import (Dflash2Error, dynconv, edges, lib, project,  # noqa: F401
+                      project_workspace_bytes, select, take_device_faults, version)
 from .build import build as build_library  # noqa: F401

@@ -51,6 +51,10 @@ def lib() -> ctypes.CDLL:
             L.dflash2_dynconv.restype = i
             L.dflash2_project.argtypes = [vp, vp, vp, i, i, i, i, vp]
             L.dflash2_project.restype = i
+            L.dflash2_project_workspace_bytes.argtypes = [i, i, i]
+            L.dflash2_project_workspace_bytes.restype = ctypes.c_size_t
+            L.dflash2_project_ws.argtypes = [vp, vp, vp, i, i, i, i, vp, ctypes.c_size_t, vp]
+            L.dflash2_project_ws.restype = i
             L.dflash2_edges.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, vp, vp]
             L.dflash2_edges.restype = i
             L.dflash2_select.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp,
@@ -117,8 +121,15 @@ def dynconv(x, hist, base, delta, out=None, out_dtype=None):
     return out
 
 
-def project(h, W, u=None):
-    """u [P,R] fp32 = h [P,d] @ W[R,d]^T."""
+def project_workspace_bytes(P: int, d: int, R: int) -> int:
+    """Bytes of split-K workspace project(..., workspace=...) needs on this device."""
+    return int(lib().dflash2_project_workspace_bytes(P, d, R))
+
+
+def project(h, W, u=None, workspace=None):
+    """u [P,R] fp32 = h [P,d] @ W[R,d]^T.  With `workspace` (a CUDA tensor of at
+    least project_workspace_bytes(P, d, R) bytes) the split-K partial tiles are
+    exchanged through it instead of through distributed shared memory."""
     P, d = h.shape
     R = W.shape[0]
     _need(h, "h")
@@ -126,8 +137,15 @@ def project(h, W, u=None):
     if u is None:
         u = torch.empty((P, R), dtype=torch.float32, device=h.device)
     _need(u, "u", torch.float32)
-    _check(lib().dflash2_project(_ptr(h), _ptr(W), _ptr(u), P, d, R, _code(h.dtype),
-                                 _stream(h.device)))
+    if workspace is None:
+        _check(lib().dflash2_project(_ptr(h), _ptr(W), _ptr(u), P, d, R, _code(h.dtype),
+                                     _stream(h.device)))
+    else:
+        _need(workspace, "workspace")
+        _check(lib().dflash2_project_ws(_ptr(h), _ptr(W), _ptr(u), P, d, R, _code(h.dtype),
+                                        _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(h.device)))
     return u
 
 

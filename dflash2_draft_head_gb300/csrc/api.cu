@@ -151,8 +151,9 @@ int run_edges(const int32_t* cand_ids, const float* u, const void* A, const void
 }
 
 int run_project(const void* h, const void* W, float* u, int P, int d, int R, int dtype,
-                cudaStream_t stream) {
+                cudaStream_t stream, float* ws = nullptr) {
     df2::ProjectArgs a{h, W, u, P, d, R};
+    a.ws = ws;
     cudaError_t e = dtype == DF2_BF16
                         ? df2::launch_project_bf16_tc(a, stream, num_sms_of_current_device())
                         : df2::launch_project_f32(a, stream);
@@ -223,6 +224,36 @@ int dflash2_project(const void* h, const void* W, float* u, int P, int d, int R,
     int st = validate_project(h, W, u, P, d, R, in_dtype);
     if (st != DF2_OK) return st;
     return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream));
+}
+
+size_t dflash2_project_workspace_bytes(int P, int d, int R) {
+    if (P <= 0 || d <= 0 || R <= 0) return 0;
+    return df2::project_workspace_bytes(P, d, R, num_sms_of_current_device());
+}
+
+int dflash2_project_ws(const void* h, const void* W, float* u, int P, int d, int R, int in_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    int st = validate_project(h, W, u, P, d, R, in_dtype);
+    if (st != DF2_OK) return st;
+    if (in_dtype != DF2_BF16)  // the fp32 path has no split-K reduction
+        return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream));
+    const size_t need = df2::project_workspace_bytes(P, d, R, num_sms_of_current_device());
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(DF2_ERR_INVALID_ARG, "project_ws: workspace of %zu bytes needed, got %zu",
+                        need, workspace == nullptr ? (size_t)0 : workspace_bytes);
+        if (!aligned16(workspace))
+            return fail(DF2_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+        const size_t b = esize(in_dtype);
+        const Buf ws[1] = {{workspace, need, "workspace"}};
+        const Buf others[3] = {{h, (size_t)P * d * b, "h"}, {W, (size_t)R * d * b, "W"},
+                               {u, (size_t)P * R * 4, "u"}};
+        st = check_disjoint(ws, 1, others, 3);
+        if (st != DF2_OK) return st;
+    }
+    return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream),
+                       need > 0 ? static_cast<float*>(workspace) : nullptr);
 }
 
 int dflash2_edges(const int32_t* cand_ids, const float* u, const void* A, const void* B,

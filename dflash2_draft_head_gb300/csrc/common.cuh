@@ -27,6 +27,7 @@ struct ProjectArgs {
     const void* W;
     float* u;
     int P, d, R;
+    float* ws = nullptr;  // optional split-K workspace (project_workspace_bytes)
 };
 
 struct EdgesArgs {
@@ -51,6 +52,8 @@ cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream);
 // Reads and clears the convolution kernels' device fault word (synchronous).
 cudaError_t take_dynconv_faults(unsigned* flags);
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
+// Bytes of split-K workspace the bf16 projection uses for these shapes (0: none).
+size_t project_workspace_bytes(int P, int d, int R, int num_sms);
 cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
 // Reads and clears the projection kernel's device fault word (synchronous).
 cudaError_t take_project_faults(unsigned* flags);

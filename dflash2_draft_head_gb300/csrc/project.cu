@@ -53,6 +53,9 @@ struct ProjParams {
     int P, R;
     int kblocks;
     int splitk;
+    // Optional split-K workspace [tiles][SPLIT][128][BN] fp32; nullptr selects the
+    // reduction through distributed shared memory.
+    float* ws;
 };
 
 template <int SPLIT>
@@ -168,6 +171,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc_fence_before();
         __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, BN);
+        }
+    } else if (p.ws != nullptr) {
+        // Split-K reduction through an L2-resident workspace.  CTA r of the
+        // cluster owns rows [r*RP, (r+1)*RP).  Every CTA stages its partial tile
+        // in shared memory, writes the slices the other CTAs own to its slot of
+        // the workspace, and after one cluster barrier each owner sums the SPLIT
+        // slices in rank order (deterministic): its own from shared memory, the
+        // others from the workspace.
+        constexpr int RP = BM / SPLIT;
+        float* red = reinterpret_cast<float*>(stages);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld_wait();
+            float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+        __syncthreads();
+        const size_t tile = (size_t)m_tile * gridDim.z + n_tile;
+        float* wsl = p.ws + (tile * SPLIT + rank) * (size_t)BM * BN;  // this CTA's slot
+        for (int q = threadIdx.x; q < BM * (BN / 4); q += NTHREADS) {
+            const int rr = q / (BN / 4);
+            if (rr / RP == (int)rank) continue;  // own rows stay in shared memory
+            const int cc = (q % (BN / 4)) * 4;
+            *reinterpret_cast<float4*>(wsl + (size_t)rr * BN + cc) =
+                *reinterpret_cast<const float4*>(red + (size_t)rr * RED_STRIDE + cc);
+        }
+        tc_fence_before();
+        cluster_sync();  // every slice is written (release/acquire across the cluster)
+        const int r_base = (int)rank * RP;
+        for (int q = threadIdx.x; q < RP * (BN / 4); q += NTHREADS) {
+            const int rr = r_base + q / (BN / 4);
+            const int cc = (q % (BN / 4)) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int src = 0; src < SPLIT; ++src) {
+                const float4 v =
+                    src == (int)rank
+                        ? *reinterpret_cast<const float4*>(red + (size_t)rr * RED_STRIDE + cc)
+                        : __ldcg(reinterpret_cast<const float4*>(
+                              p.ws + ((tile * SPLIT + src) * BM + rr) * (size_t)BN + cc));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const int grow = m_tile * BM + rr;
+            const int gcol = n_tile * BN + cc;
+            if (grow < p.P && gcol < p.R)
+                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
+        }
         if (warp == 1) {
             tc_fence_after();
             tmem_dealloc(tmem, BN);
@@ -304,6 +365,16 @@ __global__ void __launch_bounds__(256) project_f32_kernel(const float* __restric
 
 }  // namespace
 
+size_t project_workspace_bytes(int P, int d, int R, int num_sms) {
+    const int kblocks = (d + BK - 1) / BK;
+    const int m_tiles = (P + BM - 1) / BM;
+    const int n_tiles = (R + BN - 1) / BN;
+    const int tiles = m_tiles * n_tiles;
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= num_sms && kblocks >= split * 4) split *= 2;
+    return split == 1 ? 0 : (size_t)tiles * split * BM * BN * sizeof(float);
+}
+
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms) {
     CUtensorMap tmA, tmB;
     if (!make_tmap_rows_bf16(&tmA, a.h, a.P, a.d, BM) || !make_tmap_rows_bf16(&tmB, a.W, a.R, a.d, BN))
@@ -324,7 +395,7 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
     cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)SMEM_BYTES);
     if (e0 != cudaSuccess) return e0;
-    ProjParams p{a.u, a.P, a.R, kblocks, split};
+    ProjParams p{a.u, a.P, a.R, kblocks, split, a.ws};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)split, (unsigned)m_tiles, (unsigned)n_tiles);
     cfg.blockDim = dim3(NTHREADS, 1, 1);

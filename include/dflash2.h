@@ -105,6 +105,29 @@ int dflash2_project(const void* h, const void* W, float* u, int P, int d, int R,
                     int in_dtype, void* stream);
 
 /*
+ * Bytes of workspace dflash2_project_ws needs for these shapes on the current
+ * device (0 when the projection is not split along d, or for bad sizes).
+ */
+size_t dflash2_project_workspace_bytes(int P, int d, int R);
+
+/*
+ * dflash2_project with a caller-provided split-K workspace (same operation and
+ * result, bit for bit).  When the projection is split along d across the CTAs
+ * of a cluster, the partial tiles are exchanged through this L2-resident
+ * workspace (one cluster barrier) instead of through distributed shared
+ * memory; this is faster for the few-row, deeply split shapes of a single
+ * draft step.  workspace: device memory of at least
+ * dflash2_project_workspace_bytes(P, d, R) bytes, 16-byte aligned, disjoint
+ * from h, W and u, unused by anything else while the call runs (calls that
+ * share one workspace must not overlap on the GPU); its contents on entry
+ * are irrelevant and on exit undefined.  May be NULL when that size is 0.
+ * F32 input ignores the workspace.  Errors as dflash2_project, plus
+ * INVALID_ARG for a missing, short, misaligned or overlapping workspace.
+ */
+int dflash2_project_ws(const void* h, const void* W, float* u, int P, int d, int R,
+                       int in_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Edge scores with the fused per-predecessor argmax (PR #27342, Overview,
  * second formula).  For s < S, position i in 1..n-1 (the candidates of
  * position i-1 are the predecessors), slots p, c < K:

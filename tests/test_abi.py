@@ -121,3 +121,21 @@ def test_select_validation(L):
 
 def test_take_device_faults_rejects_null(L):
     assert L.dflash2_take_device_faults(None) == 1
+
+
+def test_project_ws_validation(L):
+    L.dflash2_project_workspace_bytes.restype = ctypes.c_size_t
+    L.dflash2_project_workspace_bytes.argtypes = [ctypes.c_int] * 3
+    need = L.dflash2_project_workspace_bytes(4096, 5120, 128)
+    assert need > 0 and need % 16 == 0
+    assert L.dflash2_project_workspace_bytes(0, 5120, 128) == 0
+    f = L.dflash2_project_ws
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                               ctypes.c_void_p]
+    args = [P[0], P[1], P[2], 4096, 5120, 128, 1]
+    assert f(*args, None, 0, None) == 1                       # workspace missing
+    assert f(*args, P[3], need - 16, None) == 1               # workspace too small
+    assert f(*args, ctypes.c_void_p(0x40000008), need, None) == 1  # misaligned
+    assert f(*args, P[0], need, None) == 1                    # overlaps h
+    assert b"workspace" in L.dflash2_last_error()
+    assert f(P[0], P[1], P[2], 4096, 5120, 12, 1, P[3], need, None) == 2  # R % 8

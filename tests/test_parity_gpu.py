@@ -166,6 +166,38 @@ def test_project_edge_shapes(kw, dtype):
     check_project(W_(dtype=dtype, C=64, G=4, **kw))
 
 
+def check_project_ws(w):
+    """The workspace variant: oracle parity and bit-identical to the plain call."""
+    cb = synth.codebooks(w)
+    sel = synth.selector_inputs(w)
+    h = dev(sel["h"], w.dtype)
+    W = dev(cb["W"], w.dtype)
+    nbytes = df2.project_workspace_bytes(w.P, w.d, w.R)
+    ws = torch.full((max(nbytes // 4, 1),), float("nan"), device="cuda")  # contents irrelevant
+    u_ws = df2.project(h, W, workspace=ws)
+    u = df2.project(h, W)
+    torch.cuda.synchronize()
+    ref = oracle.project(sel["h"].numpy(), cb["W"].numpy())
+    assert_close(host(u_ws), ref, w.dtype, f"project_ws {w.name}")
+    assert torch.equal(u_ws, u)
+
+
+@pytest.mark.parametrize("name", [w.name for w in WORKLOADS])
+def test_project_ws_workloads(name):
+    check_project_ws(BY[name])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(S=1, n=1, d=64, R=16),
+    dict(S=3, n=43, d=200, R=24),
+    dict(S=4, n=64, d=1032, R=136),
+    dict(S=2, n=100, d=5120, R=512),
+    dict(S=64, n=40, d=5120, R=128),
+])
+def test_project_ws_edge_shapes(kw):
+    check_project_ws(W_(C=64, G=4, **kw))
+
+
 # ------------------------------------------------------------------ edges
 
 def check_edges(w, with_edges=True, u_src=None):
