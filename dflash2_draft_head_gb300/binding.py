@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_project_workspace_bytes.restype = ctypes.c_size_t
             L.dflash2_project_ws.argtypes = [vp, vp, vp, i, i, i, i, vp, ctypes.c_size_t, vp]
             L.dflash2_project_ws.restype = i
+            L.dflash2_project_noalloc.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.dflash2_project_noalloc.restype = i
             L.dflash2_edges.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, vp, vp]
             L.dflash2_edges.restype = i
             L.dflash2_select.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp,
@@ -146,6 +148,21 @@ def project(h, W, u=None, workspace=None):
                                         _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
                                         _stream(h.device)))
+    return u
+
+
+def project_noalloc(h, W, u=None):
+    """project() through the library's fixed workspace (no device allocation by
+    the library; u must be passed to avoid torch allocating it)."""
+    P, d = h.shape
+    R = W.shape[0]
+    _need(h, "h")
+    _need(W, "W", h.dtype)
+    if u is None:
+        u = torch.empty((P, R), dtype=torch.float32, device=h.device)
+    _need(u, "u", torch.float32)
+    _check(lib().dflash2_project_noalloc(_ptr(h), _ptr(W), _ptr(u), P, d, R, _code(h.dtype),
+                                         _stream(h.device)))
     return u
 
 

@@ -302,6 +302,27 @@ int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const 
                      best_score, err_flag, s, dtype == DF2_BF16 ? 1 : 0);
 }
 
+int dflash2_project_noalloc(const void* h, const void* W, float* u, int P, int d, int R,
+                            int in_dtype, void* stream) {
+    g_err[0] = 0;
+    int st = validate_project(h, W, u, P, d, R, in_dtype);
+    if (st != DF2_OK) return st;
+    if (in_dtype != DF2_BF16)  // the fp32 path uses no workspace
+        return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream));
+    const size_t need = df2::project_workspace_bytes(P, d, R, num_sms_of_current_device());
+    if (need > df2::kFixedProjectWorkspaceBytes)
+        return fail(DF2_ERR_UNSUPPORTED,
+                    "project_noalloc: these shapes need %zu bytes of workspace, more than the "
+                    "library's fixed %zu; use dflash2_project_ws with your own workspace",
+                    need, df2::kFixedProjectWorkspaceBytes);
+    float* ws = nullptr;
+    if (need > 0) {
+        cudaError_t e = df2::fixed_project_workspace(&ws);
+        if (e != cudaSuccess) return cuda_fail(e, "project_noalloc workspace address");
+    }
+    return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream), ws);
+}
+
 int dflash2_take_device_faults(int32_t* flags_out) {
     g_err[0] = 0;
     if (flags_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "flags_out is NULL");

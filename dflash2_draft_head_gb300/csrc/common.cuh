@@ -54,6 +54,10 @@ cudaError_t take_dynconv_faults(unsigned* flags);
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
 // Bytes of split-K workspace the bf16 projection uses for these shapes (0: none).
 size_t project_workspace_bytes(int P, int d, int R, int num_sms);
+// Size of the library's own fixed projection workspace (8 MiB).
+constexpr size_t kFixedProjectWorkspaceBytes = size_t(8) << 20;
+// Device address of that workspace on the current device (looked up on first use).
+cudaError_t fixed_project_workspace(float** ptr);
 cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
 // Reads and clears the projection kernel's device fault word (synchronous).
 cudaError_t take_project_faults(unsigned* flags);

@@ -23,6 +23,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "dflash2.h"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -413,6 +415,39 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fixed workspace
+//
+// A split-K workspace that lives in the library itself, for callers that are
+// not allowed to allocate device memory.  Every GPU that loads the library
+// holds it until the process exits.  All calls share it: calls that overlap on
+// the GPU race on it.  Nothing in it has to start at zero (each call writes
+// every slot it reads), so it is never cleared.
+static __device__ __align__(256) float g_fixed_ws[kFixedProjectWorkspaceBytes / sizeof(float)];
+
+namespace {
+std::mutex g_fixed_ws_mu;
+float* g_fixed_ws_ptr[64] = {};
+}  // namespace
+
+// Device address of g_fixed_ws on the current device.  The first call on a
+// device looks it up (cudaGetSymbolAddress, with that device current) and
+// caches it; the name itself is only a host-side stand-in.
+cudaError_t fixed_project_workspace(float** ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_fixed_ws_mu);
+    if (g_fixed_ws_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fixed_ws);
+        if (e != cudaSuccess) return e;
+        g_fixed_ws_ptr[dev] = static_cast<float*>(p);
+    }
+    *ptr = g_fixed_ws_ptr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t take_project_faults(unsigned* flags) {

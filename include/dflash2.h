@@ -172,6 +172,31 @@ int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const 
                    float* best_score, int32_t* err_flag, void* stream);
 
 /*
+ * dflash2_project for callers that cannot allocate device memory: plugins and
+ * custom operators inside an inference runtime that owns the whole device pool
+ * and hands them only their input and output tensors, or decode loops where an
+ * allocation call (which may synchronise the device) is not allowed.  (No
+ * counterpart in the DFlash2 pull request: this is a deployment convenience of
+ * this library.)  Same operation and result as dflash2_project_ws, but the
+ * split-K workspace is the library's own fixed 8 MiB device array, so nothing
+ * is allocated.  The caller still passes h, W and u.
+ *   - Shapes that need more than 8 MiB of workspace (see
+ *     dflash2_project_workspace_bytes; e.g. more than 4096 rows at R = 128 on
+ *     152 SMs) return DF2_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device uses the same array, so calls that overlap on the
+ *     GPU (different streams, or different host threads) race and give wrong
+ *     results; serialise them.  The array keeps the last call's contents;
+ *     nothing needs to start at zero.
+ *   - F32 input uses no workspace.
+ * Errors as dflash2_project, plus DF2_ERR_UNSUPPORTED for oversized shapes.
+ */
+int dflash2_project_noalloc(const void* h, const void* W, float* u, int P, int d, int R,
+                            int in_dtype, void* stream);
+
+/*
  * Reads and clears the library's device-side fault word for the current
  * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_project gave
  * up).  Synchronises the current device.  Returns DF2_OK or DF2_ERR_CUDA.
