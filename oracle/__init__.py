@@ -61,6 +61,8 @@ def _load():
             lib.oracle_select.argtypes = [dp, dp, ip, dp, dp, dp, L, L, L, L, L, L,
                                           dp, dp, ip, dp]
             lib.oracle_select.restype = ctypes.c_int
+            lib.oracle_topk.argtypes = [dp, L, L, L, ip, dp]
+            lib.oracle_topk.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -174,6 +176,18 @@ def select(h, W, cand_ids, A, B, unary, want_edges=True):
     if rc != 0:
         raise ValueError("oracle_select: candidate id outside [0, V)")
     return u, e, slot, score
+
+
+def topk(z, K):
+    """(ids [rows,K] int32, vals [rows,K] float64): the K largest of each row of
+    z [rows,V], descending, ties by ascending index."""
+    z = _f64(z)
+    rows, V = z.shape
+    ids = np.empty((rows, K), np.int32)
+    vals = np.empty((rows, K), np.float64)
+    if _load().oracle_topk(_dp(z), rows, V, K, _ip(ids), _dp(vals)) != 0:
+        raise ValueError("oracle_topk: need 1 <= K <= V")
+    return ids, vals
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -29,8 +29,10 @@
  * values.  OpenMP only splits the outermost independent loop; it changes no
  * arithmetic and no summation order.
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #ifdef _OPENMP
 #include <omp.h>
@@ -159,4 +161,49 @@ int oracle_select(const double* h, const double* W, const int32_t* cand_ids,
     oracle_project(h, W, u, S * n, d, R);
     return oracle_edges(cand_ids, u, A, B, unary, S, n, K, R, V, edges, best_slot,
                         best_score);
+}
+
+/*
+ * Top-K candidate extraction, the step before the selector (the pull request's
+ * review thread: the selector works on the top K of V-wide rows with small K).
+ * Reading taken: for row r of draft logits z[r, 0..V-1], ids[r, 0..K-1] are the
+ * K indices with the largest values, in descending order of value, equal
+ * values ordered by ascending index; vals[r, k] = z[r, ids[r, k]] (the
+ * draft's own score of that candidate).  K rounds of a full scan for the best
+ * element not yet taken.  Degenerate inputs (the text says nothing of them):
+ * a NaN entry is never a candidate, and when a row holds fewer than K entries
+ * that are not NaN the remaining slots get id -1 and value NaN; -0 and +0 are
+ * equal (the lower index comes first), as the comparison below already gives.
+ * Returns 0, or 1 if K > V or K < 1 (or no memory).
+ */
+int oracle_topk(const double* z, long rows, long V, long K, int32_t* ids, double* vals) {
+    if (K < 1 || K > V) return 1;
+    int fail = 0;
+    long r;
+#pragma omp parallel for schedule(static) reduction(| : fail)
+    for (r = 0; r < rows; ++r) {
+        const double* zr = z + r * V;
+        unsigned char* taken = (unsigned char*)calloc((size_t)V, 1);
+        if (taken == NULL) {
+            fail = 1;
+            continue;
+        }
+        for (long k = 0; k < K; ++k) {
+            long best = -1;
+            for (long j = 0; j < V; ++j) {
+                if (taken[j] || isnan(zr[j])) continue;
+                if (best < 0 || zr[j] > zr[best]) best = j;  /* strict: lower index wins ties */
+            }
+            if (best < 0) {
+                ids[r * K + k] = -1;
+                vals[r * K + k] = NAN;
+                continue;
+            }
+            taken[best] = 1;
+            ids[r * K + k] = (int32_t)best;
+            vals[r * K + k] = zr[best];
+        }
+        free(taken);
+    }
+    return fail;
 }

@@ -318,3 +318,69 @@ def test_select_is_project_then_edges():
     e2, slot2, score2 = oracle.edges(ids, h @ W.T, A, B, unary)
     np.testing.assert_allclose(e, e2, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(slot, slot2)
+
+
+# ---------------------------------------------------------------- top-K pins
+
+def test_topk_golden_hand_worked():
+    g = json.load(open(os.path.join(GOLD, "topk_hand.json")))
+    for case in g["cases"]:
+        ids, vals = oracle.topk(np.array(case["z"], float), case["K"])
+        np.testing.assert_array_equal(ids, np.array(case["ids"]))
+        want = np.array(case["vals"], float)
+        np.testing.assert_array_equal(vals, want)                # NaN == NaN here
+        np.testing.assert_array_equal(np.signbit(vals), np.signbit(want))
+
+
+@pytest.mark.parametrize("V,K", [(1, 1), (17, 1), (50, 7), (64, 64), (300, 16)])
+def test_topk_is_numpy_lexsort(V, K):
+    """Library sort: order by (-value, index) and take the first K."""
+    rng = _rng(V * 7 + K)
+    z = np.round(rng.standard_normal((5, V)) * 4) / 4  # coarse values: many ties
+    ids, vals = oracle.topk(z, K)
+    for r in range(5):
+        order = np.lexsort((np.arange(V), -z[r]))[:K]
+        np.testing.assert_array_equal(ids[r], order)
+        np.testing.assert_array_equal(vals[r], z[r][order])
+
+
+def test_topk_k1_is_argmax_and_invariants():
+    rng = _rng(31)
+    z = rng.standard_normal((8, 1000))
+    ids, vals = oracle.topk(z, 1)
+    np.testing.assert_array_equal(ids[:, 0], np.argmax(z, axis=1))
+    ids, vals = oracle.topk(z, 20)
+    assert np.all(np.diff(vals, axis=1) <= 0)                  # non-increasing
+    for r in range(8):
+        rest = np.delete(z[r], ids[r])
+        assert rest.max() <= vals[r].min()                      # nothing better left out
+        assert len(set(ids[r].tolist())) == 20
+
+
+def test_topk_rejects_bad_k():
+    with pytest.raises(ValueError):
+        oracle.topk(np.zeros((1, 4)), 5)
+    with pytest.raises(ValueError):
+        oracle.topk(np.zeros((1, 4)), 0)
+
+
+def test_topk_nan_and_inf_rows():
+    """Brute force over a masked row: NaN entries never chosen, -inf only when
+    nothing larger is left, short rows padded with id -1."""
+    rng = _rng(77)
+    z = rng.standard_normal((6, 40))
+    z[0, ::3] = np.nan
+    z[1, :] = -np.inf
+    z[1, 7] = 0.5
+    z[2, :] = np.nan
+    z[2, 5] = -np.inf
+    ids, vals = oracle.topk(z, 30)
+    for r in range(6):
+        ok = np.flatnonzero(~np.isnan(z[r]))
+        order = ok[np.lexsort((ok, -z[r][ok]))][:30]
+        m = len(order)
+        np.testing.assert_array_equal(ids[r, :m], order)
+        np.testing.assert_array_equal(vals[r, :m], z[r][order])
+        assert np.all(ids[r, m:] == -1) and np.all(np.isnan(vals[r, m:]))
+    assert ids[1, 0] == 7 and ids[1, 1] == 0          # 0.5 first, then -inf by index
+    assert ids[2, 0] == 5 and np.all(ids[2, 1:] == -1)
