@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libdflash2.so")
 
 DF2_OK, DF2_ERR_INVALID_ARG, DF2_ERR_UNSUPPORTED, DF2_ERR_CUDA = 0, 1, 2, 3
 DF2_F32, DF2_BF16 = 0, 1
-FLAG_BAD_ID, FLAG_TIMEOUT = 1, 2
+FLAG_BAD_ID, FLAG_TIMEOUT, FLAG_OVERFLOW = 1, 2, 4
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_select.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp,
                                          vp, vp, vp]
             L.dflash2_select.restype = i
+            L.dflash2_topk.argtypes = [vp, i, i, i, i, vp, vp, vp]
+            L.dflash2_topk.restype = i
             L.dflash2_take_device_faults.argtypes = [ctypes.POINTER(ctypes.c_int32)]
             L.dflash2_take_device_faults.restype = i
             _lib = L
@@ -224,6 +226,26 @@ def select(h, W, cand_ids, A, B, unary, u_out=None, edges_out=None, best_slot=No
                                 _ptr(best_slot), _ptr(best_score), _ptr(err_flag),
                                 _stream(h.device)))
     return u_out, edges_out, best_slot, best_score
+
+
+def topk(logits, K, cand_ids=None, values=None):
+    """Top-K candidates of every row: logits [..., V] (fp32 or bf16) ->
+    (cand_ids [..., K] int32, values [..., K] fp32), descending, ties by index."""
+    V = logits.shape[-1]
+    lead = tuple(logits.shape[:-1])
+    rows = 1
+    for s in lead:
+        rows *= s
+    _need(logits, "logits")
+    if cand_ids is None:
+        cand_ids = torch.empty(lead + (K,), dtype=torch.int32, device=logits.device)
+    if values is None:
+        values = torch.empty(lead + (K,), dtype=torch.float32, device=logits.device)
+    _need(cand_ids, "cand_ids", torch.int32)
+    _need(values, "values", torch.float32)
+    _check(lib().dflash2_topk(_ptr(logits), rows, V, K, _code(logits.dtype), _ptr(cand_ids),
+                              _ptr(values), _stream(logits.device)))
+    return cand_ids, values
 
 
 def take_device_faults() -> int:

@@ -323,6 +323,30 @@ int dflash2_project_noalloc(const void* h, const void* W, float* u, int P, int d
     return run_project(h, W, u, P, d, R, in_dtype, static_cast<cudaStream_t>(stream), ws);
 }
 
+int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32_t* cand_ids,
+                 float* values, void* stream) {
+    g_err[0] = 0;
+    if (logits == nullptr || cand_ids == nullptr || values == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "topk: NULL logits, cand_ids or values");
+    if (rows <= 0 || V <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "topk: rows=%d V=%d must be positive", rows, V);
+    if (K < 1 || K > V) return fail(DF2_ERR_INVALID_ARG, "topk: K=%d outside [1, V=%d]", K, V);
+    if (!valid_dtype(in_dtype)) return fail(DF2_ERR_INVALID_ARG, "topk: bad dtype %d", in_dtype);
+    const Buf ins[1] = {{logits, (size_t)rows * V * esize(in_dtype), "logits"}};
+    const Buf outs[2] = {{cand_ids, (size_t)rows * K * 4, "cand_ids"},
+                         {values, (size_t)rows * K * 4, "values"}};
+    int st = check_aligned(ins, 1);
+    if (st == DF2_OK) st = check_aligned(outs, 2);
+    if (st == DF2_OK) st = check_disjoint(outs, 2, ins, 1);
+    if (st != DF2_OK) return st;
+    if (K > df2::kTopkMaxK)
+        return fail(DF2_ERR_UNSUPPORTED, "topk: K=%d > %d", K, df2::kTopkMaxK);
+    df2::TopkLaunch a{logits, rows, V, K, in_dtype == DF2_BF16, cand_ids, values};
+    cudaError_t e = df2::launch_topk(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+    return DF2_OK;
+}
+
 int dflash2_take_device_faults(int32_t* flags_out) {
     g_err[0] = 0;
     if (flags_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "flags_out is NULL");
@@ -331,6 +355,8 @@ int dflash2_take_device_faults(int32_t* flags_out) {
     unsigned v2 = 0;
     if (e == cudaSuccess) e = df2::take_project_faults(&v);
     if (e == cudaSuccess) e = df2::take_dynconv_faults(&v2);
+    v |= v2;
+    if (e == cudaSuccess) e = df2::take_topk_faults(&v2);
     v |= v2;
     if (e != cudaSuccess) return cuda_fail(e, "take_device_faults");
     *flags_out = (int32_t)v;

@@ -43,6 +43,17 @@ struct EdgesArgs {
     int32_t* err_flag;
 };
 
+// Largest K the top-K kernel takes.
+constexpr int kTopkMaxK = 1024;
+
+struct TopkLaunch {
+    const void* logits;
+    int rows, V, K;
+    int bf16;
+    int32_t* ids;
+    float* vals;
+};
+
 // 2-D bf16 tensor map over a row-major [rows, cols] array with a box of
 // box_rows x 64 columns and 128-byte swizzle (out-of-range elements read as 0).
 bool make_tmap_rows_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows);
@@ -69,5 +80,10 @@ bool edges_tc_supported(int K, int R);
 cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, int u_only_dependency, cudaStream_t stream);
 // Warp-per-predecessor path (any K <= 256, R <= 512; fp32 or bf16 codebooks).
 cudaError_t launch_edges_warp(const EdgesArgs& a, int cb_bf16, cudaStream_t stream);
+
+// Top-K candidate extraction (1 <= K <= min(V, kTopkMaxK)).
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);
+// Reads and clears the top-K kernel's device fault word (synchronous).
+cudaError_t take_topk_faults(unsigned* flags);
 
 }  // namespace df2

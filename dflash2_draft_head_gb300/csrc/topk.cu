@@ -1,0 +1,747 @@
+// Top-K candidate extraction: for every row of draft logits, the K largest
+// entries in descending order of value (equal values by ascending index) and
+// the values themselves.
+//
+// ggml-org/llama.cpp pull request #27342, "spec : add DFlash2 support (local
+// convolution + candidate selector)", review thread on the TOP_K kernel: the
+// selector consumes the top K candidates of vocabulary-wide rows (a few 1e5
+// entries) with small K, swept there up to K = 1024.
+//
+// The work is one read of every logit, so the design keeps the per-element
+// cost at a load from shared memory and one comparison:
+//  - persistent CTAs, one per SM; rows are dealt out to clusters of cs CTAs,
+//    each CTA of a cluster taking one contiguous chunk of the row (cs = 1 when
+//    there are enough rows to fill the GPU);
+//  - one producer lane streams the chunk's 16-byte-aligned body through a ring
+//    of six 16 KB stages with cp.async.bulk (mbarrier completion); the
+//    unaligned head and tail (under 16 bytes each) are read directly;
+//  - 256 consumer threads compare each element with a threshold tau and
+//    append the survivors to a candidate buffer as 64-bit keys (order-
+//    preserving value bits, then the complemented index: a larger key is a
+//    better candidate and no two keys are equal), one shared atomic per warp;
+//  - when the buffer passes a trigger, an exact radix select (8-bit digits,
+//    most significant first) finds the K-th largest key, the buffer keeps the
+//    K best and tau becomes the K-th value.  Elements tested later have larger
+//    indices, so one equal to tau can never displace the K-th candidate: the
+//    strict test x > tau loses nothing;
+//  - at the end of a row the other CTAs of the cluster hand their K best to
+//    rank 0 through distributed shared memory (double-buffered, mbarrier
+//    hand-shake); rank 0 keeps the K best of the union, orders them by
+//    counting and writes ids and values (the values re-read from the logits).
+// NaN entries never pass a test; rows with fewer than K other entries get
+// id -1 and value NaN in the remaining slots.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "dflash2.h"
+#include "ptx.cuh"
+
+namespace df2 {
+
+// Device fault word of the top-K kernel: DF2_FLAG_TIMEOUT when a bounded wait
+// gives up, DF2_FLAG_OVERFLOW if the candidate buffer bound were ever hit.
+__device__ unsigned int g_topk_fault = 0;
+
+namespace {
+
+constexpr int kNC = 256;                   // consumer threads (8 warps)
+constexpr int kThreads = kNC + 32;         // + one producer warp
+constexpr uint32_t kSB = 16384;            // bytes per ring stage
+constexpr int kNS = 6;                     // ring stages
+constexpr int kCap = 12288;                // candidate keys a CTA holds
+constexpr int kFillTrigger = kTopkMaxK;    // fill mode: select once more than this many are held
+constexpr int kCheckElems = 8192;          // elements between checks (one bf16, two fp32 stages)
+// threshold mode re-selects, at a check, once more than K + max(K, 32) keys
+// are held, so tau follows the K-th best seen so far
+static_assert(2 * kTopkMaxK + kCheckElems <= kCap, "the elements between checks must fit");
+static_assert(kFillTrigger + 2 * kNC * 8 <= kCap, "fill-mode sub-blocks must fit");
+static_assert(8 * kTopkMaxK <= kCap, "a cluster merge must fit");
+static_assert(kNC == 256, "one histogram bin per consumer thread");
+
+constexpr uint32_t kOffBuf = kNS * kSB;
+constexpr uint32_t kOffTmp = kOffBuf + kCap * 8;
+constexpr uint32_t kOffOut = kOffTmp + kTopkMaxK * 8;
+constexpr uint32_t kOffHist = kOffOut + 2 * kTopkMaxK * 8;
+constexpr uint32_t kOffCtl = kOffHist + 256 * 4;
+constexpr uint32_t kSmem = kOffCtl + 256;
+static_assert(kSmem <= 227 * 1024, "shared memory");
+
+struct Ctl {
+    uint64_t full[kNS];    // producer -> consumers: stage landed
+    uint64_t empty[kNS];   // consumers -> producer: stage free (one arrival per warp)
+    uint64_t mfull[2];     // rank r -> rank 0: K best of a row written to out slot
+    uint64_t mempty[2];    // rank 0 -> rank r: out slot read
+    unsigned long long kmin;
+    uint32_t count;
+    uint32_t tmp_count;
+    uint32_t sel_digit, sel_above, sel_cnt;
+    uint32_t out_cnt[2];
+    uint32_t abort;
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+
+struct TopkParams {
+    const void* logits;
+    int rows, V, K, cs;
+    int32_t* ids;
+    float* vals;
+};
+
+// Order-preserving key: the value's bits mapped to an unsigned integer that
+// sorts like the value (-0 folded onto +0), then the complemented index.
+__device__ __forceinline__ uint64_t make_key(float x, uint32_t idx) {
+    uint32_t b = __float_as_uint(x);
+    if ((b << 1) == 0u) b = 0u;
+    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((uint64_t)o << 32) | (uint32_t)~idx;
+}
+
+__device__ __forceinline__ float key_value(uint64_t k) {
+    const uint32_t o = (uint32_t)(k >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+__device__ __forceinline__ uint32_t key_index(uint64_t k) { return ~(uint32_t)k; }
+
+template <bool BF16>
+__device__ __forceinline__ float load_logit(const void* p, size_t i) {
+    if constexpr (BF16)
+        return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p)[i] << 16);
+    else
+        return reinterpret_cast<const float*>(p)[i];
+}
+
+template <bool BF16>
+__device__ __forceinline__ void load_vec(uint32_t saddr, float (&x)[BF16 ? 8 : 4]) {
+    const uint4 w = lds_v4(saddr);
+    if constexpr (BF16) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(q[i] << 16);
+            x[2 * i + 1] = __uint_as_float(q[i] & 0xFFFF0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    }
+}
+
+// Appends this thread's passing elements to the candidate buffer: bit j of m
+// selects x[j], element idx0 + (j / G) * stride + j % G of the row (groups of
+// G consecutive elements, `stride` apart).  A warp scan of the per-lane counts
+// gives each lane its offset; one shared atomic per warp reserves the space.
+// Warp-collective.  Returns, on lane 0 of a warp that appended, whether the
+// buffer now holds more than `trig` keys.
+template <int E, int G = E>
+__device__ __forceinline__ bool append(uint32_t m, const float (&x)[E], uint32_t idx0,
+                                       uint32_t stride, uint64_t* buf, Ctl* c, int trig) {
+    const int lane = threadIdx.x & 31;
+    const int n = __popc(m);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t tot = (uint32_t)__shfl_sync(0xffffffffu, incl, 31);
+    if (tot == 0) return false;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&c->count, tot);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    uint32_t pos = base + (uint32_t)(incl - n);
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        if ((m >> j) & 1u) {
+            if (pos < (uint32_t)kCap)
+                buf[pos] = make_key(x[j], idx0 + (uint32_t)(j / G) * stride + (uint32_t)(j % G));
+            else
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+            ++pos;
+        }
+    }
+    return lane == 0 && base + tot > (uint32_t)trig;
+}
+
+// Exact selection of a small set (M <= 2 * kNC keys, M > K) by counting: a
+// key's rank is the number of larger keys, ranks are distinct, and the K keys
+// of rank < K land in rank order.  Same contract as select_top.
+__device__ uint64_t select_small(uint64_t* buf, int M, int K, uint64_t* tmp, Ctl* c) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int i = tid + q * kNC;
+        if (i < M) {
+            const uint64_t k = buf[i];
+            int r = 0;
+            for (int j = 0; j < M; ++j) r += buf[j] > k ? 1 : 0;
+            if (r < K) tmp[r] = k;
+        }
+    }
+    named_bar_sync(1, kNC);
+    for (int i = tid; i < K; i += kNC) buf[i] = tmp[i];
+    const uint64_t kth = tmp[K - 1];
+    if (tid == 0) c->count = (uint32_t)K;
+    named_bar_sync(1, kNC);
+    return kth;
+}
+
+// Exact selection over buf[0, M), M > K: leaves the K largest keys in
+// buf[0, K) (unordered), sets the count to K and returns the K-th largest.
+// Radix select, most significant 8-bit digit first: each pass histograms the
+// keys that share the prefix fixed so far and fixes the next digit of the
+// K-th key; a pass whose boundary bin holds exactly the keys still needed
+// ends the search (everything at or above the prefix is taken).
+__device__ uint64_t select_top(uint64_t* buf, int M, int K, uint64_t* tmp, uint32_t* hist,
+                               Ctl* c) {
+    const int tid = threadIdx.x;
+    uint64_t prefix = 0;
+    int need = K;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        const uint64_t hm = shift == 56 ? 0ull : (~0ull << (shift + 8));
+        hist[tid] = 0u;
+        if (tid == 0) {
+            c->tmp_count = 0u;
+            c->kmin = ~0ull;
+        }
+        named_bar_sync(1, kNC);
+        for (int i = tid; i < M; i += kNC) {
+            const uint64_t k = buf[i];
+            if ((k & hm) == prefix) atomicAdd(&hist[(uint32_t)(k >> shift) & 255u], 1u);
+        }
+        named_bar_sync(1, kNC);
+        if (tid < 32) {
+            // lane l scans bins 255-8l down to 248-8l; lanes run from the top bin down
+            uint32_t h[8], local = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                h[j] = hist[255 - 8 * tid - j];
+                local += h[j];
+            }
+            uint32_t incl = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const uint32_t excl = incl - local;
+            if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+                uint32_t acc = excl;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (acc + h[j] >= (uint32_t)need) {
+                        c->sel_digit = (uint32_t)(255 - 8 * tid - j);
+                        c->sel_above = acc;
+                        c->sel_cnt = h[j];
+                        break;
+                    }
+                    acc += h[j];
+                }
+            }
+        }
+        named_bar_sync(1, kNC);
+        need -= (int)c->sel_above;
+        prefix |= (uint64_t)c->sel_digit << shift;
+        if (c->sel_cnt == (uint32_t)need) break;
+    }
+    for (int i = tid; i < M; i += kNC) {
+        const uint64_t k = buf[i];
+        if (k >= prefix) {
+            const uint32_t pos = atomicAdd(&c->tmp_count, 1u);
+            if (pos < (uint32_t)K) tmp[pos] = k;
+            atomicMin(&c->kmin, (unsigned long long)k);
+        }
+    }
+    named_bar_sync(1, kNC);
+    for (int i = tid; i < K; i += kNC) buf[i] = tmp[i];
+    const uint64_t kth = c->kmin;
+    if (tid == 0) c->count = (uint32_t)K;
+    named_bar_sync(1, kNC);
+    return kth;
+}
+
+constexpr int kVPT = kSB / 16 / kNC;  // 16-byte vectors per thread per stage
+constexpr int kWPT = kVPT * 4;        // 32-bit words per thread per stage
+
+// Element e of a thread's staged words (fp32: one per word; bf16: two per
+// word, the lower half first).
+template <bool BF16>
+__device__ __forceinline__ float stage_elem(const uint32_t (&w)[kWPT], int e) {
+    if constexpr (BF16)
+        return __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+    else
+        return __uint_as_float(w[e]);
+}
+
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));  // NaN yields the other operand
+    return d;
+}
+
+// Largest non-NaN element of the staged words (NaN if all are NaN), by a
+// pairwise tree: fp32 in fp32, bf16 on packed pairs.
+template <bool BF16>
+__device__ __forceinline__ float stage_max(const uint32_t (&w)[kWPT]) {
+    if constexpr (BF16) {
+        uint32_t t[kWPT];
+#pragma unroll
+        for (int i = 0; i < kWPT; ++i) t[i] = w[i];
+#pragma unroll
+        for (int h = kWPT / 2; h >= 1; h /= 2)
+#pragma unroll
+            for (int i = 0; i < h; ++i) t[i] = max_bf16x2(t[i], t[i + h]);
+        return fmaxf(__uint_as_float(t[0] << 16), __uint_as_float(t[0] & 0xFFFF0000u));
+    } else {
+        float t[kWPT];
+#pragma unroll
+        for (int i = 0; i < kWPT; ++i) t[i] = __uint_as_float(w[i]);
+#pragma unroll
+        for (int h = kWPT / 2; h >= 1; h /= 2)
+#pragma unroll
+            for (int i = 0; i < h; ++i) t[i] = fmaxf(t[i], t[i + h]);
+        return t[0];
+    }
+}
+
+// Row index of staged element e: vector e / E of the thread's vectors (kNC
+// vectors apart), element e % E of it.
+template <int E>
+__device__ __forceinline__ uint32_t stage_index(uint32_t idx0, int e) {
+    return idx0 + (uint32_t)((e / E) * kNC * E + (e % E));
+}
+
+// Threshold-mode append, for the rare lanes with a passing element: the lane
+// reserves its own slots with one shared atomic (no warp-wide step, so it may
+// run divergently).  Returns whether the buffer then holds more than `trig`.
+template <bool BF16, int E>
+__device__ __forceinline__ bool append_sparse(float t, const uint32_t (&w)[kWPT], uint32_t idx0,
+                                              uint64_t* buf, Ctl* c, int trig) {
+    constexpr int EPT = kVPT * E;
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) m |= (stage_elem<BF16>(w, e) > t ? 1u : 0u) << e;
+    if (m == 0) return false;
+    const uint32_t n = (uint32_t)__popc(m);
+    uint32_t pos = atomicAdd(&c->count, n);
+    const bool over = pos + n > (uint32_t)trig;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        if ((m >> e) & 1u) {
+            if (pos < (uint32_t)kCap)
+                buf[pos] = make_key(stage_elem<BF16>(w, e), stage_index<E>(idx0, e));
+            else
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+            ++pos;
+        }
+    }
+    return over;
+}
+
+// Fill-mode append of every non-NaN staged element (x >= -inf), or of every
+// element above t.  Warp-collective.
+template <bool BF16, int E>
+__device__ __forceinline__ bool append_dense(float t, bool keep_all, const uint32_t (&w)[kWPT],
+                                             uint32_t idx0, uint64_t* buf, Ctl* c, int trig) {
+    constexpr int EPT = kVPT * E;
+    float x[EPT];
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        x[e] = stage_elem<BF16>(w, e);
+        m |= ((keep_all ? x[e] == x[e] : x[e] > t) ? 1u : 0u) << e;
+    }
+    return append<EPT, E>(m, x, idx0, (uint32_t)(kNC * E), buf, c, trig);
+}
+
+// The K best of buf[0, M) (M > K) into buf[0, K); returns the K-th best key.
+__device__ __forceinline__ uint64_t select_keep(uint64_t* buf, int M, int K, uint64_t* tmp,
+                                                uint32_t* hist, Ctl* c) {
+    return M <= 2 * kNC ? select_small(buf, M, K, tmp, c) : select_top(buf, M, K, tmp, hist, c);
+}
+
+// Orders buf[0, n) (n <= K, distinct keys) by counting and writes row `row`
+// of the outputs; slots n..K-1 get id -1 and value NaN.
+template <bool BF16>
+__device__ void write_row(const uint64_t* buf, int n, const TopkParams& p, int row) {
+    int32_t* ids = p.ids + (size_t)row * p.K;
+    float* vals = p.vals + (size_t)row * p.K;
+    for (int i = threadIdx.x; i < p.K; i += kNC) {
+        int slot = i;
+        int32_t id = -1;
+        float v = __uint_as_float(0x7FC00000u);
+        if (i < n) {
+            const uint64_t k = buf[i];
+            int r = 0;
+            for (int j = 0; j < n; ++j) r += buf[j] > k ? 1 : 0;
+            slot = r;
+            id = (int32_t)key_index(k);
+            v = key_value(k);  // exact, except that the key folded -0 onto +0
+            if ((uint32_t)id >= (uint32_t)p.V) {  // not reachable with distinct keys
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+                id = -1;
+                v = __uint_as_float(0x7FC00000u);
+            } else if (v == 0.f) {
+                v = load_logit<BF16>(p.logits, (size_t)row * p.V + (uint32_t)id);
+            }
+        }
+        ids[slot] = id;
+        vals[slot] = v;
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
+    constexpr int E = BF16 ? 8 : 4;  // elements per 16-byte vector
+    constexpr int VPT = kVPT;
+    constexpr int EPT = VPT * E;     // elements a thread holds per stage
+    constexpr uint32_t kNaNWord = BF16 ? 0x7FC07FC0u : 0x7FC00000u;
+    constexpr uint32_t esz = BF16 ? 2u : 4u;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* buf = reinterpret_cast<uint64_t*>(smem + kOffBuf);
+    uint64_t* tmp = reinterpret_cast<uint64_t*>(smem + kOffTmp);
+    uint64_t* outk = reinterpret_cast<uint64_t*>(smem + kOffOut);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+    Ctl* c = reinterpret_cast<Ctl*>(smem + kOffCtl);
+    const uint32_t full0 = smem_u32(&c->full[0]);
+    const uint32_t empty0 = smem_u32(&c->empty[0]);
+    volatile uint32_t* abort_flag = &c->abort;
+    const int tid = threadIdx.x;
+    const int cs = p.cs;
+    const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
+    const int cid = (int)blockIdx.x / cs;
+    const int ncl = (int)gridDim.x / cs;
+
+    if (tid == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kNC / 32);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&c->mfull[i]), cs > 1 ? (uint32_t)(cs - 1) : 1u);
+            mbar_init(smem_u32(&c->mempty[i]), 1);
+        }
+        c->abort = 0;
+        fence_mbar_init();
+    }
+    if (cs > 1)
+        cluster_sync();
+    else
+        __syncthreads();
+
+    // this CTA's chunk [e0, e1) of every row (64-element granules)
+    const int L = (((p.V + cs - 1) / cs) + 63) & ~63;
+    const int e0 = min(p.V, (int)rank * L);
+    const int e1 = min(p.V, e0 + L);
+    const uintptr_t lbase = reinterpret_cast<uintptr_t>(p.logits);
+
+    if (tid >= kNC) {
+        // ---------------- producer (one lane)
+        if (tid == kNC) {
+            int it = 0;
+            for (int row = cid; row < p.rows && !*abort_flag; row += ncl) {
+                const uintptr_t a0 = lbase + ((size_t)row * p.V + e0) * esz;
+                const uintptr_t a1 = lbase + ((size_t)row * p.V + e1) * esz;
+                const uintptr_t b0 = (a0 + 15) & ~(uintptr_t)15, b1 = a1 & ~(uintptr_t)15;
+                for (uintptr_t off = b0; off < b1; off += kSB, ++it) {
+                    const int st = it % kNS;
+                    const uint32_t ph = (uint32_t)(it / kNS) & 1u;
+                    if (*abort_flag) break;
+                    if (!mbar_wait_bounded(empty0 + 8 * st, ph ^ 1u, kWaitNs)) {
+                        *abort_flag = 1;
+                        atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_TIMEOUT);
+                        break;
+                    }
+                    const uint32_t bytes = (uint32_t)min((uintptr_t)kSB, b1 - off);
+                    mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+                    bulk_g2s(s0 + (uint32_t)st * kSB, reinterpret_cast<const void*>(off), bytes,
+                             full0 + 8 * st);
+                }
+            }
+        }
+        __syncwarp();
+        if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read it
+        return;
+    }
+
+    // ---------------- consumers
+    const int steady_trig = p.K + max(p.K, 32);
+    int it = 0, rit = 0;
+    for (int row = cid; row < p.rows; row += ncl, ++rit) {
+        const size_t rowoff = (size_t)row * p.V;
+        const uintptr_t a0 = lbase + (rowoff + e0) * esz;
+        const uintptr_t a1 = lbase + (rowoff + e1) * esz;
+        const uintptr_t b0 = (a0 + 15) & ~(uintptr_t)15, b1 = a1 & ~(uintptr_t)15;
+        const bool body = b0 < b1;
+        const int head = body ? (int)((b0 - a0) / esz) : e1 - e0;
+        const int tail = body ? (int)((a1 - b1) / esz) : 0;
+        // the unaligned head and tail elements (under 16 bytes each, so one per
+        // thread) are loaded now and tested in index order: head first, tail last
+        float hx[1] = {0.f}, tx[1] = {0.f};
+        if (tid < head) hx[0] = load_logit<BF16>(p.logits, rowoff + e0 + tid);
+        if (tid < tail) tx[0] = load_logit<BF16>(p.logits, rowoff + (e1 - tail) + tid);
+        named_bar_sync(1, kNC);  // the previous row's readers of buf and count are done
+        if (tid == 0) c->count = 0u;
+        named_bar_sync(1, kNC);
+        // Modes: fill (tau = -inf: every non-NaN element is kept) until a
+        // selection; then threshold (x > tau).  tau is either just below a lower
+        // bound of the K-th best value (x > tau keeps every x >= the bound) or,
+        // after an exact selection, the K-th best value itself.
+        float tau = -INFINITY;
+        bool fill = true, seeded = false, over = false;
+        int ks = 0;  // stages of this row so far
+        over |= append<1>(tid < head && hx[0] == hx[0] ? 1u : 0u, hx, (uint32_t)(e0 + tid), 0u,
+                          buf, c, kFillTrigger);
+
+        for (uintptr_t off = b0; off < b1; off += kSB, ++it) {
+            const int st = it % kNS;
+            const uint32_t ph = (uint32_t)(it / kNS) & 1u;
+            if (!*abort_flag && !mbar_wait_bounded(full0 + 8 * st, ph, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_TIMEOUT);
+            }
+            const uint32_t nvec = (uint32_t)min((uintptr_t)kSB, b1 - off) / 16u;
+            const uint32_t ebase = (uint32_t)e0 + (uint32_t)((off - a0) / esz);
+            const uint32_t sb = s0 + (uint32_t)st * kSB;
+            // the whole stage at once: thread t holds vectors t, t+256, t+512, t+768
+            uint32_t w[kWPT];
+#pragma unroll
+            for (int q = 0; q < VPT; ++q) {
+                const uint32_t v = (uint32_t)(q * kNC + tid);
+                uint4 u = make_uint4(kNaNWord, kNaNWord, kNaNWord, kNaNWord);  // NaN passes no test
+                if (v < nvec) u = lds_v4(sb + v * 16u);
+                w[4 * q] = u.x;
+                w[4 * q + 1] = u.y;
+                w[4 * q + 2] = u.z;
+                w[4 * q + 3] = u.w;
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(empty0 + 8 * st);  // the stage is in registers
+            const uint32_t idx0 = ebase + (uint32_t)tid * (uint32_t)E;
+            const float mx = stage_max<BF16>(w);
+            if (!fill) {
+                if (mx > tau) over |= append_sparse<BF16, E>(tau, w, idx0, buf, c, steady_trig);
+            } else if (!seeded && p.K <= kNC && nvec == (uint32_t)(VPT * kNC)) {
+                // First full stage: the K-th largest of the per-thread maxima (and
+                // the head) is at most the K-th largest element seen, since those
+                // K maxima are distinct elements.  Rebuild the buffer from
+                // everything at or above that bound.
+                seeded = true;
+                int me = -1;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e)
+                    if (me < 0 && stage_elem<BF16>(w, e) == mx) me = e;  // mx is NaN: none
+                const float mxa[1] = {mx};
+                append<1>(me >= 0 ? 1u : 0u, mxa, stage_index<E>(idx0, max(me, 0)), 0u, buf, c,
+                          kCap);
+                named_bar_sync(1, kNC);
+                const int M = min((int)c->count, kCap);
+                float bound = -INFINITY;
+                if (M > p.K) bound = key_value(select_keep(buf, M, p.K, tmp, hist, c));
+                named_bar_sync(1, kNC);  // count read (and the selection done) everywhere
+                if (tid == 0) c->count = 0u;
+                named_bar_sync(1, kNC);
+                // -inf has no float below it: stay in fill mode then
+                const bool use = bound != -INFINITY;
+                const float tb = use ? nextafterf(bound, -INFINITY) : -INFINITY;
+                over = append<1>(tid < head && (use ? hx[0] > tb : hx[0] == hx[0]) ? 1u : 0u, hx,
+                                 (uint32_t)(e0 + tid), 0u, buf, c, kFillTrigger);
+                over |= append_dense<BF16, E>(tb, !use, w, idx0, buf, c,
+                                              use ? steady_trig : kFillTrigger);
+                if (use) {
+                    fill = false;
+                    tau = tb;
+                }
+            } else {
+                over |= append_dense<BF16, E>(-INFINITY, true, w, idx0, buf, c, kFillTrigger);
+            }
+            // Check at most every kCheckElems elements (fp32: every other stage).
+            // Elements after a check have larger indices than every key held, so
+            // after an exact selection x > tau loses nothing.
+            ++ks;
+            if ((BF16 || (ks & 1) == 0) && bar_red_or(1, kNC, over)) {
+                tau = key_value(select_keep(buf, min((int)c->count, kCap), p.K, tmp, hist, c));
+                fill = false;
+                over = false;
+            }
+        }
+
+        if (tail > 0) {
+            const uint32_t m = tid < tail && (fill ? tx[0] == tx[0] : tx[0] > tau) ? 1u : 0u;
+            append<1>(m, tx, (uint32_t)(e1 - tail + tid), 0u, buf, c, kCap);
+        }
+        named_bar_sync(1, kNC);
+        int n = min((int)c->count, kCap);
+        if (n > p.K) {
+            select_keep(buf, n, p.K, tmp, hist, c);
+            n = p.K;
+        }
+
+        if (cs == 1) {
+            write_row<BF16>(buf, n, p, row);
+            continue;
+        }
+        const int slot = rit & 1;
+        const uint32_t par = (uint32_t)(rit >> 1) & 1u;
+        if (rank != 0) {
+            if (!*abort_flag &&
+                !mbar_wait_cluster_bounded(smem_u32(&c->mempty[slot]), par ^ 1u, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_TIMEOUT);
+            }
+            uint64_t* o = outk + (size_t)slot * kTopkMaxK;
+            for (int i = tid; i < n; i += kNC) o[i] = buf[i];
+            if (tid == 0) c->out_cnt[slot] = (uint32_t)n;
+            named_bar_sync(1, kNC);
+            if (tid == 0) {
+                fence_acq_rel_cluster();
+                mbar_arrive_remote(map_cluster(smem_u32(&c->mfull[slot]), 0));
+            }
+        } else {
+            if (!*abort_flag &&
+                !mbar_wait_cluster_bounded(smem_u32(&c->mfull[slot]), par, kWaitNs)) {
+                *abort_flag = 1;
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_TIMEOUT);
+            }
+            int M = n;
+            for (int r = 1; r < cs; ++r) {
+                const int cnt = (int)min(
+                    ld_cluster_u32(map_cluster(smem_u32(&c->out_cnt[slot]), (uint32_t)r)),
+                    (uint32_t)p.K);
+                const uint32_t src =
+                    map_cluster(smem_u32(outk + (size_t)slot * kTopkMaxK), (uint32_t)r);
+                for (int i = tid; i < cnt; i += kNC) buf[M + i] = ld_cluster_u64(src + 8u * i);
+                M += cnt;
+            }
+            named_bar_sync(1, kNC);
+            if (tid == 0) {
+                fence_acq_rel_cluster();
+                for (int r = 1; r < cs; ++r)
+                    mbar_arrive_remote(map_cluster(smem_u32(&c->mempty[slot]), (uint32_t)r));
+            }
+            if (M > p.K) {
+                select_keep(buf, M, p.K, tmp, hist, c);
+                M = p.K;
+            }
+            write_row<BF16>(buf, M, p, row);
+        }
+    }
+    // On an abandoned pipeline, give copies still in flight a bounded time to
+    // land before the CTA's shared memory is released.
+    if (tid == 0 && *abort_flag) {
+        for (int i = 0; i < kNS; ++i) mbar_wait_bounded(full0 + 8 * i, 0, kWaitNs / 4);
+    }
+    if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read it
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    int max_clusters[2][4] = {};  // [bf16][log2 cs]: clusters resident at once
+};
+
+std::mutex g_mu;
+DeviceInfo g_info[64];
+
+template <bool BF16>
+cudaError_t query_device(DeviceInfo& d) {
+    auto kern = topk_kernel<BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmem);
+    if (e != cudaSuccess) return e;
+    for (int l = 0; l < 4; ++l) {
+        const int cs = 1 << l;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(cs, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        d.max_clusters[BF16 ? 1 : 0][l] = n;
+    }
+    return cudaSuccess;
+}
+
+template <bool BF16>
+cudaError_t launch_t(const TopkLaunch& a, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int maxc[4];
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DeviceInfo& d = g_info[dev];
+        if (!d.ready) {
+            e = query_device<false>(d);
+            if (e == cudaSuccess) e = query_device<true>(d);
+            if (e != cudaSuccess) return e;
+            d.ready = true;
+        }
+        for (int l = 0; l < 4; ++l) maxc[l] = d.max_clusters[BF16 ? 1 : 0][l];
+    }
+    // cluster size: the fewest waves of the longest per-CTA chunk, plus a fixed
+    // per-row cost (selection, merge) worth about 8192 elements
+    int best_l = -1;
+    long long best_cost = 0;
+    for (int l = 0; l < 4; ++l) {
+        if (maxc[l] <= 0) continue;
+        const int cs = 1 << l;
+        const long long waves = (a.rows + maxc[l] - 1) / maxc[l];
+        const long long cost = waves * ((a.V + cs - 1) / cs + 8192LL);
+        if (best_l < 0 || cost < best_cost) {
+            best_l = l;
+            best_cost = cost;
+        }
+    }
+    if (best_l < 0) return cudaErrorInvalidConfiguration;
+    const int cs = 1 << best_l;
+    const int nclusters = a.rows < maxc[best_l] ? a.rows : maxc[best_l];
+    TopkParams p{a.logits, a.rows, a.V, a.K, cs, a.ids, a.vals};
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(nclusters * cs), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, topk_kernel<BF16>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
+    return a.bf16 ? launch_t<true>(a, stream) : launch_t<false>(a, stream);
+}
+
+cudaError_t take_topk_faults(unsigned* flags) {
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_topk_fault, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_topk_fault, &zero, sizeof(zero));
+    *flags = v;
+    return e;
+}
+
+}  // namespace df2

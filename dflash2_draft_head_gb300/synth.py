@@ -7,7 +7,8 @@ fed from it, so they read identical values.
 Distributions (normal laws written N(mean, variance)):
   x, hist, h ~ N(0, 1); base ~ N(0, 1/T); delta ~ N(0, 0.1/T);
   W ~ N(0, 1/d); A, B ~ N(0, 1/sqrt(R)); unary ~ N(0, 1);
-  cand_ids: K distinct ids per position, uniform over [0, V).
+  cand_ids: K distinct ids per position, uniform over [0, V);
+  draft logits ~ N(0, 4), one generator per row.
 bf16 workloads draw fp32 and round once to bf16 (round-to-nearest-even); the
 returned fp32 arrays hold those exact bf16 values.
 
@@ -24,7 +25,8 @@ import torch
 CHUNK = 4096
 
 _TAG = {"x": 1, "hist": 2, "base": 3, "delta": 4, "h": 5, "W": 6, "A": 7, "B": 8,
-        "unary": 9, "cand": 10, "cand_fix": 11}
+        "unary": 9, "cand": 10, "cand_fix": 11,
+        "logits": 12}
 
 
 def _gen(seed: int, *key: int) -> torch.Generator:
@@ -144,3 +146,13 @@ def selector_inputs(w) -> dict:
     cand = torch.stack([cand_rows(sd, s, 0, w.n_sel, w.K, w.V, w.n_sel) for s in range(w.S_sel)], 0)
     unary = normal_tensor(sd, "unary", w.S_sel, w.n_sel, (w.K,), 1.0, "f32")
     return {"h": h, "cand_ids": cand, "unary": unary}
+
+
+def logits_rows(seed: int, lo: int, hi: int, V: int, dtype: str, std: float = 2.0) -> torch.Tensor:
+    """Rows [lo, hi) of a [rows, V] draft-logit matrix; row r comes from its own
+    generator, so any row can be regenerated alone."""
+    out = torch.empty((max(hi - lo, 0), V), dtype=torch.float32)
+    for r in range(lo, hi):
+        g = _gen(seed, _TAG["logits"], r, 0)
+        out[r - lo] = torch.randn((V,), generator=g, dtype=torch.float32) * std
+    return to_storage(out, dtype)

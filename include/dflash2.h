@@ -51,6 +51,8 @@ typedef enum { DF2_F32 = 0, DF2_BF16 = 1 } df2_dtype;
 /* Bits a kernel ORs into a caller-provided device err_flag (int32). */
 #define DF2_FLAG_BAD_ID 1    /* a candidate id outside [0, V): it was clamped for the load */
 #define DF2_FLAG_TIMEOUT 2   /* a bounded on-chip wait gave up; outputs of that tile are undefined */
+#define DF2_FLAG_OVERFLOW 4  /* an internal buffer bound was reached (not expected for any input);
+                                that call's outputs are undefined */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int dflash2_version(void);
@@ -197,9 +199,32 @@ int dflash2_project_noalloc(const void* h, const void* W, float* u, int P, int d
                             int in_dtype, void* stream);
 
 /*
+ * Top-K candidate extraction, the step that makes the selector's cand_ids and
+ * unary from the draft's logits (ggml-org/llama.cpp pull request #27342, "spec
+ * : add DFlash2 support (local convolution + candidate selector)", review
+ * thread on the TOP_K kernel: the selector works on the top K candidates of
+ * vocabulary-wide rows, with K small).
+ *   logits   [rows,V] in `in_dtype` (DF2_F32 or DF2_BF16)
+ *   cand_ids [rows,K] int32 out: the indices of the K largest entries of each
+ *            row in descending order of value, equal values in ascending
+ *            order of index (-0 and +0 are equal)
+ *   values   [rows,K] fp32 out: logits[row, cand_ids[row,k]], exactly
+ * A NaN entry is never selected; when a row holds fewer than K entries that
+ * are not NaN, its remaining slots get id -1 and value NaN.  All three
+ * buffers are caller-owned device memory; nothing is allocated.
+ * INVALID_ARG: rows or V <= 0; K < 1 or K > V; NULL pointer; misalignment;
+ * an output overlapping the logits or the other output.
+ * UNSUPPORTED: K > 1024.
+ */
+int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32_t* cand_ids,
+                 float* values, void* stream);
+
+/*
  * Reads and clears the library's device-side fault word for the current
- * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_project gave
- * up).  Synchronises the current device.  Returns DF2_OK or DF2_ERR_CUDA.
+ * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_dynconv,
+ * dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from
+ * dflash2_topk).  Synchronises the current device.  Returns DF2_OK or
+ * DF2_ERR_CUDA.
  */
 int dflash2_take_device_faults(int32_t* flags_out);
 

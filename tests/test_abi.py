@@ -139,3 +139,21 @@ def test_project_ws_validation(L):
     assert f(*args, P[0], need, None) == 1                    # overlaps h
     assert b"workspace" in L.dflash2_last_error()
     assert f(P[0], P[1], P[2], 4096, 5120, 12, 1, P[3], need, None) == 2  # R % 8
+
+
+def _topk(L, lg=P[0], rows=4, V=100, K=8, dt=0, ids=P[1], vals=P[2]):
+    return L.dflash2_topk(lg, rows, V, K, dt, ids, vals, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lg=NULL), 1), (dict(ids=NULL), 1), (dict(vals=NULL), 1),
+    (dict(rows=0), 1), (dict(V=0), 1), (dict(K=0), 1), (dict(K=101), 1), (dict(dt=2), 1),
+    (dict(lg=ctypes.c_void_p(0x10000004)), 1), (dict(vals=ctypes.c_void_p(0x30000008)), 1),
+    (dict(ids=P[0]), 1),                        # cand_ids aliases the logits
+    (dict(vals=P[1]), 1),                       # the two outputs alias
+    (dict(V=5000, K=1025), 2),
+])
+def test_topk_validation(L, kw, code):
+    assert _topk(L, **kw) == code
+    assert b"topk" in L.dflash2_last_error() or b"aligned" in L.dflash2_last_error() or \
+        b"overlaps" in L.dflash2_last_error()
