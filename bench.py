@@ -495,6 +495,23 @@ def main():
         t_proj, t_edge = _timed_graph(K_iso, stream, flush, iso_calls, record_ext, L)
     else:
         t_proj, t_edge = _timed_eager(K_iso, stream, flush, iso_calls, L)
+    # top-K candidate extraction, the step before the selector, on the draft
+    # logits of the same positions: [P, V] fp32 rows (the review thread's
+    # top-k microbenchmark runs fp32 rows); also an isolated loop
+    logits = synth.logits_rows(w.seed, 0, P, w.V, "f32").to(dev)
+    tk_ids = torch.empty((P, w.K), dtype=torch.int32, device=dev)
+    tk_vals = torch.empty((P, w.K), dtype=torch.float32, device=dev)
+    topk_args = (ptr(logits), P, w.V, w.K, 0, ptr(tk_ids), ptr(tk_vals), sp)
+    f_topk = L.dflash2_topk
+    _call(f_topk, topk_args, L)  # first call per device queries occupancy (not capturable)
+    barrier()
+    if record_ext is not None:
+        t_topk = _timed_graph(K_iso, stream, flush, [(f_topk, topk_args)], record_ext, L)[0]
+    else:
+        t_topk = _timed_eager(K_iso, stream, flush, [(f_topk, topk_args)], L)[0]
+    topk_b = P * w.V * 4 + P * w.K * 8
+    topk_us = 1000.0 * statistics.mean(t_topk)
+    del logits
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -539,6 +556,10 @@ def main():
                                                "dynconv.cu"), "rb").read()).hexdigest()
     tr = TRAFFIC.get((w.name, "dynconv"))
     traffic = tr["bytes"] if tr and tr["sha"] == src_sha else None
+    tk_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
+                                              "topk.cu"), "rb").read()).hexdigest()
+    tr = TRAFFIC.get((w.name, "topk"))
+    topk_traffic = tr["bytes"] if tr and tr["sha"] == tk_sha else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -557,6 +578,9 @@ def main():
             "edges": {"bound": "hbm", "achieved": edge_b / edge_us / 1e3, "peak": hbm,
                       "unit": "GB/s", "frac": edge_b / edge_us / 1e3 / hbm,
                       "timing": "isolated loop"},
+            "topk": {"bound": "hbm", "achieved": topk_b / topk_us / 1e3, "peak": hbm,
+                     "unit": "GB/s", "frac": topk_b / topk_us / 1e3 / hbm,
+                     "traffic": topk_traffic, "timing": "isolated loop"},
         },
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
@@ -573,6 +597,10 @@ def main():
             "edges": {"isolated": True, "steps": K_iso, "us": edge_us, "bytes": edge_b,
                       "GB/s": edge_b / edge_us / 1e3,
                       "frac_hbm": edge_b / edge_us / 1e3 / hbm},
+            "topk": {"isolated": True, "steps": K_iso, "us": topk_us, "bytes": topk_b,
+                     "rows": P, "V": w.V, "K": w.K, "logits": "f32",
+                     "GB/s": topk_b / topk_us / 1e3, "frac_hbm": topk_b / topk_us / 1e3 / hbm,
+                     "note": "not part of the timed step; candidate extraction before it"},
         },
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2},

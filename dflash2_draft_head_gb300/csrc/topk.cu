@@ -172,7 +172,7 @@ __device__ __forceinline__ bool append(uint32_t m, const float (&x)[E], uint32_t
 // Exact selection of a small set (M <= 2 * kNC keys, M > K) by counting: a
 // key's rank is the number of larger keys, ranks are distinct, and the K keys
 // of rank < K land in rank order.  Same contract as select_top.
-__device__ uint64_t select_small(uint64_t* buf, int M, int K, uint64_t* tmp, Ctl* c) {
+__device__ uint64_t select_small(uint64_t* buf, int M, int K, uint64_t* tmp, uint32_t* count) {
     const int tid = threadIdx.x;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -187,7 +187,7 @@ __device__ uint64_t select_small(uint64_t* buf, int M, int K, uint64_t* tmp, Ctl
     named_bar_sync(1, kNC);
     for (int i = tid; i < K; i += kNC) buf[i] = tmp[i];
     const uint64_t kth = tmp[K - 1];
-    if (tid == 0) c->count = (uint32_t)K;
+    if (tid == 0) *count = (uint32_t)K;
     named_bar_sync(1, kNC);
     return kth;
 }
@@ -363,7 +363,8 @@ __device__ __forceinline__ bool append_dense(float t, bool keep_all, const uint3
 // The K best of buf[0, M) (M > K) into buf[0, K); returns the K-th best key.
 __device__ __forceinline__ uint64_t select_keep(uint64_t* buf, int M, int K, uint64_t* tmp,
                                                 uint32_t* hist, Ctl* c) {
-    return M <= 2 * kNC ? select_small(buf, M, K, tmp, c) : select_top(buf, M, K, tmp, hist, c);
+    return M <= 2 * kNC ? select_small(buf, M, K, tmp, &c->count)
+                        : select_top(buf, M, K, tmp, hist, c);
 }
 
 // Orders buf[0, n) (n <= K, distinct keys) by counting and writes row `row`
@@ -641,26 +642,718 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     if (cs > 1) cluster_sync();  // no CTA leaves while a peer may still read it
 }
 
+
+// ================================================================ K <= 256
+//
+// For small K the filtering warps never wait for one another.  Eight filter
+// warps stream the stages and push the elements that beat the published
+// threshold key into their own single-producer queue; a selector warp drains
+// the queues into an exact sorted top-K list and raises the threshold key
+// (atomic max) as the list improves.  The threshold is a full key (value,
+// then index), so the test "key > threshold" is exact in any processing
+// order: the threshold is the K-th best key of a subset of the row, so every
+// element of the row's top K has a larger key.  Filter warps run at most one
+// row ahead of the selector.
+
+constexpr int kAsyncMaxK = 256;
+constexpr int kNF = 8;                       // filter warps
+constexpr int kAThreads = (kNF + 2) * 32;    // + selector warp + producer warp
+constexpr int kQW = 1024;                    // queue slots per filter warp (power of two)
+static_assert(kNF * 32 == kNC, "the filter warps are the kNC threads of the seeding step");
+static_assert(32 * 8 * kVPT <= kQW, "one stage's pushes must fit a queue");
+
+constexpr uint32_t kAQueue = kNS * kSB;
+constexpr uint32_t kASeed = kAQueue + kNF * kQW * 8;
+constexpr uint32_t kASeedTmp = kASeed + 2 * kNC * 8;
+constexpr uint32_t kAList = kASeedTmp + kAsyncMaxK * 8;
+constexpr uint32_t kABatch = kAList + 2 * kAsyncMaxK * 8;
+constexpr uint32_t kAOut = kABatch + 32 * 8;
+constexpr uint32_t kAMerge = kAOut + 2 * kAsyncMaxK * 8;
+constexpr uint32_t kACtl = kAMerge + 8 * kAsyncMaxK * 8;
+constexpr uint32_t kASmem = kACtl + 512;
+static_assert(kASmem <= 227 * 1024, "shared memory");
+
+struct ACtl {
+    uint64_t full[kNS];
+    uint64_t empty[kNS];
+    uint64_t mfull[2];
+    uint64_t mempty[2];
+    unsigned long long tau[2];  // published threshold key, by row parity (0: none yet)
+    uint32_t qhead[kNF];        // keys pushed by each filter warp (running count)
+    uint32_t qtail[kNF];        // keys the selector has taken from each queue
+    uint32_t rowend[kNF][2];    // qhead at the end of a row, by row parity
+    uint32_t rowtag[kNF][2];    // (row iteration + 1) that rowend belongs to
+    uint32_t sel_done;          // rows the selector has finished
+    uint32_t seed_count;
+    uint32_t out_cnt[2];
+    uint32_t abort;
+};
+static_assert(sizeof(ACtl) <= 512, "control block");
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// Marks the pipeline abandoned (a bounded wait gave up).
+__device__ __forceinline__ void set_abort(volatile uint32_t* abort_flag) {
+    *abort_flag = 1;
+    atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_TIMEOUT);
+}
+
+// Bounded wait until *p >= v (a running counter written with release).
+__device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t v,
+                                             volatile uint32_t* abort_flag) {
+    if (*abort_flag || (int32_t)(ld_acquire_u32(p) - v) >= 0) return;
+    const uint64_t t0 = global_ns();
+    while ((int32_t)(ld_acquire_u32(p) - v) < 0) {
+        if (*abort_flag) return;
+        if (global_ns() - t0 > kWaitNs) {
+            set_abort(abort_flag);
+            return;
+        }
+        __nanosleep(64);
+    }
+}
+
+// Element e of thread t's staged vectors, read back from the stage at sb.
+template <bool BF16>
+__device__ __forceinline__ float stage_elem_smem(uint32_t sb, int t, int e) {
+    constexpr int E = BF16 ? 8 : 4;
+    const uint32_t a = sb + (uint32_t)((e / E) * kNC + t) * 16u + (uint32_t)(e % E) * (BF16 ? 2u : 4u);
+    if constexpr (BF16) {
+        uint16_t h;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+        return __uint_as_float((uint32_t)h << 16);
+    } else {
+        float f;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f) : "r"(a));
+        return f;
+    }
+}
+
+// Pushes this lane's marked staged elements (bit e of m: element e, re-read
+// from the stage at sb) into the warp's queue.  Warp-collective.
+template <bool BF16, int E>
+__device__ __forceinline__ void push_keys(uint32_t m, uint32_t sb, uint32_t idx0, uint64_t* q,
+                                          uint32_t& qh, ACtl* c, int fw,
+                                          volatile uint32_t* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const int n = __popc(m);
+    int incl;
+    uint32_t tot;
+    if (!__any_sync(0xffffffffu, n > 1)) {  // at most one key per lane: offsets from a ballot
+        const uint32_t b = __ballot_sync(0xffffffffu, n != 0);
+        incl = __popc(b & ((2u << lane) - 1u));
+        tot = (uint32_t)__popc(b);
+    } else {
+        incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        tot = (uint32_t)__shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (tot == 0) return;
+    if (lane == 0) wait_counter(&c->qtail[fw], qh + tot - kQW, abort_flag);  // room for tot keys
+    __syncwarp();
+    uint32_t pos = qh + (uint32_t)(incl - n);
+    for (uint32_t mm = m; mm; mm &= mm - 1u) {
+        const int e = __ffs(mm) - 1;
+        q[(pos++) & (kQW - 1)] =
+            make_key(stage_elem_smem<BF16>(sb, (int)threadIdx.x, e), stage_index<E>(idx0, e));
+    }
+    __syncwarp();
+    qh += tot;
+    if (lane == 0) st_release_u32(&c->qhead[fw], qh);
+}
+
+// Single-value variant of push_keys (head and tail elements).
+__device__ __forceinline__ void push_one(bool pass, float x, uint32_t idx, uint64_t* q,
+                                         uint32_t& qh, ACtl* c, int fw,
+                                         volatile uint32_t* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t b = __ballot_sync(0xffffffffu, pass);
+    const uint32_t tot = (uint32_t)__popc(b);
+    if (tot == 0) return;
+    if (lane == 0) wait_counter(&c->qtail[fw], qh + tot - kQW, abort_flag);
+    __syncwarp();
+    if (pass) q[(qh + (uint32_t)__popc(b & ((1u << lane) - 1u))) & (kQW - 1)] = make_key(x, idx);
+    __syncwarp();
+    qh += tot;
+    if (lane == 0) st_release_u32(&c->qhead[fw], qh);
+}
+
+// Inserts key k into the descending list L[0, s) (capacity K), keeping the
+// best K.  Precondition: s < K or k > L[K-1].  Selector warp.
+__device__ __forceinline__ void list_insert(uint64_t* L, int& s, int K, uint64_t k) {
+    const int lane = threadIdx.x & 31;
+    int p = 0;
+    for (int b = 0; b < s; b += 32) {
+        const int i = b + lane;
+        p += __popc(__ballot_sync(0xffffffffu, i < s && L[i] > k));
+    }
+    const int last = min(s, K - 1);  // L[p, last) moves one place down
+    uint64_t v[kAsyncMaxK / 32];
+#pragma unroll
+    for (int t = 0; t < kAsyncMaxK / 32; ++t) {
+        const int i = p + lane + 32 * t;
+        if (i < last) v[t] = L[i];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < kAsyncMaxK / 32; ++t) {
+        const int i = p + lane + 32 * t;
+        if (i < last) L[i + 1] = v[t];
+    }
+    if (lane == 0) L[p] = k;
+    __syncwarp();
+    s = min(s + 1, K);
+}
+
+// Number of keys greater than k in the descending list l[0, n).
+__device__ __forceinline__ int count_greater(const uint64_t* l, int n, uint64_t k) {
+    int lo = 0, hi = n;  // answer in [lo, hi]
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (l[mid] > k)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Merges up to 32 new keys (one per lane, 0 = none; every real key beats the
+// list's K-th when the list is full) into the descending list L[0, s), writing
+// the best K of the union to Ln (descending).  The batch is sorted across the
+// lanes with a bitonic network, then every key goes to its rank in the union:
+// its own position plus the keys above it in the other sorted sequence.
+__device__ __forceinline__ void list_merge(const uint64_t* L, uint64_t* Ln, int& s, int K,
+                                           uint64_t k, uint64_t* Bs) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, k, j);
+            const bool desc = (lane & size) == 0;
+            const bool lower = (lane & j) == 0;
+            k = (lower == desc) ? (k > o ? k : o) : (k < o ? k : o);
+        }
+    }
+    const int nb = __popc(__ballot_sync(0xffffffffu, k != 0ull));  // real keys come first
+    Bs[lane] = k;
+    __syncwarp();
+    if (lane < nb) {
+        const int r = lane + count_greater(L, s, k);
+        if (r < K) Ln[r] = k;
+    }
+    for (int i = lane; i < s; i += 32) {
+        const uint64_t v = L[i];
+        const int r = i + count_greater(Bs, nb, v);
+        if (r < K) Ln[r] = v;
+    }
+    __syncwarp();
+    s = min(s + nb, K);
+}
+
+// Writes one output row from the sorted list (selector warp).
+template <bool BF16>
+__device__ void write_sorted(const uint64_t* L, int n, const TopkParams& p, int row) {
+    int32_t* ids = p.ids + (size_t)row * p.K;
+    float* vals = p.vals + (size_t)row * p.K;
+    for (int i = threadIdx.x & 31; i < p.K; i += 32) {
+        int32_t id = -1;
+        float v = __uint_as_float(0x7FC00000u);
+        if (i < n) {
+            id = (int32_t)key_index(L[i]);
+            v = key_value(L[i]);
+            if ((uint32_t)id >= (uint32_t)p.V) {  // not reachable with distinct keys
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+                id = -1;
+                v = __uint_as_float(0x7FC00000u);
+            } else if (v == 0.f) {  // the key folded -0 onto +0
+                v = load_logit<BF16>(p.logits, (size_t)row * p.V + (uint32_t)id);
+            }
+        }
+        ids[i] = id;
+        vals[i] = v;
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) {
+    constexpr int E = BF16 ? 8 : 4;
+    constexpr int VPT = kVPT;
+    constexpr int EPT = VPT * E;
+    constexpr uint32_t esz = BF16 ? 2u : 4u;
+    constexpr uint32_t kNaNWord = BF16 ? 0x7FC07FC0u : 0x7FC00000u;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t s0 = smem_u32(smem);
+    uint64_t* queues = reinterpret_cast<uint64_t*>(smem + kAQueue);
+    uint64_t* seedbuf = reinterpret_cast<uint64_t*>(smem + kASeed);
+    uint64_t* seedtmp = reinterpret_cast<uint64_t*>(smem + kASeedTmp);
+    uint64_t* Lbuf = reinterpret_cast<uint64_t*>(smem + kAList);  // two lists of kAsyncMaxK
+    uint64_t* Bs = reinterpret_cast<uint64_t*>(smem + kABatch);
+    uint64_t* outk = reinterpret_cast<uint64_t*>(smem + kAOut);
+    uint64_t* merge = reinterpret_cast<uint64_t*>(smem + kAMerge);
+    ACtl* c = reinterpret_cast<ACtl*>(smem + kACtl);
+    const uint32_t full0 = smem_u32(&c->full[0]);
+    const uint32_t empty0 = smem_u32(&c->empty[0]);
+    volatile uint32_t* abort_flag = &c->abort;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int cs = p.cs;
+    const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
+    const int cid = (int)blockIdx.x / cs;
+    const int ncl = (int)gridDim.x / cs;
+
+    if (tid == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kNF);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&c->mfull[i]), cs > 1 ? (uint32_t)(cs - 1) : 1u);
+            mbar_init(smem_u32(&c->mempty[i]), 1);
+            c->tau[i] = 0ull;
+        }
+        for (int w = 0; w < kNF; ++w) {
+            c->qhead[w] = 0u;
+            c->qtail[w] = 0u;
+            c->rowtag[w][0] = c->rowtag[w][1] = 0u;
+            c->rowend[w][0] = c->rowend[w][1] = 0u;
+        }
+        c->sel_done = 0u;
+        c->seed_count = 0u;
+        c->abort = 0u;
+        fence_mbar_init();
+    }
+    if (cs > 1)
+        cluster_sync();
+    else
+        __syncthreads();
+
+    const int L_ = (((p.V + cs - 1) / cs) + 63) & ~63;
+    const int e0 = min(p.V, (int)rank * L_);
+    const int e1 = min(p.V, e0 + L_);
+    const uintptr_t lbase = reinterpret_cast<uintptr_t>(p.logits);
+    const int warp = tid >> 5;
+
+    if (warp == kNF + 1) {
+        // ---------------- producer (one lane), as in the general kernel
+        if (lane == 0) {
+            int it = 0;
+            for (int row = cid; row < p.rows && !*abort_flag; row += ncl) {
+                const uintptr_t a0 = lbase + ((size_t)row * p.V + e0) * esz;
+                const uintptr_t a1 = lbase + ((size_t)row * p.V + e1) * esz;
+                const uintptr_t b0 = (a0 + 15) & ~(uintptr_t)15, b1 = a1 & ~(uintptr_t)15;
+                for (uintptr_t off = b0; off < b1; off += kSB, ++it) {
+                    const int st = it % kNS;
+                    const uint32_t ph = (uint32_t)(it / kNS) & 1u;
+                    if (*abort_flag) break;
+                    if (!mbar_wait_bounded(empty0 + 8 * st, ph ^ 1u, kWaitNs)) {
+                        set_abort(abort_flag);
+                        break;
+                    }
+                    const uint32_t bytes = (uint32_t)min((uintptr_t)kSB, b1 - off);
+                    mbar_arrive_expect_tx(full0 + 8 * st, bytes);
+                    bulk_g2s(s0 + (uint32_t)st * kSB, reinterpret_cast<const void*>(off), bytes,
+                             full0 + 8 * st);
+                }
+            }
+        }
+        __syncwarp();
+        if (cs > 1) cluster_sync();
+        return;
+    }
+
+    if (warp == kNF) {
+        // ---------------- selector warp
+        uint32_t qt[kNF];
+#pragma unroll
+        for (int w = 0; w < kNF; ++w) qt[w] = 0u;
+        int rit = 0;
+        int cur = 0;
+        for (int row = cid; row < p.rows; row += ncl, ++rit) {
+            const int slot = rit & 1;
+            int s = 0;
+            uint64_t* L = Lbuf + cur * kAsyncMaxK;
+            uint32_t done = 0u;
+            unsigned long long pub = 0ull;
+            uint64_t t_idle = 0;
+            uint32_t nap = 32u;  // idle back-off (ns)
+            int nst = 0;  // keys staged in Bs[0, nst) for the next merge
+            if (p.K <= 32) {
+                // The list lives in registers, lane i holding L[i]: an insertion
+                // is one ballot (its place) and one shuffle (the shift), so the
+                // threshold can follow every key.
+                uint64_t Lr = 0ull, kth = 0ull;  // kth: L[K-1] once the list is full
+                while (done != (1u << kNF) - 1u) {
+                    bool prog = false;
+#pragma unroll
+                    for (int w = 0; w < kNF; ++w) {
+                        if ((done >> w) & 1u) continue;
+                        const uint32_t qh = ld_acquire_u32(&c->qhead[w]);
+                        const bool ended =
+                            ld_acquire_u32(&c->rowtag[w][slot]) == (uint32_t)(rit + 1);
+                        const uint32_t lim = ended ? c->rowend[w][slot] : qh;
+                        const uint64_t* q = queues + (size_t)w * kQW;
+                        while (qt[w] != lim && !*abort_flag) {
+                            const uint32_t nb = min(32u, lim - qt[w]);
+                            const uint64_t k =
+                                (uint32_t)lane < nb ? q[(qt[w] + lane) & (kQW - 1)] : 0ull;
+                            uint32_t mask = __ballot_sync(0xffffffffu, k > kth);
+                            qt[w] += nb;
+                            prog = true;
+                            __syncwarp();
+                            if (lane == 0) st_release_u32(&c->qtail[w], qt[w]);
+                            while (mask) {
+                                const int b = __ffs(mask) - 1;
+                                mask &= mask - 1u;
+                                const uint64_t kk = __shfl_sync(0xffffffffu, k, b);
+                                if (kk <= kth) continue;
+                                const int pos =
+                                    __popc(__ballot_sync(0xffffffffu, lane < s && Lr > kk));
+                                const uint64_t up = __shfl_up_sync(0xffffffffu, Lr, 1);
+                                Lr = lane < pos ? Lr : (lane == pos ? kk : up);
+                                if (lane >= p.K) Lr = 0ull;
+                                s = min(s + 1, p.K);
+                                if (s == p.K) kth = __shfl_sync(0xffffffffu, Lr, p.K - 1);
+                            }
+                            if (kth > pub) {
+                                pub = kth;
+                                if (lane == 0) atomicMax(&c->tau[slot], pub);
+                            }
+                        }
+                        if (ended && qt[w] == lim) done |= 1u << w;
+                        if (*abort_flag) done |= 1u << w;
+                    }
+                    if (prog) {
+                        t_idle = 0;
+                        nap = 32u;
+                    } else {
+                        const uint64_t now = global_ns();
+                        if (t_idle == 0) t_idle = now;
+                        else if (now - t_idle > kWaitNs) set_abort(abort_flag);
+                        __nanosleep(nap);
+                        nap = min(2u * nap, 1024u);
+                    }
+                }
+                if (lane < s) L[lane] = Lr;
+            }
+            while (done != (1u << kNF) - 1u) {
+                bool prog = false;
+#pragma unroll
+                for (int w = 0; w < kNF; ++w) {
+                    if ((done >> w) & 1u) continue;
+                    // qhead before the tag: if the tag is not yet set, every key
+                    // below that qhead belongs to this row
+                    const uint32_t qh = ld_acquire_u32(&c->qhead[w]);
+                    const bool ended = ld_acquire_u32(&c->rowtag[w][slot]) == (uint32_t)(rit + 1);
+                    const uint32_t lim = ended ? c->rowend[w][slot] : qh;
+                    const uint64_t* q = queues + (size_t)w * kQW;
+                    while (qt[w] != lim && !*abort_flag) {
+                        // stage the keys that beat the list's K-th (32 at most)
+                        const uint32_t nb = min((uint32_t)(32 - nst), lim - qt[w]);
+                        const uint64_t k = (uint32_t)lane < nb ? q[(qt[w] + lane) & (kQW - 1)] : 0ull;
+                        const bool cand = (uint32_t)lane < nb && (s < p.K || k > L[p.K - 1]);
+                        const uint32_t mask = __ballot_sync(0xffffffffu, cand);
+                        if (cand) Bs[nst + __popc(mask & ((1u << lane) - 1u))] = k;
+                        nst += __popc(mask);
+                        qt[w] += nb;
+                        prog = true;
+                        __syncwarp();
+                        if (lane == 0) st_release_u32(&c->qtail[w], qt[w]);
+                        if (nst >= 24) {
+                            uint64_t* Ln = Lbuf + (cur ^ 1) * kAsyncMaxK;
+                            const uint64_t kb = lane < nst ? Bs[lane] : 0ull;
+                            __syncwarp();
+                            list_merge(L, Ln, s, p.K, kb, Bs);
+                            cur ^= 1;
+                            L = Ln;
+                            nst = 0;
+                            if (s == p.K && L[p.K - 1] > pub) {
+                                pub = L[p.K - 1];
+                                if (lane == 0) atomicMax(&c->tau[slot], pub);
+                            }
+                        }
+                    }
+                    if (ended && qt[w] == lim) done |= 1u << w;
+                    if (*abort_flag) done |= 1u << w;
+                }
+                // merge what is staged (a few keys: one by one), re-checking each
+                // against the K-th, which staging may have raised meanwhile
+                if (nst > 3) {
+                    uint64_t* Ln = Lbuf + (cur ^ 1) * kAsyncMaxK;
+                    uint64_t kb = lane < nst ? Bs[lane] : 0ull;
+                    if (s == p.K && kb != 0ull && kb <= L[p.K - 1]) kb = 0ull;
+                    __syncwarp();
+                    list_merge(L, Ln, s, p.K, kb, Bs);
+                    cur ^= 1;
+                    L = Ln;
+                } else {
+                    for (int i = 0; i < nst; ++i) {
+                        const uint64_t kk = Bs[i];
+                        if (s < p.K || kk > L[p.K - 1]) list_insert(L, s, p.K, kk);
+                    }
+                }
+                nst = 0;
+                if (s == p.K && L[p.K - 1] > pub) {
+                    pub = L[p.K - 1];
+                    if (lane == 0) atomicMax(&c->tau[slot], pub);
+                }
+                if (prog) {
+                    t_idle = 0;
+                    nap = 32u;
+                } else {
+                    const uint64_t now = global_ns();
+                    if (t_idle == 0) t_idle = now;
+                    else if (now - t_idle > kWaitNs) set_abort(abort_flag);
+                    __nanosleep(nap);
+                    nap = min(2u * nap, 1024u);
+                }
+            }
+            __syncwarp();
+            if (cs == 1) {
+                write_sorted<BF16>(L, s, p, row);
+            } else {
+                const uint32_t par = (uint32_t)(rit >> 1) & 1u;
+                if (rank != 0) {
+                    if (!*abort_flag &&
+                        !mbar_wait_cluster_bounded(smem_u32(&c->mempty[slot]), par ^ 1u, kWaitNs))
+                        set_abort(abort_flag);
+                    uint64_t* o = outk + (size_t)slot * kAsyncMaxK;
+                    for (int i = lane; i < s; i += 32) o[i] = L[i];
+                    if (lane == 0) c->out_cnt[slot] = (uint32_t)s;
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_cluster();
+                        mbar_arrive_remote(map_cluster(smem_u32(&c->mfull[slot]), 0));
+                    }
+                } else {
+                    if (!*abort_flag &&
+                        !mbar_wait_cluster_bounded(smem_u32(&c->mfull[slot]), par, kWaitNs))
+                        set_abort(abort_flag);
+                    // the cs sorted lists side by side, K apart: list 0 is ours
+                    int cnt[8];
+                    cnt[0] = s;
+                    for (int i = lane; i < s; i += 32) merge[i] = L[i];
+                    for (int r = 1; r < 8; ++r) {
+                        cnt[r] = 0;
+                        if (r >= cs) continue;
+                        cnt[r] = (int)min(ld_cluster_u32(map_cluster(smem_u32(&c->out_cnt[slot]),
+                                                                     (uint32_t)r)),
+                                          (uint32_t)p.K);
+                        const uint32_t src = map_cluster(
+                            smem_u32(outk + (size_t)slot * kAsyncMaxK), (uint32_t)r);
+                        for (int i = lane; i < cnt[r]; i += 32)
+                            merge[r * kAsyncMaxK + i] = ld_cluster_u64(src + 8u * i);
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_cluster();
+                        for (int r = 1; r < cs; ++r)
+                            mbar_arrive_remote(
+                                map_cluster(smem_u32(&c->mempty[slot]), (uint32_t)r));
+                    }
+                    // rank of each key in the union: its place in its own list plus
+                    // the keys above it in the others (keys are distinct)
+                    int total = 0;
+                    for (int r = 0; r < cs; ++r) total += cnt[r];
+                    int32_t* ids = p.ids + (size_t)row * p.K;
+                    float* vals = p.vals + (size_t)row * p.K;
+                    for (int r = 0; r < cs; ++r) {
+                        for (int i = lane; i < cnt[r]; i += 32) {
+                            const uint64_t k = merge[r * kAsyncMaxK + i];
+                            int rk = i;
+                            for (int r2 = 0; r2 < cs; ++r2)
+                                if (r2 != r) rk += count_greater(merge + r2 * kAsyncMaxK, cnt[r2], k);
+                            if (rk < p.K) {
+                                int32_t id = (int32_t)key_index(k);
+                                float v = key_value(k);
+                                if ((uint32_t)id >= (uint32_t)p.V) {
+                                    atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+                                    id = -1;
+                                    v = __uint_as_float(0x7FC00000u);
+                                } else if (v == 0.f) {
+                                    v = load_logit<BF16>(p.logits, (size_t)row * p.V + (uint32_t)id);
+                                }
+                                ids[rk] = id;
+                                vals[rk] = v;
+                            }
+                        }
+                    }
+                    for (int i = total + lane; i < p.K; i += 32) {
+                        ids[i] = -1;
+                        vals[i] = __uint_as_float(0x7FC00000u);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) st_release_u32(&c->sel_done, (uint32_t)(rit + 1));
+        }
+        __syncwarp();
+        if (cs > 1) cluster_sync();
+        return;
+    }
+
+    // ---------------- filter warps
+    uint64_t* myq = queues + (size_t)warp * kQW;
+    uint32_t qh = 0u;
+    int fst = 0, rit = 0;  // ring stage and its phase parity, carried across rows
+    uint32_t fph = 0u;
+    for (int row = cid; row < p.rows; row += ncl, ++rit) {
+        const int slot = rit & 1;
+        const size_t rowoff = (size_t)row * p.V;
+        const uintptr_t a0 = lbase + (rowoff + e0) * esz;
+        const uintptr_t a1 = lbase + (rowoff + e1) * esz;
+        const uintptr_t b0 = (a0 + 15) & ~(uintptr_t)15, b1 = a1 & ~(uintptr_t)15;
+        const bool body = b0 < b1;
+        const int head = body ? (int)((b0 - a0) / esz) : e1 - e0;
+        const int tail = body ? (int)((a1 - b1) / esz) : 0;
+        const bool seedable = p.K <= kNC && body && b1 - b0 >= kSB;
+        float hx = 0.f, tx = 0.f;
+        if (tid < head) hx = load_logit<BF16>(p.logits, rowoff + e0 + tid);
+        if (tid < tail) tx = load_logit<BF16>(p.logits, rowoff + (e1 - tail) + tid);
+        // at most one row ahead of the selector: this row's threshold slot is free
+        if (lane == 0 && rit >= 2) wait_counter(&c->sel_done, (uint32_t)(rit - 1), abort_flag);
+        __syncwarp();
+        named_bar_sync(1, kNC);
+        if (tid == 0) {
+            c->tau[slot] = 0ull;  // no threshold yet: every non-NaN element is a candidate
+            c->seed_count = 0u;
+        }
+        named_bar_sync(1, kNC);
+        if (!seedable && warp == 0)
+            push_one(tid < head && hx == hx, hx, (uint32_t)(e0 + tid), myq, qh, c, warp, abort_flag);
+
+        int ks = 0;
+        for (uintptr_t off = b0; off < b1; off += kSB, ++ks) {
+            const int st = fst;
+            const uint32_t ph = fph;
+            if (++fst == kNS) {
+                fst = 0;
+                fph ^= 1u;
+            }
+            if (!*abort_flag && !mbar_wait_bounded(full0 + 8 * st, ph, kWaitNs)) set_abort(abort_flag);
+            const uint32_t nvec = (uint32_t)min((uintptr_t)kSB, b1 - off) / 16u;
+            const uint32_t ebase = (uint32_t)e0 + (uint32_t)((off - a0) / esz);
+            const uint32_t sb = s0 + (uint32_t)st * kSB;
+            uint32_t w[kWPT];
+#pragma unroll
+            for (int q = 0; q < VPT; ++q) {
+                const uint32_t v = (uint32_t)(q * kNC + tid);
+                uint4 u = make_uint4(kNaNWord, kNaNWord, kNaNWord, kNaNWord);  // NaN passes no test
+                if (v < nvec) u = lds_v4(sb + v * 16u);
+                w[4 * q] = u.x;
+                w[4 * q + 1] = u.y;
+                w[4 * q + 2] = u.z;
+                w[4 * q + 3] = u.w;
+            }
+            const uint32_t idx0 = ebase + (uint32_t)tid * (uint32_t)E;
+            const float mx = stage_max<BF16>(w);
+            if (seedable && ks == 0) {
+                // First (full) stage: the K-th largest of the per-thread maxima
+                // and the head values bounds the K-th best of the row from below.
+                int me = -1;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e)
+                    if (me < 0 && stage_elem<BF16>(w, e) == mx) me = e;  // mx is NaN: none
+                if (me >= 0)
+                    seedbuf[atomicAdd(&c->seed_count, 1u)] = make_key(mx, stage_index<E>(idx0, me));
+                if (tid < head && hx == hx)
+                    seedbuf[atomicAdd(&c->seed_count, 1u)] = make_key(hx, (uint32_t)(e0 + tid));
+                named_bar_sync(1, kNC);
+                const int M = (int)c->seed_count;
+                if (M > p.K) {
+                    const uint64_t kth = select_small(seedbuf, M, p.K, seedtmp, &c->seed_count);
+                    const float bound = key_value(kth);
+                    // key of (bound, largest index): x beats it iff x >= bound
+                    if (tid == 0 && bound != -INFINITY) c->tau[slot] = make_key(bound, 0xFFFFFFFFu);
+                }
+                named_bar_sync(1, kNC);
+                if (warp == 0) {
+                    const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+                    const bool pass = tid < head && hx == hx && make_key(hx, (uint32_t)(e0 + tid)) > tk;
+                    push_one(pass, hx, (uint32_t)(e0 + tid), myq, qh, c, warp, abort_flag);
+                }
+            }
+            const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+            const float tv = (tk >> 32) == 0ull ? -INFINITY : key_value(tk);
+            if (__any_sync(0xffffffffu, mx >= tv)) {
+                // key > tk: value above tv, or equal to it (-0 == +0) with an
+                // index below the threshold's (complemented in the key)
+                uint32_t m = 0, mt = 0;
+#pragma unroll
+                for (int e = 0; e < EPT; ++e) {
+                    const float x = stage_elem<BF16>(w, e);
+                    m |= (x > tv ? 1u : 0u) << e;
+                    mt |= (x == tv ? 1u : 0u) << e;
+                }
+                const uint32_t ti = ~(uint32_t)tk;
+                for (uint32_t mm = mt; mm; mm &= mm - 1u) {
+                    const int e = __ffs(mm) - 1;
+                    if (stage_index<E>(idx0, e) < ti) m |= 1u << e;
+                }
+                push_keys<BF16, E>(m, sb, idx0, myq, qh, c, warp, abort_flag);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * st);  // done with the stage
+        }
+        if (warp == 0 && tail > 0) {
+            const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+            const uint32_t ti = (uint32_t)(e1 - tail + tid);
+            push_one(tid < tail && tx == tx && make_key(tx, ti) > tk, tx, ti, myq, qh, c, warp,
+                     abort_flag);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            c->rowend[warp][slot] = qh;
+            st_release_u32(&c->rowtag[warp][slot], (uint32_t)(rit + 1));
+        }
+    }
+    // On an abandoned pipeline, give copies still in flight a bounded time to
+    // land before the CTA's shared memory is released.
+    if (tid == 0 && *abort_flag) {
+        for (int i = 0; i < kNS; ++i) mbar_wait_bounded(full0 + 8 * i, 0, kWaitNs / 4);
+    }
+    __syncwarp();
+    if (cs > 1) cluster_sync();
+}
+
 struct DeviceInfo {
     bool ready = false;
-    int max_clusters[2][4] = {};  // [bf16][log2 cs]: clusters resident at once
+    int max_clusters[2][2][4] = {};  // [async][bf16][log2 cs]: clusters resident at once
 };
 
 std::mutex g_mu;
 DeviceInfo g_info[64];
 
-template <bool BF16>
-cudaError_t query_device(DeviceInfo& d) {
-    auto kern = topk_kernel<BF16>;
+template <typename Kern>
+cudaError_t query_kernel(Kern kern, uint32_t smem_bytes, int threads, int (&out)[4]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmem);
+                                         (int)smem_bytes);
     if (e != cudaSuccess) return e;
     for (int l = 0; l < 4; ++l) {
         const int cs = 1 << l;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(cs, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmem;
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = cs;
@@ -669,36 +1362,44 @@ cudaError_t query_device(DeviceInfo& d) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
             (void)cudaGetLastError();
             n = 0;
         }
-        d.max_clusters[BF16 ? 1 : 0][l] = n;
+        out[l] = n;
     }
     return cudaSuccess;
 }
 
-template <bool BF16>
-cudaError_t launch_t(const TopkLaunch& a, cudaStream_t stream) {
+cudaError_t query_device(DeviceInfo& d) {
+    cudaError_t e = query_kernel(topk_kernel<false>, kSmem, kThreads, d.max_clusters[0][0]);
+    if (e == cudaSuccess) e = query_kernel(topk_kernel<true>, kSmem, kThreads, d.max_clusters[0][1]);
+    if (e == cudaSuccess)
+        e = query_kernel(topk_async_kernel<false>, kASmem, kAThreads, d.max_clusters[1][0]);
+    if (e == cudaSuccess)
+        e = query_kernel(topk_async_kernel<true>, kASmem, kAThreads, d.max_clusters[1][1]);
+    return e;
+}
+
+cudaError_t launch_any(const TopkLaunch& a, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const bool async = a.K <= kAsyncMaxK;
     int maxc[4];
     {
         std::lock_guard<std::mutex> lk(g_mu);
         DeviceInfo& d = g_info[dev];
         if (!d.ready) {
-            e = query_device<false>(d);
-            if (e == cudaSuccess) e = query_device<true>(d);
+            e = query_device(d);
             if (e != cudaSuccess) return e;
             d.ready = true;
         }
-        for (int l = 0; l < 4; ++l) maxc[l] = d.max_clusters[BF16 ? 1 : 0][l];
+        for (int l = 0; l < 4; ++l) maxc[l] = d.max_clusters[async ? 1 : 0][a.bf16 ? 1 : 0][l];
     }
     // cluster size: the fewest waves of the longest per-CTA chunk, plus a fixed
-    // per-row cost (selection, merge) worth about 8192 elements
+    // per-row cost (seeding, selection, merge) worth about 8192 elements
     int best_l = -1;
     long long best_cost = 0;
     for (int l = 0; l < 4; ++l) {
@@ -717,8 +1418,8 @@ cudaError_t launch_t(const TopkLaunch& a, cudaStream_t stream) {
     TopkParams p{a.logits, a.rows, a.V, a.K, cs, a.ids, a.vals};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(nclusters * cs), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.blockDim = dim3(async ? kAThreads : kThreads, 1, 1);
+    cfg.dynamicSmemBytes = async ? kASmem : kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -727,14 +1428,16 @@ cudaError_t launch_t(const TopkLaunch& a, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cs > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, topk_kernel<BF16>, p);
+    if (async)
+        return a.bf16 ? cudaLaunchKernelEx(&cfg, topk_async_kernel<true>, p)
+                      : cudaLaunchKernelEx(&cfg, topk_async_kernel<false>, p);
+    return a.bf16 ? cudaLaunchKernelEx(&cfg, topk_kernel<true>, p)
+                  : cudaLaunchKernelEx(&cfg, topk_kernel<false>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
-    return a.bf16 ? launch_t<true>(a, stream) : launch_t<false>(a, stream);
-}
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) { return launch_any(a, stream); }
 
 cudaError_t take_topk_faults(unsigned* flags) {
     unsigned v = 0, zero = 0;
