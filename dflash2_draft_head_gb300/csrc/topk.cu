@@ -663,9 +663,8 @@ static_assert(kNF * 32 == kNC, "the filter warps are the kNC threads of the seed
 static_assert(32 * 8 * kVPT <= kQW, "one stage's pushes must fit a queue");
 
 constexpr uint32_t kAQueue = kNS * kSB;
-constexpr uint32_t kASeed = kAQueue + kNF * kQW * 8;
-constexpr uint32_t kASeedTmp = kASeed + 2 * kNC * 8;
-constexpr uint32_t kAList = kASeedTmp + kAsyncMaxK * 8;
+constexpr uint32_t kASeedLists = kAQueue + kNF * kQW * 8;  // 2 x 256 keys
+constexpr uint32_t kAList = kASeedLists + 2 * kNC * 8;
 constexpr uint32_t kABatch = kAList + 2 * kAsyncMaxK * 8;
 constexpr uint32_t kAOut = kABatch + 32 * 8;
 constexpr uint32_t kAMerge = kAOut + 2 * kAsyncMaxK * 8;
@@ -683,8 +682,8 @@ struct ACtl {
     uint32_t qtail[kNF];        // keys the selector has taken from each queue
     uint32_t rowend[kNF][2];    // qhead at the end of a row, by row parity
     uint32_t rowtag[kNF][2];    // (row iteration + 1) that rowend belongs to
+    unsigned long long seedk[2];       // seeding bound key, by row parity (0: none)
     uint32_t sel_done;          // rows the selector has finished
-    uint32_t seed_count;
     uint32_t out_cnt[2];
     uint32_t abort;
 };
@@ -904,9 +903,8 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t s0 = smem_u32(smem);
     uint64_t* queues = reinterpret_cast<uint64_t*>(smem + kAQueue);
-    uint64_t* seedbuf = reinterpret_cast<uint64_t*>(smem + kASeed);
-    uint64_t* seedtmp = reinterpret_cast<uint64_t*>(smem + kASeedTmp);
     uint64_t* Lbuf = reinterpret_cast<uint64_t*>(smem + kAList);  // two lists of kAsyncMaxK
+    uint64_t* slists = reinterpret_cast<uint64_t*>(smem + kASeedLists);
     uint64_t* Bs = reinterpret_cast<uint64_t*>(smem + kABatch);
     uint64_t* outk = reinterpret_cast<uint64_t*>(smem + kAOut);
     uint64_t* merge = reinterpret_cast<uint64_t*>(smem + kAMerge);
@@ -938,7 +936,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             c->rowend[w][0] = c->rowend[w][1] = 0u;
         }
         c->sel_done = 0u;
-        c->seed_count = 0u;
+        c->seedk[0] = c->seedk[1] = 0ull;
         c->abort = 0u;
         fence_mbar_init();
     }
@@ -1050,7 +1048,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                         if (t_idle == 0) t_idle = now;
                         else if (now - t_idle > kWaitNs) set_abort(abort_flag);
                         __nanosleep(nap);
-                        nap = min(2u * nap, 1024u);
+                        nap = min(2u * nap, 512u);
                     }
                 }
                 if (lane < s) L[lane] = Lr;
@@ -1124,7 +1122,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     if (t_idle == 0) t_idle = now;
                     else if (now - t_idle > kWaitNs) set_abort(abort_flag);
                     __nanosleep(nap);
-                    nap = min(2u * nap, 1024u);
+                    nap = min(2u * nap, 512u);
                 }
             }
             __syncwarp();
@@ -1204,7 +1202,10 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 }
             }
             __syncwarp();
-            if (lane == 0) st_release_u32(&c->sel_done, (uint32_t)(rit + 1));
+            if (lane == 0) {
+                c->tau[slot] = 0ull;  // free for row rit + 2
+                st_release_u32(&c->sel_done, (uint32_t)(rit + 1));
+            }
         }
         __syncwarp();
         if (cs > 1) cluster_sync();
@@ -1225,19 +1226,17 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
         const bool body = b0 < b1;
         const int head = body ? (int)((b0 - a0) / esz) : e1 - e0;
         const int tail = body ? (int)((a1 - b1) / esz) : 0;
-        const bool seedable = p.K <= kNC && body && b1 - b0 >= kSB;
+        // the same for every row of this CTA (the chunk length is), so the
+        // filter warps pass the seeding barrier on the same rows
+        const bool seedable = p.K <= kAsyncMaxK && (uint32_t)(e1 - e0) * esz >= kSB + 32u;
+        unsigned long long seed_key = 0ull;
         float hx = 0.f, tx = 0.f;
         if (tid < head) hx = load_logit<BF16>(p.logits, rowoff + e0 + tid);
         if (tid < tail) tx = load_logit<BF16>(p.logits, rowoff + (e1 - tail) + tid);
-        // at most one row ahead of the selector: this row's threshold slot is free
+        // At most one row ahead of the selector: it has finished the row that
+        // last used this threshold slot and reset it to 0 (no threshold).
         if (lane == 0 && rit >= 2) wait_counter(&c->sel_done, (uint32_t)(rit - 1), abort_flag);
         __syncwarp();
-        named_bar_sync(1, kNC);
-        if (tid == 0) {
-            c->tau[slot] = 0ull;  // no threshold yet: every non-NaN element is a candidate
-            c->seed_count = 0u;
-        }
-        named_bar_sync(1, kNC);
         if (!seedable && warp == 0)
             push_one(tid < head && hx == hx, hx, (uint32_t)(e0 + tid), myq, qh, c, warp, abort_flag);
 
@@ -1267,32 +1266,55 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             const uint32_t idx0 = ebase + (uint32_t)tid * (uint32_t)E;
             const float mx = stage_max<BF16>(w);
             if (seedable && ks == 0) {
-                // First (full) stage: the K-th largest of the per-thread maxima
-                // and the head values bounds the K-th best of the row from below.
+                // First (full) stage: the K-th largest of the 256 lane maxima is at
+                // most the row's K-th best (those K maxima are distinct elements).
+                // Every warp sorts its 32 maxima; a candidate's rank among all 256
+                // is its place in its own sorted list plus the keys above it in the
+                // other seven (binary searches); the one of rank K-1 is the bound.
                 int me = -1;
 #pragma unroll
                 for (int e = 0; e < EPT; ++e)
                     if (me < 0 && stage_elem<BF16>(w, e) == mx) me = e;  // mx is NaN: none
-                if (me >= 0)
-                    seedbuf[atomicAdd(&c->seed_count, 1u)] = make_key(mx, stage_index<E>(idx0, me));
-                if (tid < head && hx == hx)
-                    seedbuf[atomicAdd(&c->seed_count, 1u)] = make_key(hx, (uint32_t)(e0 + tid));
+                uint64_t kk = me >= 0 ? make_key(mx, stage_index<E>(idx0, me)) : 0ull;
+#pragma unroll
+                for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                    for (int j = size >> 1; j > 0; j >>= 1) {
+                        const uint64_t o = __shfl_xor_sync(0xffffffffu, kk, j);
+                        const bool desc = (lane & size) == 0;
+                        const bool lower = (lane & j) == 0;
+                        kk = (lower == desc) ? (kk > o ? kk : o) : (kk < o ? kk : o);
+                    }
+                }
+                uint64_t* sl = slists + (size_t)slot * kNC;  // 8 sorted lists of 32
+                sl[tid] = kk;
                 named_bar_sync(1, kNC);
-                const int M = (int)c->seed_count;
-                if (M > p.K) {
-                    const uint64_t kth = select_small(seedbuf, M, p.K, seedtmp, &c->seed_count);
-                    const float bound = key_value(kth);
-                    // key of (bound, largest index): x beats it iff x >= bound
-                    if (tid == 0 && bound != -INFINITY) c->tau[slot] = make_key(bound, 0xFFFFFFFFu);
+                if (tid == 0) c->seedk[slot ^ 1] = 0ull;  // the other row's readers are done
+                if (kk != 0ull && lane < p.K) {
+                    int rk = lane;
+#pragma unroll
+                    for (int v = 0; v < kNF; ++v)
+                        if (v != warp) rk += count_greater(sl + v * 32, 32, kk);
+                    if (rk == p.K - 1) c->seedk[slot] = kk;
                 }
                 named_bar_sync(1, kNC);
+                const uint64_t bk = c->seedk[slot];
+                // 0: fewer than K lanes held a non-NaN element (no bound); a bound
+                // of -inf has no float below it either
+                if (bk != 0ull && key_value(bk) != -INFINITY && tid == 0)
+                    atomicMax(&c->tau[slot], make_key(key_value(bk), 0xFFFFFFFFu));
                 if (warp == 0) {
-                    const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+                    unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+                    if (bk != 0ull && key_value(bk) != -INFINITY)
+                        tk = max(tk, (unsigned long long)make_key(key_value(bk), 0xFFFFFFFFu));
                     const bool pass = tid < head && hx == hx && make_key(hx, (uint32_t)(e0 + tid)) > tk;
                     push_one(pass, hx, (uint32_t)(e0 + tid), myq, qh, c, warp, abort_flag);
                 }
+                seed_key = (bk != 0ull && key_value(bk) != -INFINITY)
+                               ? (unsigned long long)make_key(key_value(bk), 0xFFFFFFFFu)
+                               : 0ull;
             }
-            const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
+            const unsigned long long tk = max(ld_volatile_u64(&c->tau[slot]), seed_key);
             const float tv = (tk >> 32) == 0ull ? -INFINITY : key_value(tk);
             if (__any_sync(0xffffffffu, mx >= tv)) {
                 // key > tk: value above tv, or equal to it (-0 == +0) with an
