@@ -683,6 +683,9 @@ struct ACtl {
     uint32_t rowend[kNF][2];    // qhead at the end of a row, by row parity
     uint32_t rowtag[kNF][2];    // (row iteration + 1) that rowend belongs to
     unsigned long long seedk[2];       // seeding bound key, by row parity (0: none)
+    // best bound any CTA of the cluster has for the row, by row parity:
+    // (row iteration + 1) << 32 | ordered value bits; x >= that value passes
+    unsigned long long cbound[2];
     uint32_t sel_done;          // rows the selector has finished
     uint32_t out_cnt[2];
     uint32_t abort;
@@ -703,6 +706,20 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
     unsigned long long v;
     asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
     return v;
+}
+
+// Offers the value part of threshold key tk for row iteration rit to every CTA
+// of the cluster (lane r of the calling warp writes to rank r; lanes >= cs
+// idle).  The word's high half is the row tag, so a late offer for an older
+// row never wins over, or passes for, the current row's.
+__device__ __forceinline__ void share_bound(unsigned long long* cb, int cs, int rit,
+                                            unsigned long long tk) {
+    const int lane = threadIdx.x & 31;
+    if (lane < cs && (tk >> 32) != 0ull) {
+        const unsigned long long word = ((unsigned long long)(uint32_t)(rit + 1) << 32) | (tk >> 32);
+        const uint32_t a = map_cluster(smem_u32(cb), (uint32_t)lane);
+        asm volatile("red.shared::cluster.max.u64 [%0], %1;" ::"r"(a), "l"(word) : "memory");
+    }
 }
 
 // Marks the pipeline abandoned (a bounded wait gave up).
@@ -869,6 +886,46 @@ __device__ __forceinline__ void list_merge(const uint64_t* L, uint64_t* Ln, int&
     s = min(s + nb, K);
 }
 
+// Sorts one 64-bit key per lane into descending lane order (bitonic network).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t k) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, k, j);
+            const bool desc = (lane & size) == 0;
+            const bool lower = (lane & j) == 0;
+            k = (lower == desc) ? (k > o ? k : o) : (k < o ? k : o);
+        }
+    }
+    return k;
+}
+
+// The 32 largest of two descending lane-sorted sequences a and b, descending:
+// max(a[i], b[31-i]) holds the 32 largest and is bitonic; five half-cleaner
+// steps sort it.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t a, uint64_t b) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t br = __shfl_sync(0xffffffffu, b, 31 - lane);
+    uint64_t k = a > br ? a : br;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, k, j);
+        k = ((lane & j) == 0) ? (k > o ? k : o) : (k < o ? k : o);
+    }
+    return k;
+}
+
+// Number of keys greater than k in the descending list l[0, 32): a fixed
+// binary descent (no data-dependent trip count) so that several can overlap.
+__device__ __forceinline__ int count_greater32(const uint64_t* l, uint64_t k) {
+    int pos = 0;
+#pragma unroll
+    for (int step = 16; step >= 1; step >>= 1) pos += l[pos + step - 1] > k ? step : 0;
+    return pos + (l[pos] > k ? 1 : 0);
+}
+
 // Writes one output row from the sorted list (selector warp).
 template <bool BF16>
 __device__ void write_sorted(const uint64_t* L, int n, const TopkParams& p, int row) {
@@ -937,6 +994,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
         }
         c->sel_done = 0u;
         c->seedk[0] = c->seedk[1] = 0ull;
+        c->cbound[0] = c->cbound[1] = 0ull;
         c->abort = 0u;
         fence_mbar_init();
     }
@@ -1019,6 +1077,15 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                             prog = true;
                             __syncwarp();
                             if (lane == 0) st_release_u32(&c->qtail[w], qt[w]);
+                            if (__popc(mask) >= 4) {
+                                // many at once: sort them and merge with the list
+                                const uint64_t kb = warp_sort_desc(k > kth ? k : 0ull);
+                                Lr = warp_merge_desc(Lr, kb);
+                                if (lane >= p.K) Lr = 0ull;
+                                s = min(s + __popc(mask), p.K);
+                                if (s == p.K) kth = __shfl_sync(0xffffffffu, Lr, p.K - 1);
+                                mask = 0u;
+                            }
                             while (mask) {
                                 const int b = __ffs(mask) - 1;
                                 mask &= mask - 1u;
@@ -1035,6 +1102,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                             if (kth > pub) {
                                 pub = kth;
                                 if (lane == 0) atomicMax(&c->tau[slot], pub);
+                                if (cs > 1) share_bound(&c->cbound[slot], cs, rit, pub);
                             }
                         }
                         if (ended && qt[w] == lim) done |= 1u << w;
@@ -1087,6 +1155,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                             if (s == p.K && L[p.K - 1] > pub) {
                                 pub = L[p.K - 1];
                                 if (lane == 0) atomicMax(&c->tau[slot], pub);
+                                if (cs > 1) share_bound(&c->cbound[slot], cs, rit, pub);
                             }
                         }
                     }
@@ -1113,6 +1182,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 if (s == p.K && L[p.K - 1] > pub) {
                     pub = L[p.K - 1];
                     if (lane == 0) atomicMax(&c->tau[slot], pub);
+                                if (cs > 1) share_bound(&c->cbound[slot], cs, rit, pub);
                 }
                 if (prog) {
                     t_idle = 0;
@@ -1275,17 +1345,8 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
 #pragma unroll
                 for (int e = 0; e < EPT; ++e)
                     if (me < 0 && stage_elem<BF16>(w, e) == mx) me = e;  // mx is NaN: none
-                uint64_t kk = me >= 0 ? make_key(mx, stage_index<E>(idx0, me)) : 0ull;
-#pragma unroll
-                for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-                    for (int j = size >> 1; j > 0; j >>= 1) {
-                        const uint64_t o = __shfl_xor_sync(0xffffffffu, kk, j);
-                        const bool desc = (lane & size) == 0;
-                        const bool lower = (lane & j) == 0;
-                        kk = (lower == desc) ? (kk > o ? kk : o) : (kk < o ? kk : o);
-                    }
-                }
+                const uint64_t kk =
+                    warp_sort_desc(me >= 0 ? make_key(mx, stage_index<E>(idx0, me)) : 0ull);
                 uint64_t* sl = slists + (size_t)slot * kNC;  // 8 sorted lists of 32
                 sl[tid] = kk;
                 named_bar_sync(1, kNC);
@@ -1294,7 +1355,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     int rk = lane;
 #pragma unroll
                     for (int v = 0; v < kNF; ++v)
-                        if (v != warp) rk += count_greater(sl + v * 32, 32, kk);
+                        if (v != warp) rk += count_greater32(sl + v * 32, kk);
                     if (rk == p.K - 1) c->seedk[slot] = kk;
                 }
                 named_bar_sync(1, kNC);
@@ -1313,8 +1374,13 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 seed_key = (bk != 0ull && key_value(bk) != -INFINITY)
                                ? (unsigned long long)make_key(key_value(bk), 0xFFFFFFFFu)
                                : 0ull;
+                if (cs > 1 && warp == 0) share_bound(&c->cbound[slot], cs, rit, seed_key);
             }
-            const unsigned long long tk = max(ld_volatile_u64(&c->tau[slot]), seed_key);
+            unsigned long long tk = max(ld_volatile_u64(&c->tau[slot]), seed_key);
+            if (cs > 1) {
+                const unsigned long long cw = ld_volatile_u64(&c->cbound[slot]);
+                if ((uint32_t)(cw >> 32) == (uint32_t)(rit + 1)) tk = max(tk, (cw & 0xFFFFFFFFull) << 32);
+            }
             const float tv = (tk >> 32) == 0ull ? -INFINITY : key_value(tk);
             if (__any_sync(0xffffffffu, mx >= tv)) {
                 // key > tk: value above tv, or equal to it (-0 == +0) with an
