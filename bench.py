@@ -44,6 +44,12 @@ TRAFFIC = {
         "sha": "47572124d5f40e41464a543ea1c97502bb69257dab6c86207b28879788e5e683",
         "bytes": 51192576 + 2756096,  # dram__bytes_read.sum + dram__bytes_write.sum
     },
+    # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
+    # streams once, so DRAM traffic grows in proportion to the rows
+    ("batched_256x16_d5120", "topk"): {
+        "sha": "9a55b3583121964ddebdf496a7fbb8d5aa75eeea8fe6cee46801ab39210312e7",
+        "bytes": 8 * (311319040 + 3629312),
+    },
 }
 
 
