@@ -63,6 +63,8 @@ def _load():
             lib.oracle_select.restype = ctypes.c_int
             lib.oracle_topk.argtypes = [dp, L, L, L, ip, dp]
             lib.oracle_topk.restype = ctypes.c_int
+            lib.oracle_chain.argtypes = [ip, dp, dp, ip, ip, L, L, L, ctypes.c_double, ip, dp, ip]
+            lib.oracle_chain.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -188,6 +190,31 @@ def topk(z, K):
     if _load().oracle_topk(_dp(z), rows, V, K, _ip(ids), _dp(vals)) != 0:
         raise ValueError("oracle_topk: need 1 <= K <= V")
     return ids, vals
+
+
+def chain(cand_ids, unary, edges, best_slot, p_min, start_slot=None):
+    """(tokens [S,n] int32, probs [S,n] float64, length [S] int32) of the greedy
+    chain through each sequence's argmax table, cut at the first p < p_min.
+
+    cand_ids, unary [S,n,K]; edges [S,n-1,K,K]; best_slot [S,n-1,K];
+    start_slot [S] (a slot, or -1 for the unary argmax) or None.
+    """
+    cand_ids = _i32(cand_ids)
+    S, n, K = cand_ids.shape
+    unary = _f64(unary)
+    E = max(n - 1, 0)
+    edges = _f64(edges).reshape(S, E, K, K) if E else np.zeros((1,), np.float64)
+    best_slot = _i32(best_slot).reshape(S, E, K) if E else np.zeros((1,), np.int32)
+    st = None if start_slot is None else _i32(start_slot)
+    tokens = np.empty((S, n), np.int32)
+    probs = np.empty((S, n), np.float64)
+    length = np.empty((S,), np.int32)
+    rc = _load().oracle_chain(_ip(cand_ids), _dp(unary), _dp(edges), _ip(best_slot),
+                              _ip(st) if st is not None else ctypes.POINTER(ctypes.c_int32)(),
+                              S, n, K, float(p_min), _ip(tokens), _dp(probs), _ip(length))
+    if rc != 0:
+        raise ValueError("oracle_chain: slot outside [0, K)")
+    return tokens, probs, length
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -207,3 +207,61 @@ int oracle_topk(const double* z, long rows, long V, long K, int32_t* ids, double
     }
     return fail;
 }
+
+/*
+ * Greedy chain readout with a p_min cut, the step after the selector (the
+ * pull request names "selector + p_min" as the DFlash2 draft path but gives no
+ * formula; readings taken here):
+ *   slot_0 = start_slot[s] if given (>= 0), else the argmax over k of
+ *            unary[s,0,k] (lowest k on ties);
+ *   slot_i = best_slot[s,i-1,slot_{i-1}]  (each predecessor's argmax candidate);
+ *   p_0 = softmax_k(unary[s,0,:])[slot_0];
+ *   p_i = softmax_c(edges[s,i-1,slot_{i-1},:])[slot_i], the chosen candidate's
+ *         share among the K scores leaving the chosen predecessor;
+ *   tokens[s,i] = cand_ids[s,i,slot_i];
+ *   length[s] = the number of leading positions with p_i >= p_min.
+ * The softmax is taken about the row maximum (exp(x - max) / sum exp(y - max)).
+ * Returns 0, or 1 if a slot falls outside [0, K).
+ */
+int oracle_chain(const int32_t* cand_ids, const double* unary, const double* edges,
+                 const int32_t* best_slot, const int32_t* start_slot, long S, long n, long K,
+                 double p_min, int32_t* tokens, double* probs, int32_t* length) {
+    int bad = 0;
+    long s;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (s = 0; s < S; ++s) {
+        const double* u0 = unary + (s * n) * K;
+        long slot = start_slot != NULL ? start_slot[s] : -1;
+        if (slot < 0) {
+            slot = 0;
+            for (long k = 1; k < K; ++k)
+                if (u0[k] > u0[slot]) slot = k;
+        }
+        if (slot >= K) { bad = 1; continue; }
+        double mx = u0[0];
+        for (long k = 1; k < K; ++k) if (u0[k] > mx) mx = u0[k];
+        double z = 0.0;
+        for (long k = 0; k < K; ++k) z += exp(u0[k] - mx);
+        double p = exp(u0[slot] - mx) / z;
+        int32_t len = 0;
+        int open = 1;
+        for (long i = 0; i < n; ++i) {
+            if (i > 0) {
+                const double* row = edges + (((s * (n - 1) + (i - 1)) * K) + slot) * K;
+                const long next = best_slot[(s * (n - 1) + (i - 1)) * K + slot];
+                if (next < 0 || next >= K) { bad = 1; break; }
+                double m2 = row[0];
+                for (long c = 1; c < K; ++c) if (row[c] > m2) m2 = row[c];
+                double z2 = 0.0;
+                for (long c = 0; c < K; ++c) z2 += exp(row[c] - m2);
+                p = exp(row[next] - m2) / z2;
+                slot = next;
+            }
+            tokens[s * n + i] = cand_ids[(s * n + i) * K + slot];
+            probs[s * n + i] = p;
+            if (open && p >= p_min) ++len; else open = 0;
+        }
+        length[s] = len;
+    }
+    return bad;
+}

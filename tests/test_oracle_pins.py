@@ -384,3 +384,84 @@ def test_topk_nan_and_inf_rows():
         assert np.all(ids[r, m:] == -1) and np.all(np.isnan(vals[r, m:]))
     assert ids[1, 0] == 7 and ids[1, 1] == 0          # 0.5 first, then -inf by index
     assert ids[2, 0] == 5 and np.all(ids[2, 1:] == -1)
+
+
+# ---------------------------------------------------------------- chain readout pins
+
+def test_chain_golden_hand_worked():
+    g = json.load(open(os.path.join(GOLD, "chain_hand.json")))
+    cand = np.array(g["cand_ids"])
+    unary = np.log(np.array(g["unary_w"], float))
+    edges = np.log(np.array(g["edges_w"], float))
+    bs = np.array(g["best_slot"])
+    for pm, want_len in g["length"].items():
+        t, p, L = oracle.chain(cand, unary, edges, bs, float(pm))
+        np.testing.assert_array_equal(t, np.array(g["tokens"]))
+        np.testing.assert_allclose(p, np.array(g["probs"]), rtol=1e-12)
+        assert int(L[0]) == want_len, pm
+    t, p, L = oracle.chain(cand, unary, edges, bs, 0.0, start_slot=np.array([1]))
+    np.testing.assert_array_equal(t, np.array(g["start1_tokens"]))
+    np.testing.assert_allclose(p, np.array(g["start1_probs"]), rtol=1e-12)
+
+
+def test_chain_follows_argmax_and_scipy_softmax():
+    """Slots from numpy.argmax over the oracle's own edge rows, shares from
+    scipy.special.softmax (library routines), on a random lattice."""
+    from scipy.special import softmax
+    rng = _rng(11)
+    S, n, K, R, V = 3, 7, 6, 8, 50
+    ids = np.stack([np.stack([rng.choice(V, K, replace=False) for _ in range(n)]) for _ in range(S)])
+    u = rng.standard_normal((S * n, R))
+    A, B = rng.standard_normal((V, R)), rng.standard_normal((V, R))
+    un = rng.standard_normal((S, n, K))
+    e, bs, _ = oracle.edges(ids, u, A, B, un)
+    t, p, L = oracle.chain(ids, un, e, bs, 0.0)
+    for s in range(S):
+        slot = int(np.argmax(un[s, 0]))
+        assert abs(p[s, 0] - softmax(un[s, 0])[slot]) < 1e-12
+        assert t[s, 0] == ids[s, 0, slot]
+        for i in range(1, n):
+            row = e[s, i - 1, slot]
+            nxt = int(np.argmax(row))
+            assert abs(p[s, i] - softmax(row)[nxt]) < 1e-12
+            slot = nxt
+            assert t[s, i] == ids[s, i, slot]
+        assert L[s] == n
+
+
+def test_chain_cut_closed_forms():
+    rng = _rng(12)
+    S, n, K = 4, 5, 3
+    ids = rng.integers(0, 100, (S, n, K)).astype(np.int32)
+    un = rng.standard_normal((S, n, K))
+    e = rng.standard_normal((S, n - 1, K, K))
+    bs = e.argmax(axis=-1).astype(np.int32)
+    _, p, L0 = oracle.chain(ids, un, e, bs, 0.0)
+    assert np.all(L0 == n) and np.all((p > 0) & (p <= 1))
+    _, _, L1 = oracle.chain(ids, un, e, bs, 1.01)
+    assert np.all(L1 == 0)
+    prev = L0
+    for pm in np.linspace(0.0, 1.0, 21):                 # non-increasing in p_min
+        _, pp, Lm = oracle.chain(ids, un, e, bs, pm)
+        assert np.all(Lm <= prev)
+        for s in range(S):                                 # = leading run of p >= p_min
+            assert Lm[s] == next((i for i in range(n) if pp[s, i] < pm), n)
+        prev = Lm
+    # constant rows: every share is 1/K; K = 1: every share is 1
+    _, pc, _ = oracle.chain(ids, np.zeros_like(un), np.zeros_like(e), np.zeros_like(bs), 0.0)
+    np.testing.assert_allclose(pc, 1.0 / K, rtol=1e-12)
+    _, p1, L1k = oracle.chain(ids[:, :, :1], un[:, :, :1], e[:, :, :1, :1],
+                              np.zeros((S, n - 1, 1), np.int32), 1.0)
+    np.testing.assert_allclose(p1, 1.0) and np.testing.assert_array_equal(L1k, n)
+    # one position: only p0
+    t, p, L = oracle.chain(ids[:, :1], un[:, :1], None, None, 0.5)
+    assert t.shape == (S, 1) and np.all(L == (p[:, 0] >= 0.5))
+
+
+def test_chain_rejects_bad_slot():
+    ids = np.zeros((1, 2, 2), np.int32)
+    with pytest.raises(ValueError):
+        oracle.chain(ids, np.zeros((1, 2, 2)), np.zeros((1, 1, 2, 2)), np.array([[[5, 0]]]), 0.0)
+    with pytest.raises(ValueError):
+        oracle.chain(ids, np.zeros((1, 2, 2)), np.zeros((1, 1, 2, 2)), np.zeros((1, 1, 2)), 0.0,
+                     start_slot=np.array([2]))
