@@ -36,6 +36,7 @@ UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FLUSH_BYTES = 256 << 20
+P_MIN = 0.05  # draft-probability cut of the chain readout line
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by the
 # sha256 of the kernel source they were taken on (null when the source changed).
@@ -518,6 +519,27 @@ def main():
     topk_b = P * w.V * 4 + P * w.K * 8
     topk_us = 1000.0 * statistics.mean(t_topk)
     del logits
+    # greedy chain readout (p_min cut) after the selector: the edge scores of the
+    # same step materialised once (outside timing), then an isolated loop
+    e_full = torch.empty((max(E, 1), w.K, w.K), dtype=torch.float32, device=dev)
+    _call(f_edge, edge_args[:11] + (ptr(e_full),) + edge_args[12:], L)
+    ch_tok = torch.empty((w.S_sel, w.n_sel), dtype=torch.int32, device=dev)
+    ch_pr = torch.empty((w.S_sel, w.n_sel), dtype=torch.float32, device=dev)
+    ch_len = torch.empty((w.S_sel,), dtype=torch.int32, device=dev)
+    chain_args = (ptr(d_in["cand_ids"]), ptr(d_in["unary"]), ptr(e_full), ptr(best_slot), None,
+                  w.S_sel, w.n_sel, w.K, ctypes.c_float(P_MIN), ptr(ch_tok), ptr(ch_pr),
+                  ptr(ch_len), ptr(flag), sp)
+    f_chain = L.dflash2_chain
+    if record_ext is not None:
+        t_chain = _timed_graph(K_iso, stream, flush, [(f_chain, chain_args)], record_ext, L)[0]
+    else:
+        t_chain = _timed_eager(K_iso, stream, flush, [(f_chain, chain_args)], L)[0]
+    chain_us = 1000.0 * statistics.mean(t_chain)
+    # bytes: argmax table, the n-1 chosen edge rows, the unary row, the chosen ids
+    # (one 4-byte word each) and the outputs, per sequence
+    chain_b = w.S_sel * (2 * max(w.n_sel - 1, 0) * w.K * 4 + w.K * 4 + w.n_sel * 4
+                         + w.n_sel * 8 + 4)
+    del e_full
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -603,6 +625,10 @@ def main():
             "edges": {"isolated": True, "steps": K_iso, "us": edge_us, "bytes": edge_b,
                       "GB/s": edge_b / edge_us / 1e3,
                       "frac_hbm": edge_b / edge_us / 1e3 / hbm},
+            "chain": {"isolated": True, "steps": K_iso, "us": chain_us, "bytes": chain_b,
+                      "p_min": P_MIN, "GB/s": chain_b / chain_us / 1e3,
+                      "bound": "latency (a walk of n dependent lookups per sequence)",
+                      "note": "not part of the timed step; readout after it"},
             "topk": {"isolated": True, "steps": K_iso, "us": topk_us, "bytes": topk_b,
                      "rows": P, "V": w.V, "K": w.K, "logits": "f32",
                      "GB/s": topk_b / topk_us / 1e3, "frac_hbm": topk_b / topk_us / 1e3 / hbm,

@@ -3,11 +3,12 @@
 The CUDA library (libdflash2.so, C ABI in include/dflash2.h) implements the
 grouped dynamic depthwise causal convolution, the top-K candidate extraction
 that feeds the selector, and the candidate selector (projection,
-codebook-gathered edge scores, per-predecessor argmax) of
+codebook-gathered edge scores, per-predecessor argmax) and the greedy chain
+readout with its p_min cut, of
 ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local convolution
 + candidate selector)".  This package is the thin Python binding over it.
 """
-from .binding import (Dflash2Error, dynconv, edges, lib, project,  # noqa: F401
+from .binding import (Dflash2Error, chain, dynconv, edges, lib, project,  # noqa: F401
                       project_noalloc, project_workspace_bytes, select, take_device_faults,
                       topk, version)
 from .build import build as build_library  # noqa: F401

@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
             L.dflash2_select.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp,
                                          vp, vp, vp]
             L.dflash2_select.restype = i
+            L.dflash2_chain.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, vp, vp, vp,
+                                        vp, vp]
+            L.dflash2_chain.restype = i
             L.dflash2_topk.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.dflash2_topk.restype = i
             L.dflash2_take_device_faults.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -246,6 +249,27 @@ def topk(logits, K, cand_ids=None, values=None):
     _check(lib().dflash2_topk(_ptr(logits), rows, V, K, _code(logits.dtype), _ptr(cand_ids),
                               _ptr(values), _stream(logits.device)))
     return cand_ids, values
+
+
+def chain(cand_ids, unary, edges, best_slot, p_min, start_slot=None, err_flag=None):
+    """Greedy chain readout: (tokens [S,n] int32, probs [S,n] fp32, length [S] int32).
+    cand_ids, unary [S,n,K]; edges [S,n-1,K,K] and best_slot [S,n-1,K] from
+    select(..., edges_out=True) (None when n == 1); start_slot [S] int32 or None."""
+    S, n, K = cand_ids.shape
+    _need(cand_ids, "cand_ids", torch.int32)
+    _need(unary, "unary", torch.float32)
+    _need(edges, "edges", torch.float32)
+    _need(best_slot, "best_slot", torch.int32)
+    _need(start_slot, "start_slot", torch.int32)
+    _need(err_flag, "err_flag", torch.int32)
+    dev = cand_ids.device
+    tokens = torch.empty((S, n), dtype=torch.int32, device=dev)
+    probs = torch.empty((S, n), dtype=torch.float32, device=dev)
+    length = torch.empty((S,), dtype=torch.int32, device=dev)
+    _check(lib().dflash2_chain(_ptr(cand_ids), _ptr(unary), _ptr(edges), _ptr(best_slot),
+                               _ptr(start_slot), S, n, K, float(p_min), _ptr(tokens), _ptr(probs),
+                               _ptr(length), _ptr(err_flag), _stream(dev)))
+    return tokens, probs, length
 
 
 def take_device_faults() -> int:

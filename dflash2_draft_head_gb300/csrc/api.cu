@@ -347,6 +347,43 @@ int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32
     return DF2_OK;
 }
 
+int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edges,
+                  const int32_t* best_slot, const int32_t* start_slot, int S, int n, int K,
+                  float p_min, int32_t* tokens, float* probs, int32_t* length, int32_t* err_flag,
+                  void* stream) {
+    g_err[0] = 0;
+    if (cand_ids == nullptr || unary == nullptr || tokens == nullptr || probs == nullptr ||
+        length == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "chain: NULL cand_ids, unary, tokens, probs or length");
+    if (S <= 0 || n <= 0 || K <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "chain: S=%d n=%d K=%d must be positive", S, n, K);
+    if (n > 1 && (edges == nullptr || best_slot == nullptr))
+        return fail(DF2_ERR_INVALID_ARG, "chain: NULL edges or best_slot with n > 1");
+    const size_t SnK = (size_t)S * n * K, EK = (size_t)S * (n - 1) * K;
+    const Buf ins[5] = {{cand_ids, SnK * 4, "cand_ids"},
+                        {unary, SnK * 4, "unary"},
+                        {edges, EK * K * 4, "edges"},
+                        {best_slot, EK * 4, "best_slot"},
+                        {start_slot, (size_t)S * 4, "start_slot"}};
+    const Buf outs[4] = {{tokens, (size_t)S * n * 4, "tokens"},
+                         {probs, (size_t)S * n * 4, "probs"},
+                         {length, (size_t)S * 4, "length"},
+                         {err_flag, 4, "err_flag"}};
+    int st = check_aligned(ins, 5);
+    if (st == DF2_OK) st = check_aligned(outs, 3);
+    if (st == DF2_OK && err_flag != nullptr && (reinterpret_cast<uintptr_t>(err_flag) & 3u))
+        st = fail(DF2_ERR_INVALID_ARG, "err_flag is not 4-byte aligned");
+    if (st == DF2_OK) st = check_disjoint(outs, 4, ins, 5);
+    if (st != DF2_OK) return st;
+    if (df2::chain_smem_bytes(n, K) > 200 * 1024)
+        return fail(DF2_ERR_UNSUPPORTED, "chain: argmax table of n=%d, K=%d exceeds 200 KB", n, K);
+    df2::ChainArgs a{cand_ids, unary, edges, best_slot, start_slot, S, n, K, p_min,
+                     tokens, probs, length, err_flag};
+    cudaError_t e = df2::launch_chain(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "chain launch");
+    return DF2_OK;
+}
+
 int dflash2_take_device_faults(int32_t* flags_out) {
     g_err[0] = 0;
     if (flags_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "flags_out is NULL");

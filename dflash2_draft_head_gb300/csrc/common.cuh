@@ -43,6 +43,20 @@ struct EdgesArgs {
     int32_t* err_flag;
 };
 
+struct ChainArgs {
+    const int32_t* cand_ids;
+    const float* unary;
+    const float* edges;
+    const int32_t* best_slot;
+    const int32_t* start_slot;
+    int S, n, K;
+    float p_min;
+    int32_t* tokens;
+    float* probs;
+    int32_t* length;
+    int32_t* err_flag;
+};
+
 // Largest K the top-K kernel takes.
 constexpr int kTopkMaxK = 1024;
 
@@ -80,6 +94,10 @@ bool edges_tc_supported(int K, int R);
 cudaError_t launch_edges_bf16_tc(const EdgesArgs& a, int u_only_dependency, cudaStream_t stream);
 // Warp-per-predecessor path (any K <= 256, R <= 512; fp32 or bf16 codebooks).
 cudaError_t launch_edges_warp(const EdgesArgs& a, int cb_bf16, cudaStream_t stream);
+
+// Greedy chain readout (one CTA per sequence; shared memory per CTA below).
+size_t chain_smem_bytes(int n, int K);
+cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);
 
 // Top-K candidate extraction (1 <= K <= min(V, kTopkMaxK)).
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);

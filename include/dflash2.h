@@ -220,6 +220,35 @@ int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32
                  float* values, void* stream);
 
 /*
+ * Greedy chain readout with a p_min cut: the draft tokens of each sequence,
+ * read from the selector's per-predecessor argmax table (ggml-org/llama.cpp
+ * pull request #27342: the Overview's readout is each predecessor's argmax
+ * candidate; the merged tree names the DFlash2 draft path "selector + p_min";
+ * the pages give no formula, so the readings are stated here):
+ *   slot_0 = start_slot[s] if start_slot != NULL and start_slot[s] >= 0,
+ *            else the argmax over k of unary[s,0,k] (lowest k on ties);
+ *   slot_i = best_slot[s,i-1,slot_{i-1}]              (i = 1..n-1)
+ *   p_0    = softmax_k(unary[s,0,:])[slot_0]
+ *   p_i    = softmax_c(edges[s,i-1,slot_{i-1},:])[slot_i]
+ *   tokens[s,i] = cand_ids[s,i,slot_i];  probs[s,i] = p_i (fp32)
+ *   length[s]   = number of leading positions with p_i >= p_min.
+ *   cand_ids, unary [S,n,K] (int32, fp32); edges [S,n-1,K,K] fp32 and
+ *   best_slot [S,n-1,K] int32 as written by dflash2_edges / dflash2_select
+ *   (edges_out must have been requested); both may be NULL when n == 1;
+ *   start_slot [S] int32 or NULL; tokens, probs [S,n]; length [S] int32.
+ * A slot outside [0,K) (from best_slot or start_slot) is clamped and flagged
+ * in err_flag (DF2_FLAG_BAD_ID) when err_flag is not NULL.  Non-finite scores
+ * are not supported.
+ * INVALID_ARG: S, n, K <= 0; NULL required pointer; misalignment; an output
+ * overlapping an input or another output.
+ * UNSUPPORTED: (n-1)*K*4 + 8*n bytes of argmax table above 200 KB.
+ */
+int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edges,
+                  const int32_t* best_slot, const int32_t* start_slot, int S, int n, int K,
+                  float p_min, int32_t* tokens, float* probs, int32_t* length, int32_t* err_flag,
+                  void* stream);
+
+/*
  * Reads and clears the library's device-side fault word for the current
  * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_dynconv,
  * dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from

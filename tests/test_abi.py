@@ -157,3 +157,29 @@ def test_topk_validation(L, kw, code):
     assert _topk(L, **kw) == code
     assert b"topk" in L.dflash2_last_error() or b"aligned" in L.dflash2_last_error() or \
         b"overlaps" in L.dflash2_last_error()
+
+
+def _chain(L, ci=P[0], un=P[1], ed=P[2], bs=P[3], st=None, S=2, n=4, K=8, pm=0.5, tk=P[4],
+           pr=P[5], ln=P[6], fl=None):
+    f = L.dflash2_chain
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 3 + [ctypes.c_float] + \
+        [ctypes.c_void_p] * 5
+    return f(ci, un, ed, bs, st, S, n, K, pm, tk, pr, ln, fl, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ci=NULL), 1), (dict(tk=NULL), 1), (dict(ln=NULL), 1), (dict(ed=NULL), 1),
+    (dict(bs=NULL), 1), (dict(S=0), 1), (dict(n=0), 1), (dict(K=-1), 1),
+    (dict(tk=P[0]), 1),                              # tokens alias cand_ids
+    (dict(pr=ctypes.c_void_p(0x60000004)), 1),       # misaligned
+    (dict(fl=ctypes.c_void_p(0x70000002)), 1),       # err_flag not 4-byte aligned
+    (dict(n=7000, K=8), 2),                          # argmax table above 200 KB
+])
+def test_chain_validation(L, kw, code):
+    assert _chain(L, **kw) == code
+    assert L.dflash2_last_error()
+
+
+def test_chain_single_position_needs_no_table(L):
+    # n == 1: edges and best_slot may be NULL; the call then fails only on a bad size
+    assert _chain(L, ed=NULL, bs=NULL, n=1, S=0) == 1
