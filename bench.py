@@ -519,6 +519,23 @@ def main():
     topk_b = P * w.V * 4 + P * w.K * 8
     topk_us = 1000.0 * statistics.mean(t_topk)
     del logits
+    # delta predictor (delta = x . Wc^T, the conv's taps from its input), bf16 on
+    # the tensor cores; the conv inputs of the step
+    TG = w.T * w.G
+    Wc = synth.conv_proj(w0).to(bt).to(dev)
+    d_pred = torch.empty((w.S, w.n, w.T, w.G), dtype=bt, device=dev)
+    pd_args = (ptr(d_in["x"]), ptr(Wc), ptr(d_pred), w.S * w.n, w.C, TG, code, sp)
+    f_pd = L.dflash2_predict_delta
+    _call(f_pd, pd_args, L)
+    if record_ext is not None:
+        t_pd = _timed_graph(K_iso, stream, flush, [(f_pd, pd_args)], record_ext, L)[0]
+    else:
+        t_pd = _timed_eager(K_iso, stream, flush, [(f_pd, pd_args)], L)[0]
+    pd_us = 1000.0 * statistics.mean(t_pd)
+    bsz = 2 if w.dtype == "bf16" else 4
+    pd_b = (w.S * w.n * w.C + TG * w.C + w.S * w.n * TG) * bsz
+    pd_f = 2.0 * w.S * w.n * w.C * TG
+    del Wc, d_pred
     # greedy chain readout (p_min cut) after the selector: the edge scores of the
     # same step materialised once (outside timing), then an isolated loop
     e_full = torch.empty((max(E, 1), w.K, w.K), dtype=torch.float32, device=dev)
@@ -625,6 +642,11 @@ def main():
             "edges": {"isolated": True, "steps": K_iso, "us": edge_us, "bytes": edge_b,
                       "GB/s": edge_b / edge_us / 1e3,
                       "frac_hbm": edge_b / edge_us / 1e3 / hbm},
+            "predict_delta": {"isolated": True, "steps": K_iso, "us": pd_us, "bytes": pd_b,
+                              "TFLOP/s": pd_f / pd_us / 1e6, "GB/s": pd_b / pd_us / 1e3,
+                              "frac_hbm": pd_b / pd_us / 1e3 / hbm,
+                              "frac_bf16_tc": pd_f / pd_us / 1e6 / tc,
+                              "note": "delta = x . Wc^T (C -> T*G), unfused, before the conv"},
             "chain": {"isolated": True, "steps": K_iso, "us": chain_us, "bytes": chain_b,
                       "p_min": P_MIN, "GB/s": chain_b / chain_us / 1e3,
                       "bound": "latency (a walk of n dependent lookups per sequence)",

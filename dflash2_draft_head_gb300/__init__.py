@@ -9,6 +9,6 @@ ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local convolution
 + candidate selector)".  This package is the thin Python binding over it.
 """
 from .binding import (Dflash2Error, chain, dynconv, edges, lib, project,  # noqa: F401
-                      project_noalloc, project_workspace_bytes, select, take_device_faults,
-                      topk, version)
+                      predict_delta, project_noalloc, project_workspace_bytes, select,
+                      take_device_faults, topk, version)
 from .build import build as build_library  # noqa: F401

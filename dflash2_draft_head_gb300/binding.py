@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_select.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp,
                                          vp, vp, vp]
             L.dflash2_select.restype = i
+            L.dflash2_predict_delta.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.dflash2_predict_delta.restype = i
             L.dflash2_chain.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, vp, vp, vp,
                                         vp, vp]
             L.dflash2_chain.restype = i
@@ -249,6 +251,20 @@ def topk(logits, K, cand_ids=None, values=None):
     _check(lib().dflash2_topk(_ptr(logits), rows, V, K, _code(logits.dtype), _ptr(cand_ids),
                               _ptr(values), _stream(logits.device)))
     return cand_ids, values
+
+
+def predict_delta(x, Wc, T, G, delta=None):
+    """delta [S,n,T,G] = x [S,n,C] . Wc[T*G, C]^T in x's dtype (the conv's
+    dynamic taps predicted from its input)."""
+    S, n, C = x.shape
+    _need(x, "x")
+    _need(Wc, "Wc", x.dtype)
+    if delta is None:
+        delta = torch.empty((S, n, T, G), dtype=x.dtype, device=x.device)
+    _need(delta, "delta", x.dtype)
+    _check(lib().dflash2_predict_delta(_ptr(x), _ptr(Wc), _ptr(delta), S * n, C, T * G,
+                                       _code(x.dtype), _stream(x.device)))
+    return delta
 
 
 def chain(cand_ids, unary, edges, best_slot, p_min, start_slot=None, err_flag=None):

@@ -347,6 +347,43 @@ int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32
     return DF2_OK;
 }
 
+int dflash2_predict_delta(const void* x, const void* Wc, void* delta, int P, int C, int TG,
+                          int dtype, void* stream) {
+    g_err[0] = 0;
+    if (x == nullptr || Wc == nullptr || delta == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "predict_delta: NULL x, Wc or delta");
+    if (P <= 0 || C <= 0 || TG <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "predict_delta: P=%d C=%d TG=%d must be positive", P, C,
+                    TG);
+    if (!valid_dtype(dtype)) return fail(DF2_ERR_INVALID_ARG, "predict_delta: bad dtype %d", dtype);
+    const size_t b = esize(dtype);
+    const Buf ins[2] = {{x, (size_t)P * C * b, "x"}, {Wc, (size_t)TG * C * b, "Wc"}};
+    const Buf outs[1] = {{delta, (size_t)P * TG * b, "delta"}};
+    int st = check_aligned(ins, 2);
+    if (st == DF2_OK) st = check_aligned(outs, 1);
+    if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 2);
+    if (st != DF2_OK) return st;
+    if (TG % 8 != 0 || TG > 512)
+        return fail(DF2_ERR_UNSUPPORTED, "predict_delta: T*G=%d must be a multiple of 8 and <= 512",
+                    TG);
+    if (dtype == DF2_BF16 && C % 8 != 0)
+        return fail(DF2_ERR_UNSUPPORTED, "predict_delta: bf16 needs C %% 8 == 0 (C=%d)", C);
+    if ((long long)P > 65535LL * 128)
+        return fail(DF2_ERR_UNSUPPORTED, "predict_delta: P=%d exceeds %d rows", P, 65535 * 128);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == DF2_F32) {
+        df2::ProjectArgs a{x, Wc, static_cast<float*>(delta), P, C, TG};
+        e = df2::launch_project_f32(a, s);
+    } else {
+        df2::ProjectArgs a{x, Wc, nullptr, P, C, TG};
+        a.out_bf16 = delta;
+        e = df2::launch_project_bf16_tc(a, s, num_sms_of_current_device());
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "predict_delta launch");
+    return DF2_OK;
+}
+
 int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edges,
                   const int32_t* best_slot, const int32_t* start_slot, int S, int n, int K,
                   float p_min, int32_t* tokens, float* probs, int32_t* length, int32_t* err_flag,

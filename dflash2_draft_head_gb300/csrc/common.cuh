@@ -28,6 +28,7 @@ struct ProjectArgs {
     float* u;
     int P, d, R;
     float* ws = nullptr;  // optional split-K workspace (project_workspace_bytes)
+    void* out_bf16 = nullptr;  // bf16 path only: write the output here in bf16 instead of u
 };
 
 struct EdgesArgs {

@@ -23,6 +23,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_bf16.h>
+
 #include <mutex>
 
 #include "dflash2.h"
@@ -52,6 +54,7 @@ static_assert((size_t)BM * RED_STRIDE * 4 * 2 <= (size_t)STAGES * STAGE_BYTES, "
 
 struct ProjParams {
     float* u;
+    __nv_bfloat16* ub;  // when set, the output is written here in bf16 (round to nearest even)
     int P, R;
     int kblocks;
     int splitk;
@@ -59,6 +62,20 @@ struct ProjParams {
     // reduction through distributed shared memory.
     float* ws;
 };
+
+// Stores four consecutive outputs (fp32, or bf16 when the bf16 output is set).
+__device__ __forceinline__ void store_out4(const ProjParams& p, size_t off, float4 v) {
+    if (p.ub != nullptr) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p.ub + off) = w;
+    } else {
+        *reinterpret_cast<float4*>(p.u + off) = v;
+    }
+}
 
 template <int SPLIT>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -166,9 +183,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (gcol + 4 * j < p.R)
-                        *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol + 4 * j) =
-                            make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        store_out4(p, (size_t)grow * p.R + gcol + 4 * j,
+                                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                               __uint_as_float(v[4 * j + 2]),
+                                               __uint_as_float(v[4 * j + 3])));
             }
         }
         tc_fence_before();
@@ -229,7 +247,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int grow = m_tile * BM + rr;
             const int gcol = n_tile * BN + cc;
             if (grow < p.P && gcol < p.R)
-                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
+                store_out4(p, (size_t)grow * p.R + gcol, acc);
         }
         if (warp == 1) {
             tc_fence_after();
@@ -293,7 +311,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int grow = m_tile * BM + r_base + rr;
             const int gcol = n_tile * BN + cc;
             if (grow < p.P && gcol < p.R)
-                *reinterpret_cast<float4*>(p.u + (size_t)grow * p.R + gcol) = acc;
+                store_out4(p, (size_t)grow * p.R + gcol, acc);
         }
         cluster_sync();  // the slices this CTA sent have all been received
         if (warp == 1) {
@@ -397,7 +415,7 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
     cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)SMEM_BYTES);
     if (e0 != cudaSuccess) return e0;
-    ProjParams p{a.u, a.P, a.R, kblocks, split, a.ws};
+    ProjParams p{a.u, static_cast<__nv_bfloat16*>(a.out_bf16), a.P, a.R, kblocks, split, a.ws};
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)split, (unsigned)m_tiles, (unsigned)n_tiles);
     cfg.blockDim = dim3(NTHREADS, 1, 1);

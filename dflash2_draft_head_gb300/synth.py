@@ -8,7 +8,8 @@ Distributions (normal laws written N(mean, variance)):
   x, hist, h ~ N(0, 1); base ~ N(0, 1/T); delta ~ N(0, 0.1/T);
   W ~ N(0, 1/d); A, B ~ N(0, 1/sqrt(R)); unary ~ N(0, 1);
   cand_ids: K distinct ids per position, uniform over [0, V);
-  draft logits ~ N(0, 4), one generator per row.
+  draft logits ~ N(0, 4), one generator per row;
+  conv_proj Wc [T*G, C] ~ N(0, 0.1/(T*C)) (so the predicted delta has delta's spread).
 bf16 workloads draw fp32 and round once to bf16 (round-to-nearest-even); the
 returned fp32 arrays hold those exact bf16 values.
 
@@ -26,7 +27,7 @@ CHUNK = 4096
 
 _TAG = {"x": 1, "hist": 2, "base": 3, "delta": 4, "h": 5, "W": 6, "A": 7, "B": 8,
         "unary": 9, "cand": 10, "cand_fix": 11,
-        "logits": 12}
+        "logits": 12, "conv_proj": 13}
 
 
 def _gen(seed: int, *key: int) -> torch.Generator:
@@ -156,3 +157,9 @@ def logits_rows(seed: int, lo: int, hi: int, V: int, dtype: str, std: float = 2.
         g = _gen(seed, _TAG["logits"], r, 0)
         out[r - lo] = torch.randn((V,), generator=g, dtype=torch.float32) * std
     return to_storage(out, dtype)
+
+
+def conv_proj(w) -> torch.Tensor:
+    """Wc [T*G, C] of the delta predictor (fp32 tensor holding storage-dtype values)."""
+    return normal_whole(w.seed, "conv_proj", (w.T * w.G, w.C), math.sqrt(0.1 / (w.T * w.C)),
+                        w.dtype)

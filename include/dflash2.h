@@ -220,6 +220,21 @@ int dflash2_topk(const void* logits, int rows, int V, int K, int in_dtype, int32
                  float* values, void* stream);
 
 /*
+ * The convolution's dynamic taps predicted from its input (the pull request's
+ * "predicted from the input" delta, tensor "*_conv_proj"; the pages give no
+ * formula, so the reading is stated here): for every position p,
+ *   delta[p, t*G + g] = sum_c Wc[t*G + g, c] * x[p, c]
+ * i.e. delta [P, T*G] = x [P, C] . Wc [T*G, C]^T, written in `dtype` (bf16:
+ * fp32 accumulation on the tensor cores, rounded to nearest even; fp32: fp32
+ * throughout).  With P = S*n the output is the [S,n,T,G] delta that
+ * dflash2_dynconv takes; this call is the unfused first half of that pair.
+ * INVALID_ARG: P, C, TG <= 0; NULL pointer; misalignment; delta overlapping x
+ * or Wc.  UNSUPPORTED: TG % 8 != 0 or TG > 512; bf16 with C % 8 != 0.
+ */
+int dflash2_predict_delta(const void* x, const void* Wc, void* delta, int P, int C, int TG,
+                          int dtype, void* stream);
+
+/*
  * Greedy chain readout with a p_min cut: the draft tokens of each sequence,
  * read from the selector's per-predecessor argmax table (ggml-org/llama.cpp
  * pull request #27342: the Overview's readout is each predecessor's argmax

@@ -183,3 +183,16 @@ def test_chain_validation(L, kw, code):
 def test_chain_single_position_needs_no_table(L):
     # n == 1: edges and best_slot may be NULL; the call then fails only on a bad size
     assert _chain(L, ed=NULL, bs=NULL, n=1, S=0) == 1
+
+
+def _pdelta(L, x=P[0], wc=P[1], de=P[2], Pn=64, C=128, TG=16, dt=1):
+    return L.dflash2_predict_delta(x, wc, de, Pn, C, TG, dt, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=NULL), 1), (dict(de=NULL), 1), (dict(Pn=0), 1), (dict(C=-1), 1), (dict(TG=0), 1),
+    (dict(dt=5), 1), (dict(de=P[0]), 1), (dict(wc=ctypes.c_void_p(0x20000002)), 1),
+    (dict(TG=12), 2), (dict(TG=520), 2), (dict(C=100), 2),
+])
+def test_predict_delta_validation(L, kw, code):
+    assert _pdelta(L, **kw) == code
