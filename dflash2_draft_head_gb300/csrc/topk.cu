@@ -689,6 +689,7 @@ struct ACtl {
     uint32_t sel_done;          // rows the selector has finished
     uint32_t out_cnt[2];
     uint32_t abort;
+    uint32_t fin_go, fin_s, fin_cur;  // hand-off of a short row's final selection
 };
 static_assert(sizeof(ACtl) <= 512, "control block");
 
@@ -926,6 +927,50 @@ __device__ __forceinline__ int count_greater32(const uint64_t* l, uint64_t k) {
     return pos + (l[pos] > k ? 1 : 0);
 }
 
+// Whether every filter warp has published the end of row iteration rit.
+__device__ __forceinline__ bool all_rows_ended(ACtl* c, int slot, int rit) {
+    bool all = true;
+#pragma unroll
+    for (int w = 0; w < kNF; ++w)
+        all = all && ld_acquire_u32(&c->rowtag[w][slot]) == (uint32_t)(rit + 1);
+    return all;
+}
+
+// Final selection of a short row by the filter warps and the selector together
+// (threads t = 0..kNC+31): the K best of the selector's sorted list L[0, s) and
+// every queue's unconsumed range [qtail, rowend), each key ranked by counting
+// the larger keys among all of them (keys are distinct), written in rank order.
+__device__ void coop_rank(ACtl* c, int slot, const uint64_t* L, int s, const uint64_t* queues,
+                          int K, uint64_t* Lout, int t, int nthreads) {
+    uint32_t len[kNF + 1], q0[kNF];
+    len[0] = (uint32_t)s;
+    uint32_t M = (uint32_t)s;
+#pragma unroll
+    for (int w = 0; w < kNF; ++w) {
+        q0[w] = c->qtail[w];
+        len[w + 1] = c->rowend[w][slot] - q0[w];
+        M += len[w + 1];
+    }
+    for (uint32_t j = (uint32_t)t; j < M; j += (uint32_t)nthreads) {
+        uint32_t off = j;
+        int seg = 0;
+        while (off >= len[seg]) {
+            off -= len[seg];
+            ++seg;
+        }
+        const uint64_t k = seg == 0 ? L[off]
+                                    : queues[(size_t)(seg - 1) * kQW + ((q0[seg - 1] + off) & (kQW - 1))];
+        int r = 0;
+        for (int i = 0; i < s; ++i) r += L[i] > k ? 1 : 0;
+#pragma unroll 1
+        for (int w = 0; w < kNF; ++w) {
+            const uint64_t* q = queues + (size_t)w * kQW;
+            for (uint32_t i = 0; i < len[w + 1]; ++i) r += q[(q0[w] + i) & (kQW - 1)] > k ? 1 : 0;
+        }
+        if (r < K) Lout[r] = k;
+    }
+}
+
 // Writes one output row from the sorted list (selector warp).
 template <bool BF16>
 __device__ void write_sorted(const uint64_t* L, int n, const TopkParams& p, int row) {
@@ -1008,6 +1053,11 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
     const int e1 = min(p.V, e0 + L_);
     const uintptr_t lbase = reinterpret_cast<uintptr_t>(p.logits);
     const int warp = tid >> 5;
+    // With at most two rows per cluster (latency, not throughput, decides) each
+    // row ends with a joint final selection: the selector stops draining once
+    // every filter warp has finished the row, and all 288 threads rank what is
+    // left (see coop_rank).  With more rows the filter warps run ahead instead.
+    const bool shortrow = (p.rows + ncl - 1) / ncl <= 2;
 
     if (warp == kNF + 1) {
         // ---------------- producer (one lane), as in the general kernel
@@ -1053,12 +1103,17 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             uint64_t t_idle = 0;
             uint32_t nap = 32u;  // idle back-off (ns)
             int nst = 0;  // keys staged in Bs[0, nst) for the next merge
+            bool exited_early = false;
             if (p.K <= 32) {
                 // The list lives in registers, lane i holding L[i]: an insertion
                 // is one ballot (its place) and one shuffle (the shift), so the
                 // threshold can follow every key.
                 uint64_t Lr = 0ull, kth = 0ull;  // kth: L[K-1] once the list is full
                 while (done != (1u << kNF) - 1u) {
+                    if (shortrow && all_rows_ended(c, slot, rit)) {
+                        exited_early = true;
+                        break;
+                    }
                     bool prog = false;
 #pragma unroll
                     for (int w = 0; w < kNF; ++w) {
@@ -1069,6 +1124,10 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                         const uint32_t lim = ended ? c->rowend[w][slot] : qh;
                         const uint64_t* q = queues + (size_t)w * kQW;
                         while (qt[w] != lim && !*abort_flag) {
+                            if (shortrow && all_rows_ended(c, slot, rit)) {
+                                exited_early = true;
+                                break;
+                            }
                             const uint32_t nb = min(32u, lim - qt[w]);
                             const uint64_t k =
                                 (uint32_t)lane < nb ? q[(qt[w] + lane) & (kQW - 1)] : 0ull;
@@ -1105,9 +1164,11 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                                 if (cs > 1) share_bound(&c->cbound[slot], cs, rit, pub);
                             }
                         }
+                        if (exited_early) break;
                         if (ended && qt[w] == lim) done |= 1u << w;
                         if (*abort_flag) done |= 1u << w;
                     }
+                    if (exited_early) break;
                     if (prog) {
                         t_idle = 0;
                         nap = 32u;
@@ -1121,7 +1182,41 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 }
                 if (lane < s) L[lane] = Lr;
             }
-            while (done != (1u << kNF) - 1u) {
+            for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                if (!shortrow) break;
+                // Short row: hand the rest to the whole CTA (when it is small)
+                uint32_t M = (uint32_t)s;
+#pragma unroll
+                for (int w = 0; w < kNF; ++w) M += c->rowend[w][slot] - qt[w];
+                const bool go = exited_early && !*abort_flag && M <= 1024u;
+                if (lane == 0) {
+                    c->fin_go = go ? 1u : 0u;
+                    c->fin_s = (uint32_t)s;
+                    c->fin_cur = (uint32_t)cur;
+                }
+                __syncwarp();
+                named_bar_sync(2, kNC + 32);
+                if (go) coop_rank(c, slot, L, s, queues, p.K, Lbuf + (cur ^ 1) * kAsyncMaxK,
+                                  tid, kNC + 32);
+                named_bar_sync(2, kNC + 32);
+                if (go) {
+                    s = (int)min(M, (uint32_t)p.K);
+                    cur ^= 1;
+                    L = Lbuf + cur * kAsyncMaxK;
+#pragma unroll
+                    for (int w = 0; w < kNF; ++w) qt[w] = c->rowend[w][slot];
+                    if (lane < kNF) st_release_u32(&c->qtail[lane], c->rowend[lane][slot]);
+                    done = (1u << kNF) - 1u;
+                }
+                if (go || !exited_early) break;
+                exited_early = false;  // too much left: drain it here after all
+            }
+            while (!exited_early && done != (1u << kNF) - 1u) {
+                if (pass == 0 && shortrow && all_rows_ended(c, slot, rit)) {
+                    exited_early = true;
+                    break;
+                }
                 bool prog = false;
 #pragma unroll
                 for (int w = 0; w < kNF; ++w) {
@@ -1133,6 +1228,10 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     const uint32_t lim = ended ? c->rowend[w][slot] : qh;
                     const uint64_t* q = queues + (size_t)w * kQW;
                     while (qt[w] != lim && !*abort_flag) {
+                        if (pass == 0 && shortrow && all_rows_ended(c, slot, rit)) {
+                            exited_early = true;
+                            break;
+                        }
                         // stage the keys that beat the list's K-th (32 at most)
                         const uint32_t nb = min((uint32_t)(32 - nst), lim - qt[w]);
                         const uint64_t k = (uint32_t)lane < nb ? q[(qt[w] + lane) & (kQW - 1)] : 0ull;
@@ -1195,6 +1294,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     nap = min(2u * nap, 512u);
                 }
             }
+            }
             __syncwarp();
             if (cs == 1) {
                 write_sorted<BF16>(L, s, p, row);
@@ -1216,20 +1316,45 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     if (!*abort_flag &&
                         !mbar_wait_cluster_bounded(smem_u32(&c->mfull[slot]), par, kWaitNs))
                         set_abort(abort_flag);
-                    // the cs sorted lists side by side, K apart: list 0 is ours
-                    int cnt[8];
-                    cnt[0] = s;
+                    // the cs sorted lists side by side, K apart: list 0 is ours.  The
+                    // counts come in one parallel round of remote loads (lane r reads
+                    // rank r's), the keys in batches of 8 loads per lane before any store.
+                    const uint32_t myc =
+                        (lane >= 1 && lane < cs)
+                            ? min(ld_cluster_u32(map_cluster(smem_u32(&c->out_cnt[slot]),
+                                                             (uint32_t)lane)),
+                                  (uint32_t)p.K)
+                            : 0u;
                     for (int i = lane; i < s; i += 32) merge[i] = L[i];
+                    int cnt[8];  // every lane holds every rank's count (shuffled, no divergence)
+                    cnt[0] = s;
+                    int tot_remote = 0;
+#pragma unroll
                     for (int r = 1; r < 8; ++r) {
-                        cnt[r] = 0;
-                        if (r >= cs) continue;
-                        cnt[r] = (int)min(ld_cluster_u32(map_cluster(smem_u32(&c->out_cnt[slot]),
-                                                                     (uint32_t)r)),
-                                          (uint32_t)p.K);
-                        const uint32_t src = map_cluster(
-                            smem_u32(outk + (size_t)slot * kAsyncMaxK), (uint32_t)r);
-                        for (int i = lane; i < cnt[r]; i += 32)
-                            merge[r * kAsyncMaxK + i] = ld_cluster_u64(src + 8u * i);
+                        cnt[r] = (int)__shfl_sync(0xffffffffu, myc, r);
+                        tot_remote += cnt[r];
+                    }
+                    for (int j0 = 0; j0 < tot_remote; j0 += 32 * 8) {
+                        uint64_t v[8];
+                        int dst[8];
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            int j = j0 + 32 * m + lane;
+                            dst[m] = -1;
+                            if (j < tot_remote) {
+                                int r = 1;
+                                while (r < 7 && j >= cnt[r]) {  // the rank whose list holds j
+                                    j -= cnt[r];
+                                    ++r;
+                                }
+                                dst[m] = r * kAsyncMaxK + j;
+                                v[m] = ld_cluster_u64(map_cluster(
+                                    smem_u32(outk + (size_t)slot * kAsyncMaxK + j), (uint32_t)r));
+                            }
+                        }
+#pragma unroll
+                        for (int m = 0; m < 8; ++m)
+                            if (dst[m] >= 0) merge[dst[m]] = v[m];
                     }
                     __syncwarp();
                     if (lane == 0) {
@@ -1412,6 +1537,13 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
         if (lane == 0) {
             c->rowend[warp][slot] = qh;
             st_release_u32(&c->rowtag[warp][slot], (uint32_t)(rit + 1));
+        }
+        if (shortrow) {
+            named_bar_sync(2, kNC + 32);
+            if (c->fin_go)
+                coop_rank(c, slot, Lbuf + c->fin_cur * kAsyncMaxK, (int)c->fin_s, queues, p.K,
+                          Lbuf + (c->fin_cur ^ 1) * kAsyncMaxK, tid, kNC + 32);
+            named_bar_sync(2, kNC + 32);
         }
     }
     // On an abandoned pipeline, give copies still in flight a bounded time to
