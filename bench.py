@@ -48,8 +48,8 @@ TRAFFIC = {
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
     ("batched_256x16_d5120", "topk"): {
-        "sha": "9a55b3583121964ddebdf496a7fbb8d5aa75eeea8fe6cee46801ab39210312e7",
-        "bytes": 8 * (311319040 + 3629312),
+        "sha": "73b56af7e4dc2138148354799a034bcb6041b381c0af898d6f88ac410598f996",
+        "bytes": 8 * (311424512 + 3649536),
     },
 }
 
