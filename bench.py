@@ -312,6 +312,25 @@ class L2Flush:
         self.w.zero_()
         torch.sum(self.r, dim=0, out=self.sink)
 
+class _NoFlush:
+    """Stands in for the L2 flush where a warm-cache variant is timed."""
+
+    def zero_(self):
+        pass
+
+
+def _input_digests(tensors):
+    """SHA-256 of every host input tensor's bytes (storage dtype), for reproducibility."""
+    import torch
+    out = {}
+    for k, v in tensors.items():
+        t = v.contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)  # numpy has no bf16: hash the raw 16-bit words
+        out[k] = hashlib.sha256(t.numpy().tobytes()).hexdigest()
+    return out
+
+
 def _event_record_external():
     """cudaEventRecordWithFlags(..., cudaEventRecordExternal) of the CUDA runtime torch
     loaded (timing events inside a captured graph), or None."""
@@ -500,8 +519,12 @@ def main():
     iso_calls = [(f_proj, proj_args), (f_edge, edge_args)]
     if record_ext is not None:
         t_proj, t_edge = _timed_graph(K_iso, stream, flush, iso_calls, record_ext, L)
+        # the projection again with h left in L2 ("warm": no flush between launches)
+        t_proj_warm = _timed_graph(K_iso, stream, _NoFlush(), [(f_proj, proj_args)], record_ext,
+                                   L)[0]
     else:
         t_proj, t_edge = _timed_eager(K_iso, stream, flush, iso_calls, L)
+        t_proj_warm = _timed_eager(K_iso, stream, _NoFlush(), [(f_proj, proj_args)], L)[0]
     # top-K candidate extraction, the step before the selector, on the draft
     # logits of the same positions: [P, V] fp32 rows (the review thread's
     # top-k microbenchmark runs fp32 rows); also an isolated loop
@@ -568,22 +591,59 @@ def main():
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = h_slot.numel() * 4 + h_score.numel() * 4
 
-    def e2e_step():
-        for k2, v in pin.items():
-            d_in[k2].copy_(v, non_blocking=True)
-        step()
+    # Two device input sets: step k+1's host->device copies (two copy streams, the
+    # tensors split between them) overlap step k's kernels; every step still copies
+    # its inputs in and its readout out inside the timed region.
+    d_in2 = {k2: torch.empty_like(v) for k2, v in d_in.items()}
+    sets = [d_in, d_in2]
+
+    def step_args(di):
+        ca = (ptr(di["x"]), ptr(di["hist"]), ptr(base), ptr(di["delta"]), ptr(out),
+              w.S, w.n, w.C, w.T, w.G, code, code, sp)
+        sa = (ptr(di["h"]), ptr(Wt), ptr(di["cand_ids"]), ptr(A), ptr(B), ptr(di["unary"]),
+              w.S_sel, w.n_sel, w.d, w.K, w.R, w.V, code, ptr(u), None, ptr(best_slot),
+              ptr(best_score), ptr(flag), sp)
+        return ca, sa
+
+    args2 = [step_args(di) for di in sets]
+    copy_streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    names = sorted(pin, key=lambda k2: -pin[k2].numel() * pin[k2].element_size())
+    split = [names[0::2], names[1::2]]  # largest tensors alternate between the streams
+    ready = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]  # [set][copy stream]
+    free = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def e2e_step(k):
+        b = k % 2
+        for j, cst in enumerate(copy_streams):
+            if used[b]:
+                cst.wait_event(free[b])  # the kernels that read this set are done
+            with torch.cuda.stream(cst):
+                for k2 in split[j]:
+                    sets[b][k2].copy_(pin[k2], non_blocking=True)
+            ready[b][j].record(cst)
+        for j in range(2):
+            stream.wait_event(ready[b][j])
+        ca, sa = args2[b]
+        r = f_conv(*ca) | f_sel(*sa)
+        if r:
+            raise RuntimeError(L.dflash2_last_error().decode())
+        free[b].record(stream)
+        used[b] = True
         h_slot.copy_(best_slot, non_blocking=True)
         h_score.copy_(best_score, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
+    for k in range(3):
+        e2e_step(k)
     barrier()
     E2 = max(args.e2e_steps, 1)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(E2):
-        e2e_step()
+    for cst in copy_streams:
+        cst.wait_event(e0)  # no copy of the timed steps starts before the start event
+    for k in range(E2):
+        e2e_step(k)
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
@@ -629,12 +689,14 @@ def main():
         },
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
-                        "frac_hbm": conv_b / conv_us / 1e3 / hbm},
+                        "frac_hbm": conv_b / conv_us / 1e3 / hbm,
+                        "positions_per_s": positions / (conv_us * 1e-6)},
             "select": {"us": sel_us, "bytes": proj_b + edge_b,
                        "GB/s": (proj_b + edge_b) / sel_us / 1e3,
                        "frac_hbm": (proj_b + edge_b) / sel_us / 1e3 / hbm,
                        "note": "project + edges in one dflash2_select call (timed region)"},
             "project": {"isolated": True, "steps": K_iso, "us": proj_us, "bytes": proj_b,
+                        "warm_us": 1000.0 * statistics.mean(t_proj_warm),
                         "GB/s": proj_b / proj_us / 1e3,
                         "TFLOP/s": proj_f / proj_us / 1e6,
                         "frac_hbm": proj_b / proj_us / 1e3 / hbm,
@@ -657,9 +719,13 @@ def main():
                      "note": "not part of the timed step; candidate extraction before it"},
         },
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2,
+                "pipelining": "double-buffered inputs: step k+1's H2D copies (2 streams) overlap "
+                              "step k's kernels"},
         "gpu_launches": 3 * K,  # dynconv + project + edges per timed step
         "clocks": clk.summary(),
+        "torch": torch.__version__,
+        "inputs_sha256": _input_digests(host_in),
         "wall_s_timed_region": wall,
         "launch_mode": mode,
         "cpu_baseline": None,
