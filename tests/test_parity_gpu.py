@@ -160,6 +160,9 @@ def test_project_workloads(name):
     dict(S=4, n=64, d=1032, R=136),        # two N tiles, ragged
     dict(S=2, n=100, d=5120, R=512),       # maximum R
     dict(S=64, n=40, d=5120, R=128),       # 20 M tiles
+    dict(S=4, n=64, d=1032, R=160),        # two N tiles (the delta predictor's T*G), split-K
+    dict(S=64, n=64, d=5120, R=160),       # two N tiles, 32 M tiles
+    dict(S=1, n=16, d=5120, R=152),        # two N tiles, ragged R, one M tile
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_project_edge_shapes(kw, dtype):
@@ -193,6 +196,9 @@ def test_project_ws_workloads(name):
     dict(S=4, n=64, d=1032, R=136),
     dict(S=2, n=100, d=5120, R=512),
     dict(S=64, n=40, d=5120, R=128),
+    dict(S=4, n=64, d=1032, R=160),
+    dict(S=64, n=64, d=5120, R=160),
+    dict(S=1, n=16, d=5120, R=152),
 ])
 def test_project_ws_edge_shapes(kw):
     check_project_ws(W_(C=64, G=4, **kw))

@@ -46,6 +46,7 @@ def _call(fn, h, W, u):
 
 
 @pytest.mark.parametrize("P,d,R", [(16, 5120, 128),     # one draft block: split-K 8
+                                   (16, 5120, 160),     # two N tiles: split-K 8
                                    (512, 5376, 256),    # wide selector
                                    (4096, 5120, 128)])  # batched: 8 MiB of workspace
 def test_noalloc_matches_project_twice(L, P, d, R):
