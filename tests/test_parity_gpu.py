@@ -80,6 +80,16 @@ def test_dynconv_edge_shapes(kw, dtype):
     check_dynconv(W_(dtype=dtype, **kw))
 
 
+@pytest.mark.parametrize("kw,hist", [
+    (dict(S=100, n=13, C=5120, T=4, G=40), True),   # more tiles than resident CTAs, ragged
+    (dict(S=77, n=21, C=5120, T=5, G=40), False),   # ragged tiles, no history
+    (dict(S=256, n=16, C=5120, T=2, G=40), True),   # T = 2
+])
+def test_dynconv_many_tiles(kw, hist):
+    """Shapes with more (sequence, tile) items than resident CTAs (bf16 pipelined path)."""
+    check_dynconv(W_(dtype="bf16", **kw), with_hist=hist)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T", [4, 8])
 def test_dynconv_null_history(dtype, T):
