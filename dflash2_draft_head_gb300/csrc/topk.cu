@@ -7,27 +7,29 @@
 // selector consumes the top K candidates of vocabulary-wide rows (a few 1e5
 // entries) with small K, swept there up to K = 1024.
 //
-// The work is one read of every logit, so the design keeps the per-element
-// cost at a load from shared memory and one comparison:
+// The work is one read of every logit, so both kernels keep the per-element
+// cost at a load from shared memory and one comparison, and share:
 //  - persistent CTAs, one per SM; rows are dealt out to clusters of cs CTAs,
 //    each CTA of a cluster taking one contiguous chunk of the row (cs = 1 when
 //    there are enough rows to fill the GPU);
-//  - one producer lane streams the chunk's 16-byte-aligned body through a ring
-//    of six 16 KB stages with cp.async.bulk (mbarrier completion); the
+//  - one producer lane streaming the chunk's 16-byte-aligned body through a
+//    ring of six 16 KB stages with cp.async.bulk (mbarrier completion); the
 //    unaligned head and tail (under 16 bytes each) are read directly;
-//  - 256 consumer threads compare each element with a threshold tau and
-//    append the survivors to a candidate buffer as 64-bit keys (order-
-//    preserving value bits, then the complemented index: a larger key is a
-//    better candidate and no two keys are equal), one shared atomic per warp;
-//  - when the buffer passes a trigger, an exact radix select (8-bit digits,
-//    most significant first) finds the K-th largest key, the buffer keeps the
-//    K best and tau becomes the K-th value.  Elements tested later have larger
-//    indices, so one equal to tau can never displace the K-th candidate: the
-//    strict test x > tau loses nothing;
-//  - at the end of a row the other CTAs of the cluster hand their K best to
-//    rank 0 through distributed shared memory (double-buffered, mbarrier
-//    hand-shake); rank 0 keeps the K best of the union, orders them by
-//    counting and writes ids and values (the values re-read from the logits).
+//  - candidates as 64-bit keys: order-preserving value bits above the
+//    complemented index, so a larger key is a better candidate and no two
+//    keys are equal;
+//  - a cluster merge at the end of a row: the other CTAs hand their K best to
+//    rank 0 through distributed shared memory (double-buffered mbarrier
+//    hand-shake), and rank 0 writes ids and values in rank order.
+// topk_async_kernel (K <= 256): eight filter warps test whole stages against
+// a threshold key and push survivors into per-warp queues, never waiting for
+// one another; a selector warp keeps the exact sorted top-K and raises the
+// published threshold (see the section header further down).
+// topk_kernel (K <= 1024): 256 consumer threads append survivors to one shared
+// candidate buffer and, at stage boundaries, re-select together (rank counting
+// or an 8-bit-digit radix select) and tighten the threshold to the K-th value;
+// elements tested later have larger indices, so the strict test x > tau is
+// exact there.
 // NaN entries never pass a test; rows with fewer than K other entries get
 // id -1 and value NaN in the remaining slots.
 #include <cuda_runtime.h>
