@@ -63,6 +63,8 @@ def _args():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="oracle time the reference arm spreads over warm-up and timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     return ap.parse_args()
@@ -213,7 +215,7 @@ def run_reference(args):
     t0 = time.perf_counter()
     pool.run(0)
     t_unit = max(time.perf_counter() - t0, 1e-4)
-    total_budget = 120.0
+    total_budget = max(float(args.ref_seconds), 0.0)
     units_per_step = max(1, int(total_budget / max(args.steps + args.warmup, 1) / t_unit))
     for k in range(args.warmup):
         for j in range(units_per_step):
