@@ -560,6 +560,34 @@ def main():
     bsz = 2 if w.dtype == "bf16" else 4
     pd_b = (w.S * w.n * w.C + TG * w.C + w.S * w.n * TG) * bsz
     pd_f = 2.0 * w.S * w.n * w.C * TG
+    # the conv with its taps predicted inside the kernel (delta never leaves the
+    # chip, x read from HBM once), against the unfused pair it replaces: predict,
+    # then convolve the stored delta, on the same inputs and output buffer
+    fz = None
+    if w.dtype == "bf16" and TG <= 256 and TG % 8 == 0 and w.T <= 8:
+        f_fz = L.dflash2_dynconv_predicted
+        fz_args = (ptr(d_in["x"]), ptr(d_in["hist"]), ptr(base), ptr(Wc), ptr(out), w.S, w.n,
+                   w.C, w.T, w.G, code, code, sp)
+        pair_conv = (ptr(d_in["x"]), ptr(d_in["hist"]), ptr(base), ptr(d_pred), ptr(out), w.S,
+                     w.n, w.C, w.T, w.G, code, code, sp)
+        _call(f_fz, fz_args, L)
+        if record_ext is not None:
+            t_fz = _timed_graph(K_iso, stream, flush, [(f_fz, fz_args)], record_ext, L)[0]
+            t_pair = _timed_graph(K_iso, stream, flush, [(f_pd, pd_args), (f_conv, pair_conv)],
+                                  record_ext, L)
+        else:
+            t_fz = _timed_eager(K_iso, stream, flush, [(f_fz, fz_args)], L)[0]
+            t_pair = _timed_eager(K_iso, stream, flush, [(f_pd, pd_args), (f_conv, pair_conv)], L)
+        fz_us = 1000.0 * statistics.mean(t_fz)
+        pair_us = 1000.0 * statistics.mean(a + b for a, b in zip(t_pair[0], t_pair[1]))
+        # algorithmic bytes: x, history, base taps and Wc read once, out written once
+        fz_b = (2 * w.S * w.n * w.C + w.S * (w.T - 1) * w.C + w.T * w.C + TG * w.C) * bsz
+        fz = {"isolated": True, "steps": K_iso, "us": fz_us, "bytes": fz_b,
+              "GB/s": fz_b / fz_us / 1e3, "frac_hbm": fz_b / fz_us / 1e3 / _peaks()[0],
+              "TFLOP/s": pd_f / fz_us / 1e6, "unfused_pair_us": pair_us,
+              "speedup_vs_pair": pair_us / fz_us,
+              "note": "delta = x . Wc^T and the conv in one kernel; not part of the timed step "
+                      "(its conv takes delta as an input)"}
     del Wc, d_pred
     # greedy chain readout (p_min cut) after the selector: the edge scores of the
     # same step materialised once (outside timing), then an isolated loop
@@ -711,6 +739,7 @@ def main():
                               "frac_hbm": pd_b / pd_us / 1e3 / hbm,
                               "frac_bf16_tc": pd_f / pd_us / 1e6 / tc,
                               "note": "delta = x . Wc^T (C -> T*G), unfused, before the conv"},
+            "dynconv_predicted": fz,
             "chain": {"isolated": True, "steps": K_iso, "us": chain_us, "bytes": chain_b,
                       "p_min": P_MIN, "GB/s": chain_b / chain_us / 1e3,
                       "bound": "latency (a walk of n dependent lookups per sequence)",

@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_select.restype = i
             L.dflash2_predict_delta.argtypes = [vp, vp, vp, i, i, i, i, vp]
             L.dflash2_predict_delta.restype = i
+            L.dflash2_dynconv_predicted.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+            L.dflash2_dynconv_predicted.restype = i
             L.dflash2_chain.argtypes = [vp, vp, vp, vp, vp, i, i, i, ctypes.c_float, vp, vp, vp,
                                         vp, vp]
             L.dflash2_chain.restype = i
@@ -265,6 +267,23 @@ def predict_delta(x, Wc, T, G, delta=None):
     _check(lib().dflash2_predict_delta(_ptr(x), _ptr(Wc), _ptr(delta), S * n, C, T * G,
                                        _code(x.dtype), _stream(x.device)))
     return delta
+
+
+def dynconv_predicted(x, hist, base, Wc, G, out=None, out_dtype=None):
+    """The conv with its taps predicted from its input, fused: x [S,n,C], hist
+    [S,T-1,C] or None, base [T,C], Wc [T*G,C] (bf16) -> out [S,n,C]; the same as
+    dynconv(x, hist, base, predict_delta(x, Wc, T, G)) without delta in HBM."""
+    S, n, C = x.shape
+    T = base.shape[0]
+    for t, nm in ((x, "x"), (hist, "hist"), (base, "base"), (Wc, "Wc")):
+        _need(t, nm, x.dtype)
+    if out is None:
+        out = torch.empty((S, n, C), dtype=out_dtype or x.dtype, device=x.device)
+    _need(out, "out")
+    _check(lib().dflash2_dynconv_predicted(_ptr(x), _ptr(hist), _ptr(base), _ptr(Wc), _ptr(out),
+                                           S, n, C, T, G, _code(x.dtype), _code(out.dtype),
+                                           _stream(x.device)))
+    return out
 
 
 def chain(cand_ids, unary, edges, best_slot, p_min, start_slot=None, err_flag=None):

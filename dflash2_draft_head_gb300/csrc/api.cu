@@ -72,6 +72,17 @@ int num_sms_of_current_device() {
     return sms;
 }
 
+size_t max_smem_optin_of_current_device() {
+    static int cached[64] = {0};
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 227 * 1024;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return (size_t)cached[dev];
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 227 * 1024;
+    if (dev >= 0 && dev < 64) cached[dev] = v;
+    return (size_t)v;
+}
+
 int validate_project(const void* h, const void* W, const float* u, int P, int d, int R,
                      int dtype) {
     if (h == nullptr || W == nullptr || u == nullptr)
@@ -165,7 +176,7 @@ int run_project(const void* h, const void* W, float* u, int P, int d, int R, int
 
 extern "C" {
 
-int dflash2_version(void) { return 100; }
+int dflash2_version(void) { return 200; }
 
 const char* dflash2_status_string(int status) {
     switch (status) {
@@ -384,6 +395,51 @@ int dflash2_predict_delta(const void* x, const void* Wc, void* delta, int P, int
     return DF2_OK;
 }
 
+int dflash2_dynconv_predicted(const void* x, const void* hist, const void* base, const void* Wc,
+                              void* out, int S, int n, int C, int T, int G, int in_dtype,
+                              int out_dtype, void* stream) {
+    g_err[0] = 0;
+    if (x == nullptr || base == nullptr || Wc == nullptr || out == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "dynconv_predicted: NULL x, base, Wc or out");
+    if (S <= 0 || n <= 0 || C <= 0 || T <= 0 || G <= 0)
+        return fail(DF2_ERR_INVALID_ARG,
+                    "dynconv_predicted: S=%d n=%d C=%d T=%d G=%d must be positive", S, n, C, T, G);
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+        return fail(DF2_ERR_INVALID_ARG, "dynconv_predicted: bad dtype");
+    if (C % G != 0)
+        return fail(DF2_ERR_INVALID_ARG, "dynconv_predicted: C=%d not a multiple of G=%d", C, G);
+    const size_t bi = esize(in_dtype), bo = esize(out_dtype);
+    const Buf ins[4] = {{x, (size_t)S * n * C * bi, "x"},
+                        {hist, (size_t)S * (T - 1) * C * bi, "hist"},
+                        {base, (size_t)T * C * bi, "base"},
+                        {Wc, (size_t)T * G * C * bi, "Wc"}};
+    const Buf outs[1] = {{out, (size_t)S * n * C * bo, "out"}};
+    int st = check_aligned(ins, 4);
+    if (st == DF2_OK) st = check_aligned(outs, 1);
+    if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 4);
+    if (st != DF2_OK) return st;
+    if (in_dtype != DF2_BF16)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: needs bf16 input");
+    if (T > df2::kMaxPredT)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: T=%d > %d", T, df2::kMaxPredT);
+    const long long TG = (long long)T * G;
+    if (C % 8 != 0 || (C / G) % 8 != 0 || TG % 8 != 0 || TG > 256)
+        return fail(DF2_ERR_UNSUPPORTED,
+                    "dynconv_predicted: needs C %% 8 == 0, (C/G) %% 8 == 0, (T*G) %% 8 == 0 and "
+                    "T*G <= 256 (C=%d T=%d G=%d)", C, T, G);
+    if ((long long)S * n > 0x7FFFFFFFLL)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: S*n above 2^31-1");
+    df2::DynconvPredArgs a{x, T > 1 ? hist : nullptr, base, Wc, out, S, n, C, T, G,
+                           out_dtype == DF2_BF16};
+    df2::DynconvPredPlan plan{};
+    if (!df2::plan_dynconv_pred(a, num_sms_of_current_device(), max_smem_optin_of_current_device(),
+                                &plan))
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: shapes do not fit shared memory");
+    cudaError_t e = df2::launch_dynconv_pred(a, plan, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dynconv_predicted launch");
+    return DF2_OK;
+}
+
 int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edges,
                   const int32_t* best_slot, const int32_t* start_slot, int S, int n, int K,
                   float p_min, int32_t* tokens, float* probs, int32_t* length, int32_t* err_flag,
@@ -431,6 +487,8 @@ int dflash2_take_device_faults(int32_t* flags_out) {
     if (e == cudaSuccess) e = df2::take_dynconv_faults(&v2);
     v |= v2;
     if (e == cudaSuccess) e = df2::take_topk_faults(&v2);
+    v |= v2;
+    if (e == cudaSuccess) e = df2::take_fused_faults(&v2);
     v |= v2;
     if (e != cudaSuccess) return cuda_fail(e, "take_device_faults");
     *flags_out = (int32_t)v;

@@ -77,6 +77,28 @@ bool make_tmap_rows_bf16(CUtensorMap* m, const void* base, int rows, int cols, i
 cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream);
 // Reads and clears the convolution kernels' device fault word (synchronous).
 cudaError_t take_dynconv_faults(unsigned* flags);
+
+// The conv with its taps predicted from its input, fused (dynconv_pred.cu).
+constexpr int kMaxPredT = 8;
+struct DynconvPredArgs {
+    const void* x;     // [S*n, C] bf16
+    const void* hist;  // [S, T-1, C] bf16 or nullptr
+    const void* base;  // [T, C] bf16
+    const void* Wc;    // [T*G, C] bf16
+    void* out;         // [S*n, C] bf16 or fp32
+    int S, n, C, T, G;
+    int out_bf16;
+};
+struct DynconvPredPlan {
+    int NP, kblocks, m_tiles, split, stages, cdepth;
+    uint32_t stage_bytes, ring_bytes, ds_bytes, tmem_cols;
+    size_t smem_bytes;
+};
+// False when the shapes are outside what the fused kernel supports.
+bool plan_dynconv_pred(const DynconvPredArgs& a, int num_sms, size_t max_smem, DynconvPredPlan* plan);
+cudaError_t launch_dynconv_pred(const DynconvPredArgs& a, const DynconvPredPlan& plan,
+                                cudaStream_t stream);
+cudaError_t take_fused_faults(unsigned* flags);
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
 // Bytes of split-K workspace the bf16 projection uses for these shapes (0: none).
 size_t project_workspace_bytes(int P, int d, int R, int num_sms);

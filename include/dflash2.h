@@ -235,6 +235,28 @@ int dflash2_predict_delta(const void* x, const void* Wc, void* delta, int P, int
                           int dtype, void* stream);
 
 /*
+ * The convolution with its taps predicted from its own input, in one kernel:
+ * dflash2_predict_delta followed by dflash2_dynconv, without delta leaving the
+ * chip and with x read from HBM once (same pull request, Overview: the conv's
+ * per-position offsets are predicted from the input):
+ *   delta[p, t, g] = bf16( sum_c Wc[t*G + g, c] * x[p, c] )      (p = s*n + i)
+ *   out[s,i,c]     = sum_{t<T} (base[t,c] + delta[s*n+i, t, c/(C/G)]) * xh[s, i-t, c]
+ * with xh as in dflash2_dynconv (x, else the history row, else zero).  delta
+ * is rounded to bf16 between the two steps, as the unfused pair stores it.
+ *   x [S,n,C], hist [S,T-1,C] or NULL, base [T,C], Wc [T*G,C]: bf16;
+ *   out [S,n,C]: out_dtype (bf16 or fp32).  All caller-owned device memory.
+ * bf16 inputs only (tcgen05 tensor cores for delta, fp32 FMA for the conv).
+ * INVALID_ARG: S, n, C, T, G <= 0; C % G != 0; bad dtype; NULL pointer;
+ * misalignment; out overlapping an input.
+ * UNSUPPORTED: fp32 input; T > 8; C % 8 != 0 or (C/G) % 8 != 0;
+ * (T*G) % 8 != 0 or T*G > 256; S*n >= 2^31; shapes whose working set does not
+ * fit one CTA's shared memory.
+ */
+int dflash2_dynconv_predicted(const void* x, const void* hist, const void* base, const void* Wc,
+                              void* out, int S, int n, int C, int T, int G, int in_dtype,
+                              int out_dtype, void* stream);
+
+/*
  * Greedy chain readout with a p_min cut: the draft tokens of each sequence,
  * read from the selector's per-predecessor argmax table (ggml-org/llama.cpp
  * pull request #27342: the Overview's readout is each predecessor's argmax
@@ -266,7 +288,7 @@ int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edge
 /*
  * Reads and clears the library's device-side fault word for the current
  * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_dynconv,
- * dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from
+ * dflash2_dynconv_predicted, dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from
  * dflash2_topk).  Synchronises the current device.  Returns DF2_OK or
  * DF2_ERR_CUDA.
  */

@@ -196,3 +196,27 @@ def _pdelta(L, x=P[0], wc=P[1], de=P[2], Pn=64, C=128, TG=16, dt=1):
 ])
 def test_predict_delta_validation(L, kw, code):
     assert _pdelta(L, **kw) == code
+
+
+def _dpred(L, x=P[0], hist=P[1], base=P[2], wc=P[3], out=P[4], S=2, n=8, C=64, T=4, G=4,
+           di=1, do=1):
+    return L.dflash2_dynconv_predicted(x, hist, base, wc, out, S, n, C, T, G, di, do, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=NULL), 1), (dict(wc=NULL), 1), (dict(base=NULL), 1), (dict(out=NULL), 1),
+    (dict(S=0), 1), (dict(n=-1), 1), (dict(C=0), 1), (dict(T=0), 1), (dict(G=0), 1),
+    (dict(C=64, G=5), 1), (dict(di=7), 1), (dict(do=3), 1),
+    (dict(x=ctypes.c_void_p(0x10000008)), 1),
+    (dict(out=P[0]), 1),                       # out aliases x
+    (dict(out=P[3]), 1),                       # out aliases Wc
+    (dict(di=0, do=0), 2),                     # fp32 input
+    (dict(T=9, G=8), 2),                       # T > 8
+    (dict(C=60, G=4), 2),                      # C % 8
+    (dict(C=64, G=16), 2),                     # C/G = 4
+    (dict(T=3, G=4), 2),                       # T*G = 12
+    (dict(C=2048, T=8, G=64), 2),              # T*G = 512
+])
+def test_dynconv_predicted_validation(L, kw, code):
+    assert _dpred(L, **kw) == code
+    assert L.dflash2_last_error()
