@@ -47,7 +47,9 @@ namespace {
 
 constexpr int kBM = 128;                  // positions per tile (MMA M)
 constexpr int kBK = 64;                   // channels per k-block (one 128-byte swizzle row)
-constexpr int kThreads = 256;             // 8 warps
+// Threads per CTA: 512 (16 warps) for T <= 4, where the conv phase's
+// registers allow it, else 256; more warps hide the conv's dependent FMAs.
+__host__ __device__ constexpr int threads_for(int T) { return T <= 4 ? 512 : 256; }
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr int kPL = 8;                    // positions per conv strip
 constexpr int kMaxStages = 6;
@@ -140,8 +142,8 @@ __device__ __forceinline__ void conv8(const float2 (&bw)[T][4], const float2 (&x
     }
 }
 
-template <int T, typename TOut>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int T, typename TOut, int NT = threads_for(T)>
+__global__ void __launch_bounds__(NT, 1)
     dynconv_pred_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                         const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -238,12 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait_bounded(accum, 0, kWaitNs)) ok = false;
     tc_fence_after();
     float* red = reinterpret_cast<float*>(ring);
-    if (warp < 4) {
-        const int row = warp * 32 + lane;
+    {
+        // warp w reads TMEM lanes 32*(w%4).. (its quadrant), column chunks
+        // (w/4)*32, stepping over the warp groups
+        const int row = (warp & 3) * 32 + lane;
 #pragma unroll 1
-        for (int c0 = 0; c0 < p.TG; c0 += 32) {
+        for (int c0 = (warp >> 2) * 32; c0 < p.TG; c0 += (NT / 128) * 32) {
             uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c0, v);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         // Each task: 4 positions of one needed column (tap t, group g_lo+gl),
         // summed over the cluster's partial tiles in rank order (deterministic)
-        // from 16-byte distributed-shared-memory loads; four tasks per round,
+        // from 16-byte distributed-shared-memory loads; two tasks per round,
         // all their loads issued before the first sum.
         const uint32_t red_s = smem_u32(red);
         uint32_t src_base[8];
@@ -269,11 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r) src_base[r] = r < p.split ? map_cluster(red_s, (uint32_t)r) : 0u;
         const int tot = T * ngl * (kBM / 4);
 #pragma unroll 1
-        for (int q0 = tid; q0 < tot; q0 += 4 * kThreads) {
-            float4 v[4][8];
+        for (int q0 = tid; q0 < tot; q0 += 2 * NT) {
+            float4 v[2][8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = min(q0 + e * kThreads, tot - 1);
+            for (int e = 0; e < 2; ++e) {
+                const int q = min(q0 + e * NT, tot - 1);
                 const int cj = q / (kBM / 4);
                 const int rq = q - cj * (kBM / 4);
                 const int t = cj / ngl;
@@ -284,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (r < p.split) v[e][r] = ld_cluster_f4(src_base[r] + off);
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = q0 + e * kThreads;
+            for (int e = 0; e < 2; ++e) {
+                const int q = q0 + e * NT;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
@@ -339,16 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nvec = (c_hi - c_lo) / 8;
     const int p0 = m_tile * kBM;
     const int items = *n_pieces * nvec;
-    const int my_n = tid < items ? (items - tid + kThreads - 1) / kThreads : 0;
+    const int my_n = tid < items ? (items - tid + NT - 1) / NT : 0;
     const int depth = p.cdepth;
     const uint32_t ring_s = smem_u32(ring);
     TOut* out = static_cast<TOut*>(p.out);
     auto slot_row = [&](int slot, int r) -> uint32_t {
-        return ring_s + (uint32_t)(((slot * RW + r) * kThreads + tid) * 16);
+        return ring_s + (uint32_t)(((slot * RW + r) * NT + tid) * 16);
     };
     auto issue = [&](int k) {
         if (k < my_n) {
-            const int item = tid + k * kThreads;
+            const int item = tid + k * NT;
             const int pc = item / nvec;
             const int c = c_lo + (item - pc * nvec) * 8;
             const int ps = p0 + piece_start[pc];
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
     for (int k = 0; k < my_n; ++k) {
         cp_wait_pending(depth - 1);  // this thread's copies of item k have landed
-        const int item = tid + k * kThreads;
+        const int item = tid + k * NT;
         const int pc = item / nvec;
         const int c = c_lo + (item - pc * nvec) * 8;
         const int row0 = piece_start[pc];
@@ -389,26 +393,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 bw[T][4];
 #pragma unroll
         for (int t = 0; t < T; ++t) row_to_f2(ldg_nc_v4(p.base + (size_t)t * C + c), bw[t]);
-        uint4 w[RW];
+        // xw[t] = x[position - t], converted once per row and slid along: each
+        // position first shifts the window by one tap, then loads its own row
+        // into xw[0]; before position 0, xw[t] holds window row T-2-t.
+        float2 xw[T][4];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) w[r] = lds_v4(slot_row(slot, r));
+        for (int t = 0; t < T - 1; ++t) row_to_f2(lds_v4(slot_row(slot, T - 2 - t)), xw[t]);
         const uint16_t* dsr = ds + (size_t)gl * kBM + row0;
 #pragma unroll
         for (int l = 0; l < kPL; ++l) {
             if (l < nl) {
-                float2 xw[T][4];
+#pragma unroll
+                for (int t = T - 1; t > 0; --t)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xw[t][q] = xw[t - 1][q];
+                row_to_f2(lds_v4(slot_row(slot, l + T - 1)), xw[0]);
                 float dt[T];
 #pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    row_to_f2(w[l + T - 1 - t], xw[t]);
+                for (int t = 0; t < T; ++t)
                     dt[t] = __uint_as_float((uint32_t)dsr[(size_t)t * ngl * kBM + l] << 16);
-                }
                 float2 acc[4];
                 conv8<T>(bw, xw, dt, acc);
                 store8(out + (size_t)(p0 + row0 + l) * C + c, acc);
             }
         }
-        issue(k + depth);  // the slot's rows are in registers: refill it
+        issue(k + depth);  // the slot's rows have been read: refill it
     }
     cp_wait_pending(0);
     if (!ok) atomicOr(&g_fused_fault, (unsigned)DF2_FLAG_TIMEOUT);
@@ -428,7 +437,7 @@ cudaError_t launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const Fused
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(T), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -491,7 +500,7 @@ bool plan_dynconv_pred(const DynconvPredArgs& a, int num_sms, size_t max_smem, D
     }
     r.stage_bytes = kABytes + (uint32_t)r.NP * 128u;
     const size_t red_bytes = (size_t)kBM * TG * 4;
-    const size_t conv_row_bytes = (size_t)(kPL + a.T - 1) * kThreads * 16;  // one item slot
+    const size_t conv_row_bytes = (size_t)(kPL + a.T - 1) * threads_for(a.T) * 16;  // one item slot
     const size_t ds_bytes = ((size_t)kBM * a.T * ngl_max * 2 + 15) & ~(size_t)15;
     // barriers, TMEM slot, piece count, piece table [129] and 4 warp counts
     const size_t tail = (2 * kMaxStages + 1) * 8 + 320;
