@@ -51,6 +51,10 @@ TRAFFIC = {
         "sha": "ba528104f498b57b66ed7ce720e829e70da5c4cdac4644f7ceaa22e20a4d59db",  # capture taken before a comment-only edit of the file
         "bytes": 8 * (311424512 + 3649536),
     },
+    ("batched_256x16_d5120", "dynconv_predicted"): {
+        "sha": "d90b1cc51824bf525afc18d4a8cf33beaac1c7f6629d7a31bec6ef475937b002",  # capture taken before a comment-only edit of the file
+        "bytes": 52443136 + 3306496,
+    },
 }
 
 
@@ -695,6 +699,10 @@ def main():
                                               "topk.cu"), "rb").read()).hexdigest()
     tr = TRAFFIC.get((w.name, "topk"))
     topk_traffic = tr["bytes"] if tr and tr["sha"] == tk_sha else None
+    fz_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
+                                              "dynconv_pred.cu"), "rb").read()).hexdigest()
+    tr = TRAFFIC.get((w.name, "dynconv_predicted"))
+    fz_traffic = tr["bytes"] if tr and tr["sha"] == fz_sha else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -716,6 +724,10 @@ def main():
             "topk": {"bound": "hbm", "achieved": topk_b / topk_us / 1e3, "peak": hbm,
                      "unit": "GB/s", "frac": topk_b / topk_us / 1e3 / hbm,
                      "traffic": topk_traffic, "timing": "isolated loop"},
+            "dynconv_predicted": None if fz is None else {
+                "bound": "hbm", "achieved": fz["bytes"] / fz["us"] / 1e3, "peak": hbm,
+                "unit": "GB/s", "frac": fz["bytes"] / fz["us"] / 1e3 / hbm,
+                "traffic": fz_traffic, "timing": "isolated loop"},
         },
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,

@@ -18,17 +18,24 @@
 //      the tile's x rows and of Wc through a TMA ring (128-byte swizzle,
 //      K-major) into tcgen05.mma (M = 128 positions, N = T*G rounded up to 16,
 //      fp32 accumulation in tensor memory);
-//   2. the partial tiles go to shared memory (tcgen05.ld); after a cluster
-//      barrier each CTA sums, in rank order (deterministic), the columns its own
-//      channel slice needs -- taps t*G+g for the groups g its channels fall
-//      in -- reading the other CTAs' partials through distributed shared memory,
-//      and keeps them as bf16;
-//   3. each CTA convolves its channel slice over the tile's 128 positions,
-//      reading x again: the tile's rows were just streamed through L2 by the
-//      TMA loads of step 1, so this second read costs L2 bandwidth, not HBM.
+//   2. the partial tiles go to shared memory, column-major (tcgen05.ld by all
+//      warps); after a cluster barrier each CTA sums, in rank order
+//      (deterministic), the columns its own channel slice needs -- taps t*G+g
+//      for the groups g its channels fall in -- with 16-byte loads of the other
+//      CTAs' partials through distributed shared memory, and keeps them as bf16;
+//   3. each CTA convolves its channel slice over the tile's 128 positions, in
+//      pieces of at most 8 positions of one sequence; every thread stages the
+//      window rows of its next items into its own slots of the freed TMA ring
+//      with 16-byte cp.async copies (zero-fill for a missing history) and
+//      slides a window of converted rows over each piece.  x is read again,
+//      but the tile's rows were just streamed through L2 by the TMA loads of
+//      step 1, so this second read costs L2 bandwidth, not HBM.
 // HBM traffic is therefore x once, Wc (shared by every tile, L2-resident) and
 // the output: the delta round trip and the second HBM pass over x of the
-// unfused predictor + conv pair are gone.
+// unfused predictor + conv pair are gone.  The single wave of CTAs runs step 1
+// (HBM-bound) and step 3 (FP32-issue-bound) one after the other, so on a
+// one-wave problem the time is close to that of the pair; what it saves is
+// bytes.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
