@@ -418,8 +418,8 @@ int dflash2_dynconv_predicted(const void* x, const void* hist, const void* base,
     if (st == DF2_OK) st = check_aligned(outs, 1);
     if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 4);
     if (st != DF2_OK) return st;
-    if (in_dtype != DF2_BF16)
-        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: needs bf16 input");
+    if (in_dtype == DF2_F32 && out_dtype == DF2_BF16)
+        return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: fp32 input with bf16 output");
     if (T > df2::kMaxPredT)
         return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: T=%d > %d", T, df2::kMaxPredT);
     const long long TG = (long long)T * G;
@@ -431,6 +431,11 @@ int dflash2_dynconv_predicted(const void* x, const void* hist, const void* base,
         return fail(DF2_ERR_UNSUPPORTED, "dynconv_predicted: S*n above 2^31-1");
     df2::DynconvPredArgs a{x, T > 1 ? hist : nullptr, base, Wc, out, S, n, C, T, G,
                            out_dtype == DF2_BF16};
+    if (in_dtype == DF2_F32) {
+        cudaError_t e = df2::launch_dynconv_pred_f32(a, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "dynconv_predicted launch");
+        return DF2_OK;
+    }
     df2::DynconvPredPlan plan{};
     if (!df2::plan_dynconv_pred(a, num_sms_of_current_device(), max_smem_optin_of_current_device(),
                                 &plan))

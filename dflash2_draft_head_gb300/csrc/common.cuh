@@ -98,6 +98,8 @@ struct DynconvPredPlan {
 bool plan_dynconv_pred(const DynconvPredArgs& a, int num_sms, size_t max_smem, DynconvPredPlan* plan);
 cudaError_t launch_dynconv_pred(const DynconvPredArgs& a, const DynconvPredPlan& plan,
                                 cudaStream_t stream);
+// fp32 inputs and output (T*G <= 256): delta in exact fp32, no tensor cores.
+cudaError_t launch_dynconv_pred_f32(const DynconvPredArgs& a, cudaStream_t stream);
 cudaError_t take_fused_faults(unsigned* flags);
 cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, int num_sms);
 // Bytes of split-K workspace the bf16 projection uses for these shapes (0: none).

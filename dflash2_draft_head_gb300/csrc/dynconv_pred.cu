@@ -477,6 +477,88 @@ cudaError_t launch_out(int T, const CUtensorMap& tmX, const CUtensorMap& tmW, co
     }
 }
 
+
+// ---------------------------------------------------------------- all-fp32 mode
+//
+// The same operation with fp32 inputs, delta in exact fp32 (FFMA, no TF32, no
+// rounding between the steps): a CTA per 16 positions computes their delta tile
+// [16][T*G] from 32-channel chunks of x and Wc staged in shared memory, then
+// convolves the 16 positions over all channels from that tile.  Meant for the
+// small fp32 shapes; the bf16 kernel above is the fast path.
+constexpr int kFP = 16;     // positions per CTA
+constexpr int kFK = 32;     // channels per staged chunk
+constexpr int kFThreads = 256;
+
+struct F32Params {
+    const float* x;
+    const float* hist;
+    const float* base;
+    const float* Wc;
+    float* out;
+    int P, n, C, T, G, TG, cg;
+};
+
+__global__ void __launch_bounds__(kFThreads) dynconv_pred_f32_kernel(const F32Params p) {
+    extern __shared__ float fsm[];
+    float* xs = fsm;                         // [kFP][kFK + 1]
+    float* ws = xs + kFP * (kFK + 1);        // [TG][kFK + 1]
+    float* dsm = ws + p.TG * (kFK + 1);      // [kFP][TG]
+    const int tid = threadIdx.x;
+    const int p0 = blockIdx.x * kFP;
+    const int nout = kFP * p.TG;             // <= 16 * 256: at most 16 per thread
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    for (int j0 = 0; j0 < p.C; j0 += kFK) {
+        for (int q = tid; q < kFP * kFK; q += kFThreads) {
+            const int r = q / kFK, jj = q % kFK, j = j0 + jj;
+            xs[r * (kFK + 1) + jj] = (p0 + r < p.P && j < p.C) ? p.x[(size_t)(p0 + r) * p.C + j] : 0.f;
+        }
+        for (int q = tid; q < p.TG * kFK; q += kFThreads) {
+            const int r = q / kFK, jj = q % kFK, j = j0 + jj;
+            ws[r * (kFK + 1) + jj] = j < p.C ? p.Wc[(size_t)r * p.C + j] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int q = tid + k * kFThreads;
+            if (q < nout) {
+                const int r = q / p.TG, col = q - r * p.TG;
+                float a = acc[k];
+#pragma unroll 8
+                for (int jj = 0; jj < kFK; ++jj)
+                    a = fmaf(xs[r * (kFK + 1) + jj], ws[col * (kFK + 1) + jj], a);
+                acc[k] = a;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const int q = tid + k * kFThreads;
+        if (q < nout) dsm[q] = acc[k];
+    }
+    __syncthreads();
+    const int T = p.T;
+    for (int q = tid; q < kFP * p.C; q += kFThreads) {
+        const int r = q / p.C, c = q - r * p.C;
+        const int pos = p0 + r;
+        if (pos >= p.P) continue;
+        const int s = pos / p.n, i = pos - s * p.n;
+        const int g = c / p.cg;
+        float a = 0.f;
+        for (int t = 0; t < T; ++t) {
+            float xv = 0.f;
+            if (i - t >= 0)
+                xv = p.x[(size_t)(pos - t) * p.C + c];
+            else if (p.hist != nullptr)
+                xv = p.hist[((size_t)s * (T - 1) + (T - 1 + i - t)) * p.C + c];
+            a = fmaf(p.base[(size_t)t * p.C + c] + dsm[r * p.TG + t * p.G + g], xv, a);
+        }
+        p.out[(size_t)pos * p.C + c] = a;
+    }
+}
+
 }  // namespace
 
 bool plan_dynconv_pred(const DynconvPredArgs& a, int num_sms, size_t max_smem, DynconvPredPlan* plan) {
@@ -570,6 +652,31 @@ cudaError_t launch_dynconv_pred(const DynconvPredArgs& a, const DynconvPredPlan&
     const int grid = r.m_tiles * r.split;
     return a.out_bf16 ? launch_out<__nv_bfloat16>(a.T, tmX, tmW, q, r.smem_bytes, grid, stream)
                       : launch_out<float>(a.T, tmX, tmW, q, r.smem_bytes, grid, stream);
+}
+
+cudaError_t launch_dynconv_pred_f32(const DynconvPredArgs& a, cudaStream_t stream) {
+    F32Params q{};
+    q.x = static_cast<const float*>(a.x);
+    q.hist = static_cast<const float*>(a.hist);
+    q.base = static_cast<const float*>(a.base);
+    q.Wc = static_cast<const float*>(a.Wc);
+    q.out = static_cast<float*>(a.out);
+    q.P = a.S * a.n;
+    q.n = a.n;
+    q.C = a.C;
+    q.T = a.T;
+    q.G = a.G;
+    q.TG = a.T * a.G;
+    q.cg = a.C / a.G;
+    if (q.TG > 256) return cudaErrorInvalidValue;
+    const size_t smem = ((size_t)kFP * (kFK + 1) + (size_t)q.TG * (kFK + 1) + (size_t)kFP * q.TG) *
+                        sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(dynconv_pred_f32_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((q.P + kFP - 1) / kFP);
+    dynconv_pred_f32_kernel<<<grid, kFThreads, smem, stream>>>(q);
+    return cudaGetLastError();
 }
 
 cudaError_t take_fused_faults(unsigned* flags) {

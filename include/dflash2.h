@@ -239,16 +239,19 @@ int dflash2_predict_delta(const void* x, const void* Wc, void* delta, int P, int
  * dflash2_predict_delta followed by dflash2_dynconv, without delta leaving the
  * chip and with x read from HBM once (same pull request, Overview: the conv's
  * per-position offsets are predicted from the input):
- *   delta[p, t, g] = bf16( sum_c Wc[t*G + g, c] * x[p, c] )      (p = s*n + i)
+ *   delta[p, t, g] = rnd( sum_c Wc[t*G + g, c] * x[p, c] )       (p = s*n + i)
  *   out[s,i,c]     = sum_{t<T} (base[t,c] + delta[s*n+i, t, c/(C/G)]) * xh[s, i-t, c]
- * with xh as in dflash2_dynconv (x, else the history row, else zero).  delta
- * is rounded to bf16 between the two steps, as the unfused pair stores it.
- *   x [S,n,C], hist [S,T-1,C] or NULL, base [T,C], Wc [T*G,C]: bf16;
- *   out [S,n,C]: out_dtype (bf16 or fp32).  All caller-owned device memory.
- * bf16 inputs only (tcgen05 tensor cores for delta, fp32 FMA for the conv).
+ * with xh as in dflash2_dynconv (x, else the history row, else zero); rnd
+ * rounds to the input dtype (bf16: nearest even), as the unfused pair stores
+ * delta between its two steps.
+ *   x [S,n,C], hist [S,T-1,C] or NULL, base [T,C], Wc [T*G,C]: in_dtype;
+ *   out [S,n,C]: out_dtype.  All caller-owned device memory.
+ * bf16 input (bf16 or fp32 out): tcgen05 tensor cores for delta, fp32 FMA for
+ * the conv.  fp32 input (fp32 out): delta in exact fp32 (no TF32) and no
+ * rounding between the steps.
  * INVALID_ARG: S, n, C, T, G <= 0; C % G != 0; bad dtype; NULL pointer;
  * misalignment; out overlapping an input.
- * UNSUPPORTED: fp32 input; T > 8; C % 8 != 0 or (C/G) % 8 != 0;
+ * UNSUPPORTED: fp32 input with bf16 output; T > 8; C % 8 != 0 or (C/G) % 8 != 0;
  * (T*G) % 8 != 0 or T*G > 256; S*n >= 2^31; shapes whose working set does not
  * fit one CTA's shared memory.
  */

@@ -210,7 +210,7 @@ def _dpred(L, x=P[0], hist=P[1], base=P[2], wc=P[3], out=P[4], S=2, n=8, C=64, T
     (dict(x=ctypes.c_void_p(0x10000008)), 1),
     (dict(out=P[0]), 1),                       # out aliases x
     (dict(out=P[3]), 1),                       # out aliases Wc
-    (dict(di=0, do=0), 2),                     # fp32 input
+    (dict(di=0, do=1), 2),                     # fp32 input with bf16 output
     (dict(T=9, G=8), 2),                       # T > 8
     (dict(C=60, G=4), 2),                      # C % 8
     (dict(C=64, G=16), 2),                     # C/G = 4

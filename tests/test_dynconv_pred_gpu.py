@@ -121,13 +121,42 @@ def test_fused_matches_predict_then_convolve():
     assert_close(f, p, "bf16", "fused vs pair")
 
 
-def test_fused_rejects_fp32_and_wide_taps():
-    w = _w(1, 8, 128, 4, 8, 5)
+def _wf(S, n, C, T, G, seed):
+    return Workload(name="dpf", S=S, n=n, C=C, T=T, G=G, d=C, R=16, V=100, K=4, dtype="f32",
+                    S_sel=S, n_sel=n, seed=seed)
+
+
+@pytest.mark.parametrize("S,n,C,T,G,hist", [
+    (1, 8, 256, 4, 8, True),      # the tiny all-fp32 workload's shape
+    (2, 37, 512, 4, 8, True),
+    (3, 50, 200, 8, 25, True),
+    (2, 9, 128, 1, 16, True),
+    (40, 1, 256, 4, 8, False),
+    (3, 21, 384, 3, 8, False),
+])
+def test_fused_fp32_parity(S, n, C, T, G, hist):
+    """All-fp32 mode: delta in exact fp32 (no rounding between the steps)."""
+    w = _wf(S, n, C, T, G, 500 + S + n + C + T)
+    ci = synth.conv_inputs(w, with_hist=hist)
+    Wc = synth.conv_proj(w)
+    out = df2.dynconv_predicted(ci["x"].cuda(), ci["hist"].cuda() if hist else None,
+                                ci["base"].cuda(), Wc.cuda(), w.G)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.float32
+    dref = oracle.project(ci["x"].reshape(-1, C).numpy(), Wc.numpy()).reshape(S, n, T, G)
+    ref = oracle.dynconv(ci["x"].numpy(), ci["hist"].numpy() if hist else None,
+                         ci["base"].numpy(), dref)
+    assert_close(out.cpu().numpy(), ref, "f32", f"dynconv_predicted fp32 {S}x{n}x{C} T{T}")
+
+
+def test_fused_rejects_fp32_to_bf16_and_wide_taps():
+    w = _wf(1, 8, 128, 4, 8, 5)
     ci = synth.conv_inputs(w)
     Wc = synth.conv_proj(w)
     x = ci["x"].cuda()
     with pytest.raises(df2.Dflash2Error):
-        df2.dynconv_predicted(x, ci["hist"].cuda(), ci["base"].cuda(), Wc.cuda(), w.G)
+        df2.dynconv_predicted(x, ci["hist"].cuda(), ci["base"].cuda(), Wc.cuda(), w.G,
+                              out_dtype=torch.bfloat16)
     b = torch.bfloat16
     xb = torch.zeros((1, 8, 2048), dtype=b, device="cuda")
     with pytest.raises(df2.Dflash2Error):  # T*G = 512
