@@ -407,6 +407,35 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int t = 0; t < T - 1; ++t) row_to_f2(lds_v4(slot_row(slot, T - 2 - t)), xw[t]);
         const uint16_t* dsr = ds + (size_t)gl * kBM + row0;
+        if (nl == kPL && (row0 & (kPL - 1)) == 0) {
+            // a full, aligned piece (every piece when n is a multiple of 8): no
+            // per-position guard, and each tap's delta for two positions in one
+            // 4-byte load
+            const uint32_t* dsw = reinterpret_cast<const uint32_t*>(dsr);
+            const int wstride = ngl * kBM / 2;  // tap t+1's column, in 4-byte words
+            uint32_t dw[T];
+#pragma unroll
+            for (int l = 0; l < kPL; ++l) {
+                if ((l & 1) == 0) {
+#pragma unroll
+                    for (int t = 0; t < T; ++t) dw[t] = dsw[t * wstride + (l >> 1)];
+                }
+#pragma unroll
+                for (int t = T - 1; t > 0; --t)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xw[t][q] = xw[t - 1][q];
+                row_to_f2(lds_v4(slot_row(slot, l + T - 1)), xw[0]);
+                float dt[T];
+#pragma unroll
+                for (int t = 0; t < T; ++t)
+                    dt[t] = __uint_as_float((l & 1) ? (dw[t] & 0xFFFF0000u) : (dw[t] << 16));
+                float2 acc[4];
+                conv8<T>(bw, xw, dt, acc);
+                store8(out + (size_t)(p0 + row0 + l) * C + c, acc);
+            }
+            issue(k + depth);
+            continue;
+        }
 #pragma unroll
         for (int l = 0; l < kPL; ++l) {
             if (l < nl) {
