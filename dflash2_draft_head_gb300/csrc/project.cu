@@ -77,10 +77,22 @@ __device__ __forceinline__ void store_out4(const ProjParams& p, size_t off, floa
     }
 }
 
-template <int SPLIT>
+// SMEM_BYTES of a kernel instance with N tile BNT (4 stages for 256 columns).
+constexpr size_t smem_bytes_for(int BNT) {
+    return 1024 + (size_t)(BNT == 256 ? 4 : STAGES) * (A_BYTES + BNT * BK * 2) + 256;
+}
+
+// BNT = 256 (one instruction of N = 256, 4 stages) only with SPLIT = 1: for
+// outputs wider than 128 columns on grids that fill the GPU without split-K,
+// where it halves how often each tile of h is read from L2.
+template <int SPLIT, int BNT = 128>
 __global__ void __launch_bounds__(NTHREADS, 1)
     project_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const ProjParams p) {
+    static_assert(BNT == 128 || (BNT == 256 && SPLIT == 1), "256-column tiles without split-K only");
+    constexpr int BN = BNT;
+    constexpr int STAGES = BNT == 256 ? 4 : ::df2::STAGES;
+    constexpr int STAGE_BYTES = A_BYTES + BN * BK * 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -407,6 +419,33 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
     // the SMs without exceeding them and leaves every CTA at least 2 k-blocks.
     int split = 1;
     while (split < 8 && tiles * split * 2 <= num_sms && kblocks >= split * 4) split *= 2;
+    if (split == 1 && a.R > BN) {
+        // 256-column tiles when they still give every SM at least one tile
+        const int n_wide = (a.R + 255) / 256;
+        if ((long long)m_tiles * n_wide >= num_sms) {
+            CUtensorMap tmW;
+            if (!make_tmap_rows_bf16(&tmW, a.W, a.R, a.d, 256)) return cudaErrorInvalidValue;
+            auto wk = project_tc_kernel<1, 256>;
+            const size_t smem = smem_bytes_for(256);
+            cudaError_t ew = cudaFuncSetAttribute(wk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)smem);
+            if (ew != cudaSuccess) return ew;
+            ProjParams pw{a.u, static_cast<__nv_bfloat16*>(a.out_bf16), a.P, a.R, kblocks, 1, a.ws};
+            cudaLaunchConfig_t cw{};
+            cw.gridDim = dim3(1u, (unsigned)m_tiles, (unsigned)n_wide);
+            cw.blockDim = dim3(NTHREADS, 1, 1);
+            cw.dynamicSmemBytes = smem;
+            cw.stream = stream;
+            cudaLaunchAttribute aw[1];
+            aw[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            aw[0].val.programmaticStreamSerializationAllowed = 1;
+            cw.attrs = aw;
+            cw.numAttrs = 1;
+            ew = cudaLaunchKernelEx(&cw, wk, tmA, tmW, pw);
+            if (ew != cudaSuccess) return ew;
+            return cudaGetLastError();
+        }
+    }
 
     auto kern = split == 1 ? project_tc_kernel<1>
                 : split == 2 ? project_tc_kernel<2>

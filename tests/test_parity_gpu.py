@@ -173,6 +173,8 @@ def test_project_workloads(name):
     dict(S=4, n=64, d=1032, R=160),        # two N tiles (the delta predictor's T*G), split-K
     dict(S=64, n=64, d=5120, R=160),       # two N tiles, 32 M tiles
     dict(S=1, n=16, d=5120, R=152),        # two N tiles, ragged R, one M tile
+    dict(S=40, n=500, d=512, R=200),       # 157 M tiles: one 256-column tile, ragged R
+    dict(S=20, n=1000, d=256, R=512),      # 157 M tiles x two 256-column tiles
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_project_edge_shapes(kw, dtype):
