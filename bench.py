@@ -52,10 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311424512 + 3649536),
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
-        # capture taken before a comment-only edit of the file and before the separate
-        # fp32 kernel was added to it; dynconv_pred_kernel itself is unchanged
-        "sha": "bbce1755fb7c7c512ed7f6b99f3633e5541e42847f8a0ca396e6603c79aa06c3",
-        "bytes": 52443136 + 3306496,
+        "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
+        "bytes": 52396288 + 3153408,
     },
 }
 
