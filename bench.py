@@ -422,6 +422,47 @@ def _timed_eager(K, stream, flush, calls, L):
     return [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nc)]
 
 
+def gather_ceiling(w, dev, stream, flush, record_ext, L, steps):
+    """Random-row gather rate of this GPU (dflash2_probe_gather), the bound of the
+    edge kernel's codebook reads: the workload's gather volume (2 rows of R per
+    candidate per transition) read as rows of 128, 256 and 512 bytes at uniform
+    random ids from a table the size of the two codebooks, L2 flushed between
+    launches."""
+    import ctypes
+
+    import torch
+    b = 2 if w.dtype == "bf16" else 4
+    E = w.S_sel * max(w.n_sel - 1, 0)
+    table_bytes = 2 * w.V * w.R * b
+    gather_bytes = 2 * E * w.K * w.R * b
+    if gather_bytes == 0:
+        return None
+    table = torch.zeros(table_bytes // 4, dtype=torch.int32, device=dev)
+    g = torch.Generator().manual_seed(4242)
+    out = {"table_bytes": table_bytes, "gathered_bytes": gather_bytes,
+           "note": "read-only random gathers at uniform ids (4 bytes written per row); the "
+                   "edge kernel reads R*b-byte codebook rows this way"}
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    for rb in (128, 256, 512):
+        rows = table_bytes // rb
+        n_ids = gather_bytes // rb
+        ids = torch.randint(0, rows, (n_ids,), generator=g, dtype=torch.int32).to(dev)
+        res = torch.empty((n_ids,), dtype=torch.int32, device=dev)
+        args = (ctypes.c_void_p(table.data_ptr()), rows, rb, ctypes.c_void_p(ids.data_ptr()),
+                n_ids, ctypes.c_void_p(res.data_ptr()), sp)
+        f = L.dflash2_probe_gather
+        _call(f, args, L)
+        if record_ext is not None:
+            t = _timed_graph(steps, stream, flush, [(f, args)], record_ext, L)[0]
+        else:
+            t = _timed_eager(steps, stream, flush, [(f, args)], L)[0]
+        us = 1000.0 * statistics.median(t)
+        out[f"rows_{rb}B"] = {"us": us, "GB/s": (n_ids * (rb + 4)) / us / 1e3,
+                              "frac_hbm": (n_ids * (rb + 4)) / us / 1e3 / _peaks()[0]}
+    del table
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def main():
@@ -614,6 +655,7 @@ def main():
     chain_b = w.S_sel * (2 * max(w.n_sel - 1, 0) * w.K * 4 + w.K * 4 + w.n_sel * 4
                          + w.n_sel * 8 + 4)
     del e_full
+    gather = gather_ceiling(w, dev, stream, flush, record_ext, L, K_iso)
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -761,6 +803,7 @@ def main():
                      "GB/s": topk_b / topk_us / 1e3, "frac_hbm": topk_b / topk_us / 1e3 / hbm,
                      "note": "not part of the timed step; candidate extraction before it"},
         },
+        "gather_ceiling": gather,
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2,
                 "pipelining": "double-buffered inputs: step k+1's H2D copies (2 streams) overlap "

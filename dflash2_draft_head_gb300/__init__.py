@@ -10,6 +10,7 @@ ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local convolution
 + candidate selector)".  This package is the thin Python binding over it.
 """
 from .binding import (Dflash2Error, chain, dynconv, dynconv_predicted, edges, lib,  # noqa: F401
-                      predict_delta, project, project_noalloc, project_workspace_bytes, select,
+                      predict_delta, probe_gather, project, project_noalloc,
+                      project_workspace_bytes, select,
                       take_device_faults, topk, version)
 from .build import build as build_library  # noqa: F401

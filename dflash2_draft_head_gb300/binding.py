@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_chain.restype = i
             L.dflash2_topk.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.dflash2_topk.restype = i
+            L.dflash2_probe_gather.argtypes = [vp, ctypes.c_longlong, i, vp, i, vp, vp]
+            L.dflash2_probe_gather.restype = i
             L.dflash2_take_device_faults.argtypes = [ctypes.POINTER(ctypes.c_int32)]
             L.dflash2_take_device_faults.restype = i
             _lib = L
@@ -312,3 +314,19 @@ def take_device_faults() -> int:
     v = ctypes.c_int32(0)
     _check(lib().dflash2_take_device_faults(ctypes.byref(v)))
     return int(v.value)
+
+
+def probe_gather(table, row_bytes: int, ids, out=None):
+    """Measurement aid: out[i] (int32 view of a uint32) = XOR of the 32-bit words of
+    row ids[i] of `table` viewed as [rows, row_bytes] bytes."""
+    _need(table, "table")
+    _need(ids, "ids", torch.int32)
+    nbytes = table.numel() * table.element_size()
+    rows = nbytes // int(row_bytes)
+    n_ids = ids.numel()
+    if out is None:
+        out = torch.empty((n_ids,), dtype=torch.int32, device=ids.device)
+    _need(out, "out", torch.int32)
+    _check(lib().dflash2_probe_gather(_ptr(table), rows, int(row_bytes), _ptr(ids), n_ids,
+                                      _ptr(out), _stream(ids.device)))
+    return out

@@ -1,6 +1,7 @@
 // C ABI of the DFlash2 draft-head library: argument validation on the host,
 // then dispatch to the kernels.  Nothing here allocates device memory or
 // synchronises the host (except dflash2_take_device_faults, by contract).
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -62,24 +63,35 @@ int check_aligned(const Buf* bufs, int nb) {
 bool valid_dtype(int d) { return d == DF2_F32 || d == DF2_BF16; }
 size_t esize(int d) { return d == DF2_BF16 ? 2 : 4; }
 
+// Per-device attribute caches.  Host threads may call in concurrently, so the
+// slots are atomics (a race only ever stores the same value twice).
+std::atomic<int> g_num_sms[64];
+std::atomic<int> g_max_smem[64];
+
 int num_sms_of_current_device() {
-    static int cached[64] = {0};
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    const bool slot = dev >= 0 && dev < 64;
+    if (slot) {
+        const int c = g_num_sms[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
-    if (dev >= 0 && dev < 64) cached[dev] = sms;
+    if (slot) g_num_sms[dev].store(sms, std::memory_order_relaxed);
     return sms;
 }
 
 size_t max_smem_optin_of_current_device() {
-    static int cached[64] = {0};
     int dev = 0, v = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 227 * 1024;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return (size_t)cached[dev];
+    const bool slot = dev >= 0 && dev < 64;
+    if (slot) {
+        const int c = g_max_smem[dev].load(std::memory_order_relaxed);
+        if (c > 0) return (size_t)c;
+    }
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 227 * 1024;
-    if (dev >= 0 && dev < 64) cached[dev] = v;
+    if (slot) g_max_smem[dev].store(v, std::memory_order_relaxed);
     return (size_t)v;
 }
 
@@ -479,6 +491,30 @@ int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edge
                      tokens, probs, length, err_flag};
     cudaError_t e = df2::launch_chain(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "chain launch");
+    return DF2_OK;
+}
+
+int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const int32_t* ids,
+                         int n_ids, uint32_t* out, void* stream) {
+    g_err[0] = 0;
+    if (table == nullptr || ids == nullptr || out == nullptr)
+        return fail(DF2_ERR_INVALID_ARG, "probe_gather: NULL table, ids or out");
+    if (rows <= 0 || n_ids < 0)
+        return fail(DF2_ERR_INVALID_ARG, "probe_gather: rows=%lld n_ids=%d", rows, n_ids);
+    if (row_bytes < 16 || row_bytes > 1024 || (row_bytes & (row_bytes - 1)) != 0)
+        return fail(DF2_ERR_INVALID_ARG,
+                    "probe_gather: row_bytes=%d must be a power of two in [16, 1024]", row_bytes);
+    const Buf ins[2] = {{table, (size_t)rows * (size_t)row_bytes, "table"},
+                        {ids, (size_t)n_ids * 4, "ids"}};
+    const Buf outs[1] = {{out, (size_t)n_ids * 4, "out"}};
+    int st = check_aligned(ins, 2);
+    if (st == DF2_OK) st = check_aligned(outs, 1);
+    if (st == DF2_OK) st = check_disjoint(outs, 1, ins, 2);
+    if (st != DF2_OK) return st;
+    df2::ProbeGatherArgs a{table, rows, row_bytes, ids, n_ids, out};
+    cudaError_t e = df2::launch_probe_gather(a, static_cast<cudaStream_t>(stream),
+                                             num_sms_of_current_device());
+    if (e != cudaSuccess) return cuda_fail(e, "probe_gather launch");
     return DF2_OK;
 }
 

@@ -106,7 +106,7 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
 size_t project_workspace_bytes(int P, int d, int R, int num_sms);
 // Size of the library's own fixed projection workspace (8 MiB).
 constexpr size_t kFixedProjectWorkspaceBytes = size_t(8) << 20;
-// Device address of that workspace on the current device (looked up on first use).
+// Device address of that workspace in the current context (looked up on every call).
 cudaError_t fixed_project_workspace(float** ptr);
 cudaError_t launch_project_f32(const ProjectArgs& a, cudaStream_t stream);
 // Reads and clears the projection kernel's device fault word (synchronous).
@@ -128,5 +128,18 @@ cudaError_t launch_chain(const ChainArgs& a, cudaStream_t stream);
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);
 // Reads and clears the top-K kernel's device fault word (synchronous).
 cudaError_t take_topk_faults(unsigned* flags);
+
+// Measurement aid: random-row gather (probe.cu).  out[i] = XOR of the 32-bit
+// words of row ids[i] (ids clamped into [0, rows)); row_bytes a power of two
+// in [16, 1024].
+struct ProbeGatherArgs {
+    const void* table;
+    long long rows;
+    int row_bytes;
+    const int32_t* ids;
+    int n_ids;
+    uint32_t* out;
+};
+cudaError_t launch_probe_gather(const ProbeGatherArgs& a, cudaStream_t stream, int num_sms);
 
 }  // namespace df2

@@ -5,25 +5,23 @@
 // For every transition into position i (predecessors = candidates of i-1):
 //   e[p,c] = sum_r A[id_p,r] u[i,r] B[id_c,r] + unary[i,c],  readout argmax_c.
 //
-// Tensor-core tile path (bf16 codebooks, K a power of two <= 128, R <= 384):
-//  - a CTA takes 128/K consecutive transitions, i.e. 128 predecessor rows and
-//    128 candidate rows;
-//  - 128 threads gather the rows by token id with 16-byte loads (a half-warp
-//    or a warp per 256/512-byte row, fully coalesced), form the gate
-//    G = A[id_p] (.) u in fp32, round it to bf16 and store G and B[id_c]
-//    straight into the 128-byte-swizzle K-major layout of the tensor core;
-//  - one thread issues tcgen05.mma (M=128, N=128, K=16 per instruction) over
-//    R into a 128x128 fp32 accumulator in tensor memory.  Only the K x K
-//    diagonal blocks (same transition) are read back; the rest of the tile
-//    is free work on an otherwise idle unit;
-//  - each thread owns one predecessor row: tcgen05.ld of its block, + unary,
-//    running argmax (lowest slot wins ties), writes best slot / score and,
-//    optionally, the K edge scores.
-//
-// Warp path (any K <= 256, R <= 512, fp32 or bf16 codebooks): one warp per
-// (transition, predecessor); lanes split R, the gate stays in registers, and
-// each candidate's dot product is reduced with warp shuffles.  This is the
-// exact-fp32 path.
+// Paths, by codebook dtype and K:
+//  - edges_pipe_kernel (bf16, K a power of two in [4, 128], R <= 512): one
+//    persistent CTA per SM, warp-specialised.  Tiles of 128/K transitions
+//    (128 predecessor rows and 128 candidate rows) round-robin over the CTAs;
+//    16 gather warps copy the codebook rows by token id with 16-byte cp.async
+//    straight into the 128-byte-swizzle K-major layout of the tensor core, 4
+//    gate warps form A[id_p] (.) u in place (fp32 product, bf16 rounding), one
+//    warp issues tcgen05.mma (M = N = 128) into one of two TMEM accumulators,
+//    and 4 epilogue warps read back only each transition's K x K diagonal
+//    block (+ unary, running argmax, lowest slot on ties).  The off-diagonal
+//    blocks are free work on an otherwise idle unit.
+//  - edges_tc_kernel (bf16, K in {1, 2}, R <= 384): the same contraction, one
+//    tile per CTA, no pipeline.
+//  - edges_warp_kernel (any K <= 256, R <= 512, fp32 or bf16 codebooks): one
+//    warp per (transition, predecessor); lanes split R, the gate stays in
+//    registers, and each candidate's dot product is reduced with warp
+//    shuffles.  This is the exact-fp32 path.
 #include <cuda.h>
 #include <cuda_bf16.h>
 

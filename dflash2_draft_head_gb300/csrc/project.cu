@@ -25,8 +25,6 @@
 
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "dflash2.h"
 #include "common.cuh"
 #include "ptx.cuh"
@@ -483,27 +481,16 @@ cudaError_t launch_project_bf16_tc(const ProjectArgs& a, cudaStream_t stream, in
 // every slot it reads), so it is never cleared.
 static __device__ __align__(256) float g_fixed_ws[kFixedProjectWorkspaceBytes / sizeof(float)];
 
-namespace {
-std::mutex g_fixed_ws_mu;
-float* g_fixed_ws_ptr[64] = {};
-}  // namespace
-
-// Device address of g_fixed_ws on the current device.  The first call on a
-// device looks it up (cudaGetSymbolAddress, with that device current) and
-// caches it; the name itself is only a host-side stand-in.
+// Device address of g_fixed_ws in the current context.  Looked up on every
+// call (cudaGetSymbolAddress, with the device current) and never cached: after
+// cudaDeviceReset, or in another context on the same device, the array lives
+// at a new address, and a cached one would be stale.  The name itself is only
+// a host-side stand-in, never a device address.
 cudaError_t fixed_project_workspace(float** ptr) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_ws);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_fixed_ws_mu);
-    if (g_fixed_ws_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fixed_ws);
-        if (e != cudaSuccess) return e;
-        g_fixed_ws_ptr[dev] = static_cast<float*>(p);
-    }
-    *ptr = g_fixed_ws_ptr[dev];
+    *ptr = static_cast<float*>(p);
     return cudaSuccess;
 }
 

@@ -185,9 +185,11 @@ int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const 
  *   - Shapes that need more than 8 MiB of workspace (see
  *     dflash2_project_workspace_bytes; e.g. more than 4096 rows at R = 128 on
  *     152 SMs) return DF2_ERR_UNSUPPORTED and launch nothing.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress, with the device current); nothing is cached, so
+ *     the address stays right after cudaDeviceReset or in another context.
+ *     The first call on a device may load the library's device code: make it
+ *     before any stream capture.
  *   - Every call on a device uses the same array, so calls that overlap on the
  *     GPU (different streams, or different host threads) race and give wrong
  *     results; serialise them.  The array keeps the last call's contents;
@@ -287,6 +289,22 @@ int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edge
                   const int32_t* best_slot, const int32_t* start_slot, int S, int n, int K,
                   float p_min, int32_t* tokens, float* probs, int32_t* length, int32_t* err_flag,
                   void* stream);
+
+/*
+ * Measurement aid (no counterpart in the DFlash2 pull request): the rate at
+ * which this GPU gathers random rows, the bound the edge kernel's codebook
+ * gathers work against.  For i < n_ids:
+ *   out[i] = XOR of the 32-bit words of row ids[i] of table
+ * where table is [rows, row_bytes] bytes and an id outside [0, rows) is
+ * clamped into range.  Reads every gathered byte once; writes 4 bytes per id.
+ *   table  device memory, rows * row_bytes bytes, 16-byte aligned
+ *   ids    [n_ids] int32 device;  out [n_ids] uint32 device, disjoint from both
+ * n_ids == 0 launches nothing.
+ * INVALID_ARG: NULL pointer; rows <= 0; n_ids < 0; row_bytes not a power of
+ * two in [16, 1024]; misalignment; out overlapping table or ids.
+ */
+int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const int32_t* ids,
+                         int n_ids, uint32_t* out, void* stream);
 
 /*
  * Reads and clears the library's device-side fault word for the current

@@ -220,3 +220,18 @@ def _dpred(L, x=P[0], hist=P[1], base=P[2], wc=P[3], out=P[4], S=2, n=8, C=64, T
 def test_dynconv_predicted_validation(L, kw, code):
     assert _dpred(L, **kw) == code
     assert L.dflash2_last_error()
+
+
+def _probe(L, tb=P[0], rows=1000, rb=256, ids=P[1], n=64, out=P[2]):
+    return L.dflash2_probe_gather(tb, rows, rb, ids, n, out, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(tb=NULL), 1), (dict(ids=NULL), 1), (dict(out=NULL), 1), (dict(rows=0), 1),
+    (dict(n=-1), 1), (dict(rb=8), 1), (dict(rb=96), 1), (dict(rb=2048), 1),
+    (dict(tb=ctypes.c_void_p(0x10000004)), 1),
+    (dict(out=P[0]), 1),                       # out inside the table
+])
+def test_probe_gather_validation(L, kw, code):
+    assert _probe(L, **kw) == code
+    assert L.dflash2_last_error()

@@ -452,7 +452,8 @@ def test_chain_cut_closed_forms():
     np.testing.assert_allclose(pc, 1.0 / K, rtol=1e-12)
     _, p1, L1k = oracle.chain(ids[:, :, :1], un[:, :, :1], e[:, :, :1, :1],
                               np.zeros((S, n - 1, 1), np.int32), 1.0)
-    np.testing.assert_allclose(p1, 1.0) and np.testing.assert_array_equal(L1k, n)
+    np.testing.assert_allclose(p1, 1.0)
+    np.testing.assert_array_equal(L1k, n)
     # one position: only p0
     t, p, L = oracle.chain(ids[:, :1], un[:, :1], None, None, 0.5)
     assert t.shape == (S, 1) and np.all(L == (p[:, 0] >= 0.5))
