@@ -71,6 +71,8 @@ def _args():
                     help="oracle time the reference arm spreads over warm-up and timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the steps of the other four workloads")
     return ap.parse_args()
 
 
@@ -365,15 +367,25 @@ def _call(f, a, L):
         raise RuntimeError(L.dflash2_last_error().decode())
 
 
-def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
+def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50, ends_only=False):
     """K steps replayed from CUDA graphs.  Each step: L2 flush, then the calls in
     order, with a timing event (recorded as a graph node) before the first call
-    and after every call.  Returns, per call, the list of per-step times (ms)."""
+    and after every call.  Returns, per call, the list of per-step times (ms).
+    With ends_only the events bracket the whole step (one before the first call,
+    one after the last) and a single list of step times is returned."""
     import ctypes
 
     import torch
     sp = ctypes.c_void_p(stream.cuda_stream)
     nc = len(calls)
+    if ends_only:
+        seq = calls
+
+        def run_all():
+            for f, a in seq:
+                _call(f, a, L)
+        calls = [(None, run_all)]
+        nc = 1
     times = [[] for _ in range(nc)]
     done = 0
     graphs = {}
@@ -392,7 +404,10 @@ def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
                     for j, (f, a) in enumerate(calls):
                         if record_ext(ctypes.c_void_p(ev[m][j].cuda_event), sp, 1):
                             raise RuntimeError("event record in capture failed")
-                        _call(f, a, L)
+                        if f is None:
+                            a()
+                        else:
+                            _call(f, a, L)
                     if record_ext(ctypes.c_void_p(ev[m][nc].cuda_event), sp, 1):
                         raise RuntimeError("event record in capture failed")
             graphs[M] = (g, ev)
@@ -403,23 +418,122 @@ def _timed_graph(K, stream, flush, calls, record_ext, L, per_graph=50):
             for j in range(nc):
                 times[j].append(e[j].elapsed_time(e[j + 1]))
         done += M
-    return times
+    return times[0] if ends_only else times
 
 
-def _timed_eager(K, stream, flush, calls, L):
+def _timed_eager(K, stream, flush, calls, L, ends_only=False):
     """K eagerly launched steps (fallback when graph timing events are unavailable)."""
     import torch
-    nc = len(calls)
+    nc = 1 if ends_only else len(calls)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(K)]
     torch.cuda._sleep(20_000_000)  # let the host queue ahead of the device
     for k in range(K):
         flush.zero_()
         for j, (f, a) in enumerate(calls):
-            ev[k][j].record(stream)
+            if not ends_only or j == 0:
+                ev[k][0 if ends_only else j].record(stream)
             _call(f, a, L)
         ev[k][nc].record(stream)
     stream.synchronize()
-    return [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nc)]
+    t = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(nc)]
+    return t[0] if ends_only else t
+
+
+def _timer(stream, record_ext, L):
+    """timer(K, flush, calls, ends_only=False): the graph timer when timing events
+    can be recorded inside a capture, else eager launches."""
+    def timer(K, flush, calls, ends_only=False):
+        if record_ext is not None:
+            return _timed_graph(K, stream, flush, calls, record_ext, L, ends_only=ends_only)
+        return _timed_eager(K, stream, flush, calls, L, ends_only=ends_only)
+    return timer
+
+
+def _select_fused(L, w):
+    """Whether dflash2_select runs these shapes as one kernel (dflash2_select_plan)."""
+    import ctypes
+    out = (ctypes.c_int * 4)()
+    code = 1 if w.dtype == "bf16" else 0
+    if L.dflash2_select_plan(w.S_sel, w.n_sel, w.d, w.K, w.R, code, out):
+        raise RuntimeError(L.dflash2_last_error().decode())
+    return {"fused": bool(out[0]), "cluster_size": out[1], "clusters": out[2],
+            "rows_per_block": out[3]}
+
+
+def workload_leg(name, dev, stream, flush, timer, L, steps):
+    """The step (dynconv + select) of another workload: the whole step between two
+    events, and each call on its own, L2 flushed before every step."""
+    import ctypes
+
+    import torch
+
+    from dflash2_draft_head_gb300 import synth
+    w = _workload(name)
+    bt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    ci = synth.conv_inputs(w)
+    cb = synth.codebooks(w)
+    si = synth.selector_inputs(w)
+
+    def d(t, dt=bt):
+        return t.to(dt).to(dev).contiguous()
+    x, hist, base, delta = d(ci["x"]), d(ci["hist"]), d(ci["base"]), d(ci["delta"])
+    h, W, A, B = d(si["h"]), d(cb["W"]), d(cb["A"]), d(cb["B"])
+    ids, un = si["cand_ids"].to(dev), si["unary"].to(dev)
+    del ci, cb, si
+    out = torch.empty((w.S, w.n, w.C), dtype=bt, device=dev)
+    P = w.S_sel * w.n_sel
+    E = w.S_sel * max(w.n_sel - 1, 0)
+    u = torch.empty((P, w.R), dtype=torch.float32, device=dev)
+    slot = torch.empty((max(E, 1), w.K), dtype=torch.int32, device=dev)
+    score = torch.empty((max(E, 1), w.K), dtype=torch.float32, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    vp = ctypes.c_void_p
+    sp = vp(stream.cuda_stream)
+    code = 1 if w.dtype == "bf16" else 0
+
+    def ptr(t):
+        return vp(t.data_ptr())
+    conv_args = (ptr(x), ptr(hist), ptr(base), ptr(delta), ptr(out), w.S, w.n, w.C, w.T, w.G,
+                 code, code, sp)
+    sel_args = (ptr(h), ptr(W), ptr(ids), ptr(A), ptr(B), ptr(un), w.S_sel, w.n_sel, w.d, w.K,
+                w.R, w.V, code, ptr(u), None, ptr(slot), ptr(score), ptr(flag), sp)
+    calls = [(L.dflash2_dynconv, conv_args), (L.dflash2_select, sel_args)]
+    for _ in range(3):
+        flush.zero_()
+        for f, a in calls:
+            _call(f, a, L)
+    torch.cuda.synchronize()
+    t_step = timer(steps, flush, calls, ends_only=True)
+    t_conv, t_sel = timer(steps, flush, calls)
+    # the two-kernel selector on the same shapes (what select runs when not fused)
+    proj_args = (ptr(h), ptr(W), ptr(u), P, w.d, w.R, code, sp)
+    edge_args = (ptr(ids), ptr(u), ptr(A), ptr(B), ptr(un), w.S_sel, w.n_sel, w.K, w.R, w.V, code,
+                 None, ptr(slot), ptr(score), ptr(flag), sp)
+    t_pair = timer(steps, flush, [(L.dflash2_project, proj_args), (L.dflash2_edges, edge_args)],
+                   ends_only=True)
+    torch.cuda.synchronize()
+    if int(flag.item()) != 0:
+        raise RuntimeError(f"device error flag set in the {name} leg")
+    hbm = _peaks()[0]
+    conv_b, proj_b, proj_f, edge_b = _bytes(w)
+    step_us = 1000.0 * statistics.median(t_step)
+    conv_us = 1000.0 * statistics.median(t_conv)
+    sel_us = 1000.0 * statistics.median(t_sel)
+    plan = _select_fused(L, w)
+    return {
+        "dtype": w.dtype, "steps": steps, "S": w.S, "n": w.n, "C": w.C, "T": w.T, "G": w.G,
+        "R": w.R, "V": w.V, "K": w.K, "selector_S": w.S_sel, "selector_n": w.n_sel,
+        "step_us": step_us, "positions_per_s": w.S * w.n / (step_us * 1e-6),
+        "step_bytes": conv_b + proj_b + edge_b,
+        "step_frac_hbm": (conv_b + proj_b + edge_b) / step_us / 1e3 / hbm,
+        "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
+                    "frac_hbm": conv_b / conv_us / 1e3 / hbm},
+        "select": {"us": sel_us, "bytes": proj_b + edge_b, "GB/s": (proj_b + edge_b) / sel_us / 1e3,
+                   "frac_hbm": (proj_b + edge_b) / sel_us / 1e3 / hbm,
+                   "TFLOP/s_project": proj_f / sel_us / 1e6, "plan": plan,
+                   "project_then_edges_us": 1000.0 * statistics.median(t_pair)},
+        "timing": "median of per-step event intervals; L2 flushed before every step",
+    }
 
 
 def gather_ceiling(w, dev, stream, flush, record_ext, L, steps):
@@ -437,29 +551,41 @@ def gather_ceiling(w, dev, stream, flush, record_ext, L, steps):
     gather_bytes = 2 * E * w.K * w.R * b
     if gather_bytes == 0:
         return None
-    table = torch.zeros(table_bytes // 4, dtype=torch.int32, device=dev)
     g = torch.Generator().manual_seed(4242)
     out = {"table_bytes": table_bytes, "gathered_bytes": gather_bytes,
-           "note": "read-only random gathers at uniform ids (4 bytes written per row); the "
-                   "edge kernel reads R*b-byte codebook rows this way"}
+           "note": "read-only random gathers at uniform ids (4 bytes written per row), one CTA "
+                   "per SM with its ids staged on chip and 16-byte cp.async into a shared-memory "
+                   "ring: the way the edge kernels read R*b-byte codebook rows"}
     sp = ctypes.c_void_p(stream.cuda_stream)
+    f = L.dflash2_probe_gather
+    big = torch.zeros(8 * table_bytes // 4, dtype=torch.int32, device=dev)
     for rb in (128, 256, 512):
-        rows = table_bytes // rb
-        n_ids = gather_bytes // rb
-        ids = torch.randint(0, rows, (n_ids,), generator=g, dtype=torch.int32).to(dev)
-        res = torch.empty((n_ids,), dtype=torch.int32, device=dev)
-        args = (ctypes.c_void_p(table.data_ptr()), rows, rb, ctypes.c_void_p(ids.data_ptr()),
-                n_ids, ctypes.c_void_p(res.data_ptr()), sp)
-        f = L.dflash2_probe_gather
-        _call(f, args, L)
-        if record_ext is not None:
-            t = _timed_graph(steps, stream, flush, [(f, args)], record_ext, L)[0]
-        else:
-            t = _timed_eager(steps, stream, flush, [(f, args)], L)[0]
-        us = 1000.0 * statistics.median(t)
-        out[f"rows_{rb}B"] = {"us": us, "GB/s": (n_ids * (rb + 4)) / us / 1e3,
-                              "frac_hbm": (n_ids * (rb + 4)) / us / 1e3 / _peaks()[0]}
-    del table
+        res_t = {}
+        for mult in (1, 8):  # the step's gather volume, and eight times it from a table 8x larger
+            table = big[: mult * table_bytes // 4]
+            rows = mult * table_bytes // rb
+            n_ids = mult * gather_bytes // rb
+            ids = torch.randint(0, rows, (n_ids,), generator=g, dtype=torch.int32).to(dev)
+            res = torch.empty((n_ids,), dtype=torch.int32, device=dev)
+            args = (ctypes.c_void_p(table.data_ptr()), rows, rb, ctypes.c_void_p(ids.data_ptr()),
+                    n_ids, ctypes.c_void_p(res.data_ptr()), sp)
+            _call(f, args, L)
+            if record_ext is not None:
+                t = _timed_graph(steps, stream, flush, [(f, args)], record_ext, L)[0]
+            else:
+                t = _timed_eager(steps, stream, flush, [(f, args)], L)[0]
+            res_t[mult] = (1000.0 * statistics.median(t), n_ids * (rb + 4))
+            del ids, res
+        (us1, b1), (us8, b8) = res_t[1], res_t[8]
+        marginal = (b8 - b1) / (us8 - us1) / 1e3
+        out[f"rows_{rb}B"] = {"us": us1, "GB/s": b1 / us1 / 1e3,
+                              "frac_hbm": b1 / us1 / 1e3 / _peaks()[0],
+                              "us_8x": us8, "marginal_GB/s": marginal,
+                              "marginal_frac_hbm": marginal / _peaks()[0]}
+    out["marginal"] = ("marginal rate = (8x bytes - 1x bytes) / (8x time - 1x time), the 8x "
+                       "volume drawn from a table 8x larger (beyond L2): the cold gather rate "
+                       "with the launch and timing-event cost taken out")
+    del big
     return out
 
 
@@ -546,23 +672,22 @@ def main():
     K = args.steps
     gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     record_ext = None if args.no_graph else _event_record_external()
+    timer = _timer(stream, record_ext, L)
+    mode = "cuda-graph" if record_ext is not None else "eager"
+    calls = [(f_conv, conv_args), (f_sel, sel_args)]
     with ClockSampler(gpu_uuid) as clk:
         barrier()
         wall0 = time.perf_counter()
-        calls = [(f_conv, conv_args), (f_sel, sel_args)]
-        if record_ext is not None:
-            t_conv, t_sel = _timed_graph(K, stream, flush, calls, record_ext, L)
-            mode = "cuda-graph"
-        else:
-            t_conv, t_sel = _timed_eager(K, stream, flush, calls, L)
-            mode = "eager"
+        # the timed steps: one event before the step's first call, one after its last
+        t_step = timer(K, flush, calls, ends_only=True)
         barrier()
         wall = time.perf_counter() - wall0
-    t_step = [a + b for a, b in zip(t_conv, t_sel)]
-    # per-kernel breakdown of the selector (separate, smaller loop: project and
-    # edges each bracketed by events, so the programmatic overlap between them
-    # inside the composite call is absent here)
     K_iso = max(min(K, 200), 1)
+    # the same step with an event between the two calls: each call's share
+    t_conv, t_sel = timer(K_iso, flush, calls)
+    sel_plan = _select_fused(L, w0)
+    # the projection and the edge kernel on their own (the path dflash2_select
+    # takes for shapes the one-kernel selector does not run)
     iso_calls = [(f_proj, proj_args), (f_edge, edge_args)]
     if record_ext is not None:
         t_proj, t_edge = _timed_graph(K_iso, stream, flush, iso_calls, record_ext, L)
@@ -656,6 +781,15 @@ def main():
                          + w.n_sel * 8 + 4)
     del e_full
     gather = gather_ceiling(w, dev, stream, flush, record_ext, L, K_iso)
+    # the other workloads' steps (rank 0 of a single-GPU run)
+    workloads = {}
+    if world == 1 and not args.no_workloads:
+        from dflash2_draft_head_gb300.workloads import WORKLOADS
+        for wk in WORKLOADS:
+            if wk.name != w0.name:
+                workloads[wk.name] = workload_leg(wk.name, dev, stream, flush, timer, L,
+                                                  K_iso)
+                torch.cuda.empty_cache()
     total_ms = max_over_ranks(sum(t_step), world, dev)
     if int(flag.item()) != 0 or df2.take_device_faults() != 0:
         raise RuntimeError("device error flag set during the benchmark")
@@ -732,11 +866,22 @@ def main():
     sel_us = 1000.0 * statistics.mean(t_sel)
     proj_us = 1000.0 * statistics.mean(t_proj)
     edge_us = 1000.0 * statistics.mean(t_edge)
-    achieved = conv_b / (conv_us * 1e-6) / 1e9
-    src_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
-                                               "dynconv.cu"), "rb").read()).hexdigest()
-    tr = TRAFFIC.get((w.name, "dynconv"))
-    traffic = tr["bytes"] if tr and tr["sha"] == src_sha else None
+
+    def _traffic(kernel, fname):
+        sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc", fname),
+                                  "rb").read()).hexdigest()
+        tr = TRAFFIC.get((w.name, kernel))
+        return tr["bytes"] if tr and tr["sha"] == sha else None
+    # the dominant kernel of the step: the call with the larger share of its time
+    if sel_us >= conv_us:
+        dom = {"kernel": "dflash2_select" + ("" if sel_plan["fused"] else " (project + edges)"),
+               "bytes": proj_b + edge_b, "us": sel_us,
+               "traffic": _traffic("select", "select.cu") if sel_plan["fused"] else None}
+    else:
+        dom = {"kernel": "dflash2_dynconv", "bytes": conv_b, "us": conv_us,
+               "traffic": _traffic("dynconv", "dynconv.cu")}
+    achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
+    traffic = _traffic("dynconv", "dynconv.cu")
     tk_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
                                               "topk.cu"), "rb").read()).hexdigest()
     tr = TRAFFIC.get((w.name, "topk"))
@@ -750,12 +895,25 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": _config(w0, world),
-        "roofline": {"bound": "hbm", "kernel": "dflash2_dynconv", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
-                     "bytes_per_launch": conv_b, "peak_source": src},
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": dom["traffic"], "bytes_per_launch": dom["bytes"],
+                     "us_per_launch": dom["us"], "peak_source": src,
+                     "timing": "live, an event between the step's two calls"},
+        "roofline_step": {"bound": "hbm", "bytes_per_step": conv_b + proj_b + edge_b,
+                          "us_per_step": 1000.0 * total_ms / K,
+                          "achieved": (conv_b + proj_b + edge_b) / (1000.0 * total_ms / K) / 1e3,
+                          "peak": hbm, "unit": "GB/s",
+                          "frac": (conv_b + proj_b + edge_b) / (1000.0 * total_ms / K) / 1e3 / hbm},
         "roofline_all": {
             "dynconv": {"bound": "hbm", "achieved": conv_b / conv_us / 1e3, "peak": hbm,
-                        "unit": "GB/s", "frac": conv_b / conv_us / 1e3 / hbm},
+                        "unit": "GB/s", "frac": conv_b / conv_us / 1e3 / hbm,
+                        "traffic": traffic},
+            "select": {"bound": "hbm", "achieved": (proj_b + edge_b) / sel_us / 1e3, "peak": hbm,
+                       "unit": "GB/s", "frac": (proj_b + edge_b) / sel_us / 1e3 / hbm,
+                       "traffic": dom["traffic"] if dom["kernel"] == "dflash2_select" else
+                       (_traffic("select", "select.cu") if sel_plan["fused"] else None),
+                       "plan": sel_plan},
             "project": {"bound": "hbm", "achieved": proj_b / proj_us / 1e3, "peak": hbm,
                         "unit": "GB/s", "frac": proj_b / proj_us / 1e3 / hbm,
                         "tensor_TFLOP/s": proj_f / proj_us / 1e6, "tensor_peak": tc,
@@ -778,7 +936,8 @@ def main():
             "select": {"us": sel_us, "bytes": proj_b + edge_b,
                        "GB/s": (proj_b + edge_b) / sel_us / 1e3,
                        "frac_hbm": (proj_b + edge_b) / sel_us / 1e3 / hbm,
-                       "note": "project + edges in one dflash2_select call (timed region)"},
+                       "plan": sel_plan,
+                       "note": "dflash2_select in the step (one kernel when plan.fused)"},
             "project": {"isolated": True, "steps": K_iso, "us": proj_us, "bytes": proj_b,
                         "warm_us": 1000.0 * statistics.mean(t_proj_warm),
                         "GB/s": proj_b / proj_us / 1e3,
@@ -804,11 +963,13 @@ def main():
                      "note": "not part of the timed step; candidate extraction before it"},
         },
         "gather_ceiling": gather,
+        "workloads": workloads,
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2,
                 "pipelining": "double-buffered inputs: step k+1's H2D copies (2 streams) overlap "
                               "step k's kernels"},
-        "gpu_launches": 3 * K,  # dynconv + project + edges per timed step
+        # dynconv + the selector (one kernel, or project + edges) per timed step
+        "gpu_launches": (2 if sel_plan["fused"] else 3) * K,
         "clocks": clk.summary(),
         "torch": torch.__version__,
         "inputs_sha256": _input_digests(host_in),

@@ -11,6 +11,6 @@ ggml-org/llama.cpp PR #27342, "spec : add DFlash2 support (local convolution
 """
 from .binding import (Dflash2Error, chain, dynconv, dynconv_predicted, edges, lib,  # noqa: F401
                       predict_delta, probe_gather, project, project_noalloc,
-                      project_workspace_bytes, select,
+                      project_workspace_bytes, select, select_plan,
                       take_device_faults, topk, version)
 from .build import build as build_library  # noqa: F401

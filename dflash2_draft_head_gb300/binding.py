@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.dflash2_chain.restype = i
             L.dflash2_topk.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.dflash2_topk.restype = i
+            L.dflash2_select_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+            L.dflash2_select_plan.restype = i
             L.dflash2_probe_gather.argtypes = [vp, ctypes.c_longlong, i, vp, i, vp, vp]
             L.dflash2_probe_gather.restype = i
             L.dflash2_take_device_faults.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -330,3 +332,12 @@ def probe_gather(table, row_bytes: int, ids, out=None):
     _check(lib().dflash2_probe_gather(_ptr(table), rows, int(row_bytes), _ptr(ids), n_ids,
                                       _ptr(out), _stream(ids.device)))
     return out
+
+
+def select_plan(S: int, n: int, d: int, K: int, R: int, dtype=torch.bfloat16) -> dict:
+    """How select() runs these shapes on the current device: {"fused": bool,
+    "cluster_size", "clusters", "rows_per_block"}."""
+    out = (ctypes.c_int * 4)()
+    _check(lib().dflash2_select_plan(S, n, d, K, R, _code(dtype), out))
+    return {"fused": bool(out[0]), "cluster_size": out[1], "clusters": out[2],
+            "rows_per_block": out[3]}

@@ -318,11 +318,43 @@ int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const 
     st = check_disjoint(uo, 1, others, 8);
     if (st != DF2_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == DF2_BF16 && df2::select_fused_supported(K, R, d, n)) {
+        df2::SelectArgs sa{h, W, cand_ids, A, B, unary, S, n, d, K, R, V, u_out, edges_out,
+                           best_slot, best_score, err_flag};
+        bool launched = false;
+        cudaError_t e = df2::launch_select_fused(sa, s, num_sms_of_current_device(),
+                                                 max_smem_optin_of_current_device(), &launched);
+        if (e != cudaSuccess) return cuda_fail(e, "select launch");
+        if (launched) return DF2_OK;
+    }
     st = run_project(h, W, u_out, S * n, d, R, dtype, s);
     if (st != DF2_OK) return st;
     // the projection only produces u_out and waited for everything before it
     return run_edges(cand_ids, u_out, A, B, unary, S, n, K, R, V, dtype, edges_out, best_slot,
                      best_score, err_flag, s, dtype == DF2_BF16 ? 1 : 0);
+}
+
+int dflash2_select_plan(int S, int n, int d, int K, int R, int dtype, int* plan_out) {
+    g_err[0] = 0;
+    if (plan_out == nullptr) return fail(DF2_ERR_INVALID_ARG, "select_plan: NULL plan_out");
+    if (S <= 0 || n <= 0 || d <= 0 || K <= 0 || R <= 0)
+        return fail(DF2_ERR_INVALID_ARG, "select_plan: S=%d n=%d d=%d K=%d R=%d must be positive",
+                    S, n, d, K, R);
+    if (!valid_dtype(dtype)) return fail(DF2_ERR_INVALID_ARG, "select_plan: bad dtype %d", dtype);
+    if ((long long)S * n > 0x7FFFFFFFLL)
+        return fail(DF2_ERR_UNSUPPORTED, "select_plan: S*n too large");
+    plan_out[0] = plan_out[1] = plan_out[2] = plan_out[3] = 0;
+    int cs = 0, nc = 0, mr = 0;
+    if (dtype == DF2_BF16 &&
+        df2::select_fused_plan(S, n, d, K, R, num_sms_of_current_device(),
+                               max_smem_optin_of_current_device(), &cs, &nc, &mr)) {
+        plan_out[0] = 1;
+        plan_out[1] = cs;
+        plan_out[2] = nc;
+        plan_out[3] = mr;
+    }
+    cudaGetLastError();  // planning queries leave no error behind
+    return DF2_OK;
 }
 
 int dflash2_project_noalloc(const void* h, const void* W, float* u, int P, int d, int R,
@@ -501,9 +533,9 @@ int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const
         return fail(DF2_ERR_INVALID_ARG, "probe_gather: NULL table, ids or out");
     if (rows <= 0 || n_ids < 0)
         return fail(DF2_ERR_INVALID_ARG, "probe_gather: rows=%lld n_ids=%d", rows, n_ids);
-    if (row_bytes < 16 || row_bytes > 1024 || (row_bytes & (row_bytes - 1)) != 0)
+    if (row_bytes < 16 || row_bytes > 512 || (row_bytes & (row_bytes - 1)) != 0)
         return fail(DF2_ERR_INVALID_ARG,
-                    "probe_gather: row_bytes=%d must be a power of two in [16, 1024]", row_bytes);
+                    "probe_gather: row_bytes=%d must be a power of two in [16, 512]", row_bytes);
     const Buf ins[2] = {{table, (size_t)rows * (size_t)row_bytes, "table"},
                         {ids, (size_t)n_ids * 4, "ids"}};
     const Buf outs[1] = {{out, (size_t)n_ids * 4, "out"}};
@@ -530,6 +562,8 @@ int dflash2_take_device_faults(int32_t* flags_out) {
     if (e == cudaSuccess) e = df2::take_topk_faults(&v2);
     v |= v2;
     if (e == cudaSuccess) e = df2::take_fused_faults(&v2);
+    v |= v2;
+    if (e == cudaSuccess) e = df2::take_select_faults(&v2);
     v |= v2;
     if (e != cudaSuccess) return cuda_fail(e, "take_device_faults");
     *flags_out = (int32_t)v;

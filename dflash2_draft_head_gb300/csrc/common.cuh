@@ -129,9 +129,36 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);
 // Reads and clears the top-K kernel's device fault word (synchronous).
 cudaError_t take_topk_faults(unsigned* flags);
 
+// The composite selector in one kernel (select.cu): bf16, K a power of two in
+// [4, 128], R in {64, 128, 256}, d % 8 == 0, n >= 2.
+struct SelectArgs {
+    const void* h;
+    const void* W;
+    const int32_t* cand_ids;
+    const void* A;
+    const void* B;
+    const float* unary;
+    int S, n, d, K, R, V;
+    float* u;
+    float* edges_out;
+    int32_t* best_slot;
+    float* best_score;
+    int32_t* err_flag;
+};
+bool select_fused_supported(int K, int R, int d, int n);
+// Sets *launched = false (and launches nothing) when no cluster layout fits the
+// shapes; the caller then runs the projection and the edge kernel separately.
+cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int num_sms,
+                                size_t max_smem, bool* launched);
+// Whether launch_select_fused runs for these shapes, and its cluster layout.
+bool select_fused_plan(int S, int n, int d, int K, int R, int num_sms, size_t max_smem,
+                       int* cluster_size, int* clusters, int* rows_per_block);
+// Reads and clears the fused selector's device fault word (synchronous).
+cudaError_t take_select_faults(unsigned* flags);
+
 // Measurement aid: random-row gather (probe.cu).  out[i] = XOR of the 32-bit
 // words of row ids[i] (ids clamped into [0, rows)); row_bytes a power of two
-// in [16, 1024].
+// in [16, 512].
 struct ProbeGatherArgs {
     const void* table;
     long long rows;

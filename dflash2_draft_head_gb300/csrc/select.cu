@@ -1,0 +1,887 @@
+// The composite candidate selector in one kernel: project(h) and the edge
+// scores with the per-predecessor argmax (ggml-org/llama.cpp PR #27342,
+// "spec : add DFlash2 support (local convolution + candidate selector)",
+// Overview, second formula):
+//   u      = h W^T                                  (each position's hidden, d -> R)
+//   e[p,c] = < A[id_p] (.) u[i], B[id_c] > + unary[i,c]   (p -> c into position i)
+//   best_slot / best_score = lowest slot reaching max_c e[p,c], and that max.
+//
+// Why one kernel: the projection streams h from HBM and the edge scores gather
+// codebook rows at random token ids; both are memory-bound, and the gathers do
+// not depend on u (only the gate A (.) u does).  Fused, the first edge tile's
+// gathers are in flight while h streams, u never goes back to HBM before the
+// gate, and the whole selector pays one launch.
+//
+// Decomposition (bf16; K a power of two in [4, 128]; R = 64, 128 or 256):
+//  - Positions are cut into row blocks of MR <= 128 consecutive rows, one per
+//    thread-block cluster of CS CTAs (one CTA per SM).  The cluster splits d:
+//    CTA r streams k-blocks [r*kb/CS, (r+1)*kb/CS) of its row block of h and
+//    of W through a TMA ring (128-byte swizzle) into tcgen05.mma (M = 128,
+//    N = R) with the fp32 partial in tensor memory.
+//  - The partial tiles are reduced through distributed shared memory: CTA r
+//    owns rows [r*MR/CS, (r+1)*MR/CS) of the block; after one cluster barrier
+//    every CTA pushes each owner's rows of its partial with one bulk
+//    shared-to-shared copy, the owner sums the CS partials in rank order
+//    (deterministic), writes its u rows to HBM (the caller's u_out) and keeps
+//    them in shared memory, and tells each sender that its buffer has been
+//    read (a remote mbarrier arrive the sender waits for only before it
+//    reuses that buffer).
+//  - CTA r then scores every transition INTO its own positions (transitions
+//    are numbered e = s*(n-1) + i-1, so a contiguous run of positions owns a
+//    contiguous run of transitions).  Tiles of 128/K transitions hold 128
+//    predecessor rows of A and 128 candidate rows of B (one edge stage per 128
+//    ranks).  8 gather warps copy the rows by token id with 16-byte cp.async
+//    straight into the tensor core's 128-byte-swizzle K-major layout; the
+//    first stage's copies are issued at kernel start, under the projection,
+//    and every later tile's rows are prefetched into L2 then.  Each gather
+//    thread later gates exactly the A chunks it copied itself (no hand-off):
+//    A (.) u in fp32, rounded to bf16, in place.  One thread issues
+//    tcgen05.mma (M = N = 128) into one of two tensor-memory accumulators; 4
+//    epilogue warps read back only each transition's K x K diagonal block,
+//    add unary, keep the running argmax (lowest slot on ties) and store.
+// Every wait on an mbarrier is bounded by the global timer; on a timeout the
+// kernel sets DF2_FLAG_TIMEOUT and runs to completion without hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "dflash2.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace df2 {
+
+// Device-side fault word of the fused selector (read by dflash2_take_device_faults).
+__device__ unsigned int g_select_fault = 0;
+
+namespace {
+
+constexpr int SEL_THREADS = 512;   // 16 warps
+constexpr int SEL_GTHREADS = 256;  // warps 8..15: gather + gate
+constexpr int EROWS = 128;         // rows of an edge operand tile
+constexpr int KB_OP = EROWS * 128; // one 64-rank k-block of one edge operand (16 KB)
+constexpr int HTILE = 128 * 128;   // one 64-column k-block of 128 rows of h (16 KB)
+constexpr int EACC = 256;          // first tensor-memory column of the edge accumulators
+
+struct SelParams {
+    const int32_t* cand_ids;
+    const float* unary;
+    const __nv_bfloat16* A;
+    const __nv_bfloat16* B;
+    float* u;
+    float* edges_out;
+    int32_t* best_slot;
+    float* best_score;
+    int32_t* err_flag;
+    int S, n, K, R, V, P;
+    int log2K;
+    int CS;            // CTAs per cluster (split of d)
+    int MR;            // rows per row block
+    int nrb;           // row blocks
+    int kblocks;       // 64-column k-blocks of d
+    int own_max;       // most rows a CTA owns after the reduction
+    int pstages;       // projection TMA stages
+    int estages;       // edge stages: stage 0 is region E, the others live in region P
+    int nkb_e;         // 64-rank k-blocks per edge stage (1 or 2)
+    int nhalf;         // edge stages per tile (R / (64 * nkb_e))
+    int drain_stage;   // first edge stage that overlaps the outgoing partial buffer
+    uint32_t pstage_bytes;  // HTILE + R * 128
+    uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
+    uint32_t off_P, off_out, off_U, off_lr, off_ids, off_bar;  // off_out is relative to region P
+    uint32_t red_stride;    // floats per row of the partial buffers (R + 4)
+};
+
+constexpr int LR_SLOTS = 4;  // tiles whose local u-row table is kept (ring)
+
+__device__ __forceinline__ int checked_id(int id, int V, bool& bad) {
+    if (id < 0 || id >= V) {
+        bad = true;
+        return id < 0 ? 0 : V - 1;
+    }
+    return id;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most `pending` of this thread's cp.async groups are outstanding.
+__device__ __forceinline__ void cp_wait_pending(int pending) {
+    switch (pending) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    }
+}
+
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Number of transitions (s, i >= 1) whose target position lies before position q.
+__device__ __forceinline__ int trans_before(int q, int n) {
+    const int s = q / n;
+    const int i = q - s * n;
+    return s * (n - 1) + (i > 0 ? i - 1 : 0);
+}
+
+__global__ void __launch_bounds__(SEL_THREADS, 1)
+    select_fused_kernel(const __grid_constant__ CUtensorMap tmH,
+                        const __grid_constant__ CUtensorMap tmW, const SelParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sE = smem_u32(smem);
+    const uint32_t sP = sE + p.off_P;
+    const float* recv_f = reinterpret_cast<const float*>(smem + p.off_P);        // [CS-1][own_max][R+4]
+    float* out_f = reinterpret_cast<float*>(smem + p.off_P + p.off_out);        // [MR][R+4]
+    float* uslice = reinterpret_cast<float*>(smem + p.off_U);                   // [own][R]
+    int* lr_ring = reinterpret_cast<int*>(smem + p.off_lr);                     // [LR_SLOTS][32]
+    int* id_ring = reinterpret_cast<int*>(smem + p.off_ids);                    // [2][256]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * p.pstages;
+    const uint32_t accum = empty0 + 8 * p.pstages;
+    const uint32_t recv = accum + 8;
+    const uint32_t drained = recv + 8;
+    const uint32_t ready0 = drained + 8;
+    const uint32_t sfree0 = ready0 + 8 * p.estages;
+    const uint32_t tfull0 = sfree0 + 8 * p.estages;
+    const uint32_t tempty0 = tfull0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.pstages + 3 + 2 * p.estages + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int CS = p.CS;
+    const int rank = (int)cluster_ctarank();
+    const int cluster_id = blockIdx.x / CS;
+    const int nclusters = gridDim.x / CS;
+    const int K = p.K;
+    const int R = p.R;
+    const int TP = EROWS >> p.log2K;  // transitions per tile
+    const int nm1 = p.n - 1;
+    const int gtid = tid - 8 * 32;    // gather thread index (>= 0 in warps 8..15)
+    const uint32_t row_bytes = p.red_stride * 4u;
+
+    auto init_edge_bars = [&]() {
+        for (int i = 0; i < p.estages; ++i) {
+            mbar_init(ready0 + 8 * i, SEL_GTHREADS);
+            mbar_init(sfree0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull0 + 8 * i, 1);
+            mbar_init(tempty0 + 8 * i, 128);
+        }
+    };
+    if (tid == 0) {
+        prefetch_tmap(&tmH);
+        prefetch_tmap(&tmW);
+        for (int i = 0; i < p.pstages; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, 1);
+        }
+        mbar_init(accum, 1);
+        mbar_init(recv, 1);
+        mbar_init(drained, CS > 1 ? CS - 1 : 1);
+        init_edge_bars();
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // Launched as a programmatic dependent: the set-up above overlapped the
+    // previous kernel; no input is read before it has completed.
+    griddep_wait();
+    griddep_launch_dependents();
+
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (*abort_flag) return;
+        if (!mbar_wait_bounded(bar, parity, kWaitNs)) *abort_flag = 1;
+    };
+    auto estage_base = [&](int st) -> uint32_t {
+        return st == 0 ? sE : sP + (uint32_t)(st - 1) * p.estage_bytes;
+    };
+
+    // A gather thread's place in an edge stage never changes: chunk ch (16 bytes)
+    // of k-block kb of rows r0, r0 + row_step, ...; so the 128-byte swizzle of
+    // its chunks is one constant (row_step is a multiple of 8).
+    const int log2cpr = p.nkb_e == 2 ? 4 : 3;          // 16-byte chunks per row: 16 or 8
+    const int g_r0 = gtid >> log2cpr;
+    const int g_kb = (gtid >> 3) & (p.nkb_e - 1);
+    const int g_ch = gtid & 7;
+    const int row_step = SEL_GTHREADS >> log2cpr;      // 16 or 32
+    const int g_col = g_kb * 64 + g_ch * 8;            // rank offset within the stage's ranks
+    const uint32_t g_off = (uint32_t)(g_kb * KB_OP + g_r0 * 128 + ((g_ch ^ (g_r0 & 7)) << 4));
+
+    bool bad = false;
+    int pit = 0;  // projection k-block iterations so far (ring phase)
+    int rbi = 0;  // row blocks so far (accumulator / receive phase)
+    for (int rb = cluster_id; rb < p.nrb; rb += nclusters, ++rbi) {
+        const int row0 = rb * p.MR;
+        const int rows = min(p.MR, p.P - row0);
+        const int kb0 = (int)((long long)rank * p.kblocks / CS);
+        const int kb1 = (int)((long long)(rank + 1) * p.kblocks / CS);
+        const int o_lo = rank * rows / CS;
+        const int o_hi = (rank + 1) * rows / CS;
+        const int pa = row0 + o_lo;  // this CTA's positions [pa, pb)
+        const int pb = row0 + o_hi;
+        const int e_lo = trans_before(pa, p.n);
+        const int e_hi = trans_before(pb, p.n);
+        const int ntile = (e_hi - e_lo + TP - 1) / TP;
+        const int nunits = ntile * p.nhalf;
+        bool drained_ok = CS == 1;  // this row block's outgoing partial no longer read
+
+        // ---- ids of tile t for gather slot g: g < 128 the predecessor id of row
+        //      g (from position i-1), else the candidate id of row g-128
+        auto id_of = [&](int t, int g) -> int {
+            if (t >= ntile) return -1;
+            const int r = g & (EROWS - 1);
+            const int e0 = e_lo + t * TP;
+            if ((r >> p.log2K) >= min(TP, e_hi - e0)) return -1;
+            const int e = e0 + (r >> p.log2K);
+            const int s = e / nm1;
+            const int i = e - s * nm1 + 1 - (g < EROWS ? 1 : 0);
+            return checked_id(p.cand_ids[((size_t)s * p.n + i) * K + (r & (K - 1))], p.V, bad);
+        };
+        auto load_id = [&](int t) -> int {
+            const int id = id_of(t, gtid);
+            return id < 0 ? 0 : id;
+        };
+        int id_next = warp >= 8 ? load_id(0) : 0;
+
+        // ---- gather issue of edge unit j (tile j / nhalf, rank half j % nhalf).
+        //      A new tile's ids go to slot t & 1 of the id ring and its local u-row
+        //      table to slot t % LR_SLOTS; the named barrier makes both visible to
+        //      all gather threads (and shows every slot being overwritten has
+        //      been read by all of them); then the next tile's id is loaded while
+        //      this one's rows are in flight.
+        auto issue_unit = [&](int j) {
+            const int st = j % p.estages;
+            const int t = j / p.nhalf;
+            const int half = j - t * p.nhalf;
+            const int e0 = e_lo + t * TP;
+            const int cnt = min(TP, e_hi - e0);
+            int* ids = id_ring + (t & 1) * 2 * EROWS;
+            if (half == 0) {
+                ids[gtid] = id_next;
+                if (gtid < cnt) {
+                    const int e = e0 + gtid;
+                    const int s = e / nm1;
+                    lr_ring[(t % LR_SLOTS) * 32 + gtid] = s * p.n + (e - s * nm1) + 1 - pa;
+                }
+                named_bar_sync(1, SEL_GTHREADS);
+                id_next = load_id(t + 1);
+            }
+            if (j >= p.estages)  // the stage's previous unit has been consumed by the MMA
+                wait(sfree0 + 8 * st, (uint32_t)((j / p.estages) - 1) & 1u);
+            if (st >= p.drain_stage && !drained_ok) {  // the outgoing partial has been sent
+                wait(drained, (uint32_t)rbi & 1u);
+                drained_ok = true;
+            }
+            const int rows_valid = cnt << p.log2K;
+            const uint32_t sb = estage_base(st) + g_off;
+            const uint32_t sbB = sb + (uint32_t)(p.nkb_e * KB_OP);
+            const int col = half * 64 * p.nkb_e + g_col;
+            if (!*abort_flag) {
+                for (int k = 0, row = g_r0; row < rows_valid; ++k, row += row_step) {
+                    const uint32_t o = (uint32_t)(k * row_step * 128);
+                    cp_async16(sb + o, p.A + (size_t)ids[row] * R + col);
+                    cp_async16(sbB + o, p.B + (size_t)ids[EROWS + row] * R + col);
+                }
+            }
+            cp_commit();
+        };
+
+        // ---- gate of edge unit j in place: each thread its own A chunks,
+        //      A (.) u in fp32, rounded to bf16
+        auto gate_unit = [&](int j) {
+            const int st = j % p.estages;
+            const int t = j / p.nhalf;
+            const int half = j - t * p.nhalf;
+            const int rows_valid = min(TP, e_hi - (e_lo + t * TP)) << p.log2K;
+            const uint32_t sb = estage_base(st) + g_off;
+            const int col = half * 64 * p.nkb_e + g_col;
+            const int* lr = lr_ring + (t % LR_SLOTS) * 32;
+            if (*abort_flag) return;
+            for (int k = 0, row = g_r0; row < rows_valid; ++k, row += row_step) {
+                const float4* ur =
+                    reinterpret_cast<const float4*>(uslice + (size_t)lr[row >> p.log2K] * R + col);
+                const float4 u0 = ur[0];
+                const float4 u1 = ur[1];
+                const uint32_t off = sb + (uint32_t)(k * row_step * 128);
+                const uint4 a = lds_v4(off);
+                const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
+                const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
+                uint4 g;
+                g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
+                g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
+                g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
+                g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
+                st_shared_v4(off, g);
+            }
+        };
+
+        // ================= phase A: projection of the row block (+ early gathers)
+        if (warp == 0) {
+            if (lane == 0) {  // TMA producer
+                const uint32_t tx = (uint32_t)p.MR * 128u + (uint32_t)R * 128u;
+                int it = pit;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int st = it % p.pstages;
+                    wait(empty0 + 8 * st, (((uint32_t)(it / p.pstages)) & 1u) ^ 1u);
+                    if (*abort_flag) continue;
+                    const uint32_t fb = full0 + 8 * st;
+                    const uint32_t dst = sP + (uint32_t)st * p.pstage_bytes;
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_2d(dst, &tmH, fb, kb * 64, row0);
+                    tma_load_2d(dst + HTILE, &tmW, fb, kb * 64, 0);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1) {
+            if (lane == 0) {  // MMA issuer
+                const uint32_t idesc = idesc_bf16_f32(128, R);
+                int it = pit;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int st = it % p.pstages;
+                    wait(full0 + 8 * st, ((uint32_t)(it / p.pstages)) & 1u);
+                    tc_fence_after();
+                    const uint32_t a0 = sP + (uint32_t)st * p.pstage_bytes;
+                    const uint32_t b0 = a0 + HTILE;
+                    if (!*abort_flag) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_bf16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                        idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty0 + 8 * st);
+                }
+                tc_commit(accum);
+            }
+            __syncwarp();
+        } else if (warp >= 8) {
+            if (nunits > 0) issue_unit(0);  // region E is free: start the first gathers now
+            // The later tiles' rows cannot land in shared memory yet (region P is
+            // the projection's ring): ask L2 for them now, so that their gathers
+            // in phase D hit L2 while HBM serves this phase.
+            if (!*abort_flag) {
+                const int lines = R / 64;  // 128-byte lines per bf16 row
+#pragma unroll 2
+                for (int qd = gtid; qd < (ntile - 1) * 2 * EROWS; qd += SEL_GTHREADS) {
+                    const int id = id_of(1 + qd / (2 * EROWS), qd & (2 * EROWS - 1));
+                    if (id < 0) continue;
+                    const __nv_bfloat16* row = ((qd & (2 * EROWS - 1)) < EROWS ? p.A : p.B) + (size_t)id * R;
+                    for (int l = 0; l < lines; ++l) prefetch_l2_last(row + l * 64);
+                }
+            }
+        }
+        pit += kb1 - kb0;
+
+        // ================= phase B: the split-d partial, then one cluster barrier
+        const int ew = warp - 4;  // tensor-memory lane quadrant of warps 4..7
+        if (tid == 0 && CS > 1)
+            mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * row_bytes);
+        if (warp >= 4 && warp < 8) {
+            wait(accum, (uint32_t)rbi & 1u);
+            tc_fence_after();
+            const int row = ew * 32 + lane;
+            for (int c0 = 0; c0 < R; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)c0, v);
+                tmem_ld_wait();
+                if (row < rows) {
+                    float4* dst = reinterpret_cast<float4*>(out_f + (size_t)row * p.red_stride + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                }
+            }
+            fence_proxy_async_smem();  // the partial -> visible to the bulk copies
+        }
+        tc_fence_before();
+        if (CS > 1)
+            cluster_sync();  // #1: every partial is written; every receive slot is free
+        else
+            __syncthreads();
+
+        // ================= phase C: owners receive their rows' partials and sum
+        // Each CTA pushes the rows other CTAs own with one bulk shared-to-shared
+        // copy per owner.  Once an owner has received all of them it tells every
+        // sender (remote arrive on its "drained" barrier) that its buffer has been
+        // read; a sender waits for that only before it reuses the buffer.
+        if (CS > 1) {
+            if (tid < CS && tid != rank) {
+                const int dst = tid;
+                const int d_lo = dst * rows / CS;
+                const int d_hi = (dst + 1) * rows / CS;
+                if (d_hi > d_lo) {
+                    const uint32_t slot = (uint32_t)(rank < dst ? rank : rank - 1);
+                    bulk_s2cluster(map_cluster(sP + slot * (uint32_t)p.own_max * row_bytes, (uint32_t)dst),
+                                   sP + p.off_out + (uint32_t)d_lo * row_bytes,
+                                   (uint32_t)(d_hi - d_lo) * row_bytes, map_cluster(recv, (uint32_t)dst));
+                }
+            }
+            wait(recv, (uint32_t)rbi & 1u);
+            if (tid < CS && tid != rank) mbar_arrive_remote(map_cluster(drained, (uint32_t)tid));
+        }
+        {
+            const int own = o_hi - o_lo;
+            const int c4 = R >> 2;
+            for (int qd = tid; qd < own * c4; qd += SEL_THREADS) {
+                const int lr = qd / c4;
+                const int cc = (qd - lr * c4) * 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int src = 0; src < CS; ++src) {  // rank order: deterministic
+                    const float* srow =
+                        src == rank ? out_f + (size_t)(o_lo + lr) * p.red_stride
+                                    : recv_f + ((size_t)(src < rank ? src : src - 1) * p.own_max + lr) *
+                                                   p.red_stride;
+                    const float4 v = *reinterpret_cast<const float4*>(srow + cc);
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                *reinterpret_cast<float4*>(uslice + (size_t)lr * R + cc) = acc;
+                *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + cc) = acc;
+            }
+        }
+        __syncthreads();  // u slice complete; the receive slots are free
+
+        // ================= phase D: the edge tiles of this CTA's positions
+        if (warp >= 8) {
+            // gather + gate: unit 0 was issued in phase A; each unit is gated as
+            // soon as its rows have landed, and only then are later units issued
+            // (up to estages - 1 ahead), so the tensor core starts on unit 0
+            const int ahead = p.estages - 1;
+            int issued = nunits > 0 ? 1 : 0;
+            for (int j = 0; j < nunits; ++j) {
+                if (issued == j) issue_unit(issued++);
+                cp_wait_pending(issued - j - 1);
+                gate_unit(j);
+                fence_proxy_async_smem();
+                mbar_arrive(ready0 + 8 * (j % p.estages));
+                while (issued < nunits && issued <= j + ahead) issue_unit(issued++);
+            }
+            cp_async_wait_all();
+            if (!drained_ok) wait(drained, (uint32_t)rbi & 1u);  // before region P is reused
+        } else if (warp == 1) {
+            if (lane == 0) {  // MMA issuer
+                constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+                for (int t = 0; t < ntile; ++t) {
+                    const int bb = t & 1;
+                    if (t >= 2) wait(tempty0 + 8 * bb, (((uint32_t)(t >> 1)) - 1u) & 1u);
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(EACC + bb * 128);
+                    for (int half = 0; half < p.nhalf; ++half) {
+                        const int j = t * p.nhalf + half;
+                        const int st = j % p.estages;
+                        wait(ready0 + 8 * st, ((uint32_t)(j / p.estages)) & 1u);
+                        tc_fence_after();
+                        const uint32_t sa = estage_base(st);
+                        const uint32_t sbb = sa + (uint32_t)(p.nkb_e * KB_OP);
+                        if (!*abort_flag) {
+                            for (int kb = 0; kb < p.nkb_e; ++kb)
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    tc_mma_bf16(d, sw128_desc(sa + kb * KB_OP + 32 * k),
+                                                sw128_desc(sbb + kb * KB_OP + 32 * k), idesc,
+                                                (half > 0 || kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit(sfree0 + 8 * st);
+                    }
+                    tc_commit(tfull0 + 8 * bb);
+                }
+            }
+            __syncwarp();
+        } else if (warp >= 4) {
+            // epilogue: one thread per predecessor row of the tile; its unary
+            // scores are loaded before the accumulator is ready (two 16-column
+            // chunks ahead)
+            const int r = ew * 32 + lane;
+            const int pslot = r & (K - 1);
+            const int blk0 = r & ~(K - 1);
+            const int colbase = K >= 32 ? blk0 : 32 * ew;  // warp-uniform
+            const int nchunk = (K >= 32 ? K : 32) >> 4;     // 16-column chunks: even, >= 2
+            for (int t = 0; t < ntile; ++t) {
+                const int bb = t & 1;
+                const int e0 = e_lo + t * TP;
+                const int cnt = min(TP, e_hi - e0);
+                const bool valid = (r >> p.log2K) < cnt;
+                const int e = e0 + (r >> p.log2K);
+                int s = 0, i = 1;
+                if (valid) {
+                    s = e / nm1;
+                    i = e - s * nm1 + 1;
+                }
+                const float* un = p.unary + ((size_t)s * p.n + i) * K;
+                float* erow = (p.edges_out != nullptr && valid)
+                                  ? p.edges_out + ((size_t)e * K + pslot) * K
+                                  : nullptr;
+                float ua0[16], ua1[16];
+                auto load_u = [&](float (&ua)[16], int ch) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int c = colbase + ch * 16 + jj - blk0;
+                        ua[jj] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
+                    }
+                };
+                auto use_chunk = [&](const float (&ua)[16], int ch, float& best, int& arg) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem + ((uint32_t)(ew * 32) << 16) +
+                                           (uint32_t)(EACC + bb * 128 + colbase + ch * 16),
+                                       v);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int c = colbase + ch * 16 + jj - blk0;
+                            if (c >= 0 && c < K) {
+                                const float ev = __uint_as_float(v[jj]) + ua[jj];
+                                if (erow != nullptr) erow[c] = ev;
+                                if (c == 0 || ev > best) {
+                                    best = ev;
+                                    arg = c;
+                                }
+                            }
+                        }
+                    }
+                };
+                load_u(ua0, 0);
+                load_u(ua1, 1);
+                wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
+                tc_fence_after();
+                float best = 0.f;
+                int arg = 0;
+#pragma unroll 1
+                for (int ch = 0; ch < nchunk; ch += 2) {
+                    use_chunk(ua0, ch, best, arg);
+                    if (ch + 2 < nchunk) load_u(ua0, ch + 2);
+                    use_chunk(ua1, ch + 1, best, arg);
+                    if (ch + 3 < nchunk) load_u(ua1, ch + 3);
+                }
+                if (valid) {
+                    p.best_slot[(size_t)e * K + pslot] = arg;
+                    p.best_score[(size_t)e * K + pslot] = best;
+                }
+                tc_fence_before();
+                mbar_arrive(tempty0 + 8 * bb);
+            }
+        }
+        // End of the row block: every edge MMA has completed (the epilogue saw
+        // its last accumulator), every copy into region E / P has landed and the
+        // outgoing partial has been read by its owners, so the next row block may
+        // reuse all of shared memory.  The edge barriers restart from phase 0.
+        tc_fence_before();
+        __syncthreads();
+        if (rb + nclusters < p.nrb) {
+            if (tid == 0) {
+                for (int i = 0; i < p.estages; ++i) {
+                    mbar_inval(ready0 + 8 * i);
+                    mbar_inval(sfree0 + 8 * i);
+                }
+                for (int i = 0; i < 2; ++i) {
+                    mbar_inval(tfull0 + 8 * i);
+                    mbar_inval(tempty0 + 8 * i);
+                }
+                init_edge_bars();
+                fence_mbar_init();
+            }
+            __syncthreads();
+        }
+        tc_fence_after();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (bad && p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_BAD_ID);
+    if (tid == 0 && *abort_flag) {
+        if (p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_TIMEOUT);
+        atomicOr(&g_select_fault, (unsigned)DF2_FLAG_TIMEOUT);
+    }
+}
+
+// ---------------------------------------------------------------- planning
+
+struct PlanKey {
+    int P, d, R, K, n, sms;
+    bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+
+struct Plan {
+    bool ok = false;
+    int CS = 0, NC = 0, MR = 0, nrb = 0, own_max = 0, pstages = 0, estages = 0, nkb_e = 0, nhalf = 0;
+    int drain_stage = 0;
+    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_lr = 0;
+    uint32_t off_ids = 0, off_bar = 0, red_stride = 0;
+    size_t smem = 0;
+};
+
+std::mutex g_plan_mu;
+constexpr int kPlanCache = 16;
+PlanKey g_plan_keys[kPlanCache];
+Plan g_plans[kPlanCache];
+int g_plan_count = 0;
+int g_plan_next = 0;
+
+// Shared-memory layout for a cluster size and row-block height; false when it
+// does not fit.  Region E = edge stage 0.  Region P = the projection's TMA ring,
+// then the receive slots [CS-1][own_max] and the outgoing partial [MR] (rows of
+// R + 4 floats), then edge stages 1..estages-1.  Then the u slice, the local
+// u-row ring, the id ring and the barriers.
+bool layout(int R, int CS, int MR, size_t max_smem, Plan* q) {
+    q->nkb_e = R >= 128 ? 2 : 1;
+    q->nhalf = R / (64 * q->nkb_e);
+    q->estage_bytes = 2u * (uint32_t)q->nkb_e * KB_OP;
+    q->pstage_bytes = (uint32_t)HTILE + (uint32_t)R * 128u;
+    q->red_stride = (uint32_t)R + 4u;
+    q->own_max = (MR + CS - 1) / CS;
+    const size_t row_bytes = (size_t)q->red_stride * 4;
+    const size_t recv_bytes = (size_t)(CS - 1) * q->own_max * row_bytes;
+    const size_t off_out = (recv_bytes + 1023) & ~(size_t)1023;
+    const size_t red_end = off_out + (size_t)MR * row_bytes;
+    const size_t u_bytes = (size_t)q->own_max * R * 4;
+    const size_t bar_bytes = 8 * (2 * 8 + 3 + 2 * 4 + 4) + 16;
+    for (int ps = 6; ps >= 2; --ps) {
+        size_t regionP = (size_t)ps * q->pstage_bytes;
+        if (regionP < red_end) regionP = (red_end + 1023) & ~(size_t)1023;
+        const int es = 1 + (int)std::min<size_t>(3, regionP / q->estage_bytes);
+        const size_t off_U = q->estage_bytes + regionP;
+        const size_t off_lr = off_U + ((u_bytes + 15) & ~(size_t)15);
+        const size_t off_ids = off_lr + LR_SLOTS * 32 * 4;
+        const size_t off_bar = off_ids + 2 * 2 * EROWS * 4;
+        const size_t total = 1024 + off_bar + bar_bytes;
+        if (total <= max_smem && es >= 2) {
+            q->pstages = ps;
+            q->estages = es;
+            q->off_P = q->estage_bytes;
+            q->off_out = (uint32_t)off_out;
+            q->off_U = (uint32_t)off_U;
+            q->off_lr = (uint32_t)off_lr;
+            q->off_ids = (uint32_t)off_ids;
+            q->off_bar = (uint32_t)off_bar;
+            // first edge stage in region P whose bytes overlap the outgoing partial
+            q->drain_stage = CS > 1 ? 1 + (int)(off_out / q->estage_bytes) : es;
+            q->smem = total;
+            return true;
+        }
+    }
+    return false;
+}
+
+int max_active_clusters(int CS, size_t smem) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)CS);
+    cfg.blockDim = dim3(SEL_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    bool ok = cudaFuncSetAttribute(select_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem) == cudaSuccess;
+    if (ok && CS > 8)
+        ok = cudaFuncSetAttribute(select_fused_kernel,
+                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (ok) ok = cudaOccupancyMaxActiveClusters(&n, select_fused_kernel, &cfg) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();  // an unsupported cluster size is not an error of the call
+        return 0;
+    }
+    return n;
+}
+
+// Dynamic shared memory every launch requests at least: more than half of an
+// SM's, so that no two CTAs share an SM.  Each CTA takes all 512 tensor-memory
+// columns; two CTAs of one cluster on one SM would otherwise wait for each
+// other (one in tcgen05.alloc, the other at the cluster barrier).
+constexpr size_t kMinSmem = 120 * 1024;
+
+// Picks the cluster size and row-block height with the least modelled time per
+// CTA: HBM bytes of h and of the gathered rows, plus the L2-served slice of W
+// at a third of their weight, times the number of waves of row blocks.
+Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
+    Plan best;
+    double best_cost = 0;
+    const int kblocks = (d + 63) / 64;
+    const double E_per_pos = (double)(n - 1) / n;
+    for (int CS = 1; CS <= 16; ++CS) {
+        if (CS > 8 && CS != 16) continue;
+        if (kblocks < CS) break;
+        const int ncmax = std::min(sms / CS, max_active_clusters(CS, std::max(kMinSmem, (size_t)160 * 1024)));
+        if (ncmax < 1) continue;
+        // the largest row block whose layout fits (owned rows <= 32)
+        int mr_fit = std::min(128, 32 * CS);
+        Plan probe;
+        while (mr_fit > 0 && !layout(R, CS, mr_fit, max_smem, &probe)) --mr_fit;
+        if (mr_fit == 0) continue;
+        // a row block per cluster when the rows allow it, else waves of full blocks
+        const int MR = std::min(mr_fit, (P + ncmax - 1) / ncmax);
+        const int nrb = (P + MR - 1) / MR;
+        const int NC = std::min(ncmax, nrb);
+        const int waves = (nrb + NC - 1) / NC;
+        Plan q;
+        if (!layout(R, CS, MR, max_smem, &q)) continue;
+        const double kpc = (double)kblocks / CS;
+        const double h_b = MR * kpc * 128.0;
+        const double w_b = R * kpc * 128.0;
+        const double g_b = (double)q.own_max * E_per_pos * 2.0 * K * R * 2.0;
+        const double cost = waves * (h_b + g_b + w_b / 3.0) + 1e-3 * NC * CS;
+        if (!best.ok || cost < best_cost) {
+            best = q;
+            best.ok = true;
+            best.CS = CS;
+            best.NC = NC;
+            best.MR = MR;
+            best.nrb = nrb;
+            best_cost = cost;
+        }
+    }
+    if (best.ok && best.smem < kMinSmem) best.smem = kMinSmem;
+    return best;
+}
+
+Plan get_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
+    const PlanKey key{P, d, R, K, n, sms};
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    for (int i = 0; i < g_plan_count; ++i)
+        if (g_plan_keys[i] == key) return g_plans[i];
+    const Plan pl = make_plan(P, d, R, K, n, sms, max_smem);
+    const int slot = g_plan_count < kPlanCache ? g_plan_count++ : (g_plan_next++ % kPlanCache);
+    g_plan_keys[slot] = key;
+    g_plans[slot] = pl;
+    return pl;
+}
+
+}  // namespace
+
+bool select_fused_supported(int K, int R, int d, int n) {
+    return K >= 4 && K <= 128 && (K & (K - 1)) == 0 && (R == 64 || R == 128 || R == 256) &&
+           d % 8 == 0 && n >= 2;
+}
+
+cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int num_sms,
+                                size_t max_smem, bool* launched) {
+    *launched = false;
+    const int P = a.S * a.n;
+    const Plan pl = get_plan(P, a.d, a.R, a.K, a.n, num_sms, max_smem);
+    if (!pl.ok) return cudaSuccess;  // the caller falls back to the two-kernel path
+    CUtensorMap tmH, tmW;
+    if (!make_tmap_rows_bf16(&tmH, a.h, P, a.d, pl.MR) ||
+        !make_tmap_rows_bf16(&tmW, a.W, a.R, a.d, a.R))
+        return cudaErrorInvalidValue;
+    SelParams p{};
+    p.cand_ids = a.cand_ids;
+    p.unary = a.unary;
+    p.A = static_cast<const __nv_bfloat16*>(a.A);
+    p.B = static_cast<const __nv_bfloat16*>(a.B);
+    p.u = a.u;
+    p.edges_out = a.edges_out;
+    p.best_slot = a.best_slot;
+    p.best_score = a.best_score;
+    p.err_flag = a.err_flag;
+    p.S = a.S;
+    p.n = a.n;
+    p.K = a.K;
+    p.R = a.R;
+    p.V = a.V;
+    p.P = P;
+    int l2 = 0;
+    while ((1 << l2) < a.K) ++l2;
+    p.log2K = l2;
+    p.CS = pl.CS;
+    p.MR = pl.MR;
+    p.nrb = pl.nrb;
+    p.kblocks = (a.d + 63) / 64;
+    p.own_max = pl.own_max;
+    p.pstages = pl.pstages;
+    p.estages = pl.estages;
+    p.nkb_e = pl.nkb_e;
+    p.nhalf = pl.nhalf;
+    p.pstage_bytes = pl.pstage_bytes;
+    p.estage_bytes = pl.estage_bytes;
+    p.off_P = pl.off_P;
+    p.off_out = pl.off_out;
+    p.off_U = pl.off_U;
+    p.off_lr = pl.off_lr;
+    p.off_ids = pl.off_ids;
+    p.off_bar = pl.off_bar;
+    p.drain_stage = pl.drain_stage;
+    p.red_stride = pl.red_stride;
+    cudaError_t e = cudaFuncSetAttribute(select_fused_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess) return e;
+    if (pl.CS > 8) {
+        e = cudaFuncSetAttribute(select_fused_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(pl.NC * pl.CS));
+    cfg.blockDim = dim3(SEL_THREADS);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, select_fused_kernel, tmH, tmW, p);
+    if (e != cudaSuccess) return e;
+    *launched = true;
+    return cudaGetLastError();
+}
+
+bool select_fused_plan(int S, int n, int d, int K, int R, int num_sms, size_t max_smem,
+                       int* cluster_size, int* clusters, int* rows_per_block) {
+    if (!select_fused_supported(K, R, d, n)) return false;
+    const Plan pl = get_plan(S * n, d, R, K, n, num_sms, max_smem);
+    if (!pl.ok) return false;
+    *cluster_size = pl.CS;
+    *clusters = pl.NC;
+    *rows_per_block = pl.MR;
+    return true;
+}
+
+cudaError_t take_select_faults(unsigned* flags) {
+    unsigned v = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_select_fault, sizeof(v));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_select_fault, &zero, sizeof(zero));
+    *flags = v;
+    return e;
+}
+
+}  // namespace df2

@@ -162,16 +162,38 @@ int dflash2_edges(const int32_t* cand_ids, const float* u, const void* A, const 
                   int32_t* err_flag, void* stream);
 
 /*
- * The composite selector: dflash2_project of every position's hidden state
- * into u_out, then dflash2_edges, both enqueued on `stream`.
+ * The composite selector: the projection of every position's hidden state
+ * (as dflash2_project, written to u_out) and the edge scores with the
+ * per-predecessor argmax (as dflash2_edges, reading that projection).
  *   h [S*n,d], W [R,d] in `dtype`; A, B [V,R] in `dtype`; u_out [S*n,R] fp32
- *   (caller-owned: it carries the projection between the two kernels).
- * Other arguments and errors as for the two calls it makes.
+ *   (caller-owned; it receives u).
+ * bf16 with K a power of two in [4,128], R = 64, 128 or 256, d % 8 == 0 and
+ * n >= 2 runs as ONE kernel (see dflash2_select_plan): thread-block clusters
+ * split d of a block of positions, reduce u through distributed shared memory,
+ * and score the transitions into those positions from u held on chip, with the
+ * first codebook gathers issued while h streams.  Other shapes run
+ * dflash2_project then dflash2_edges on `stream`.  Same results either way
+ * (within the bf16 tolerance: the d-sums are split differently).
+ * Other arguments and errors as for those two calls.
  */
 int dflash2_select(const void* h, const void* W, const int32_t* cand_ids, const void* A,
                    const void* B, const float* unary, int S, int n, int d, int K, int R,
                    int V, int dtype, float* u_out, float* edges_out, int32_t* best_slot,
                    float* best_score, int32_t* err_flag, void* stream);
+
+/*
+ * How dflash2_select runs these shapes on the current device (a query; nothing
+ * is launched).  plan_out[4] receives:
+ *   [0] 1 when the one-kernel selector runs (bf16; K a power of two in [4,128];
+ *       R = 64, 128 or 256; d % 8 == 0; n >= 2; a cluster layout that fits),
+ *       0 when the call runs dflash2_project and then dflash2_edges;
+ *   [1] CTAs per thread-block cluster (the split of d), [2] clusters launched,
+ *   [3] positions per cluster row block (0 when [0] is 0).
+ * The first query for a shape measures cluster occupancy (CUDA runtime calls,
+ * no launch) and caches the layout.
+ * INVALID_ARG: NULL plan_out; S, n, d, K, R <= 0; bad dtype.
+ */
+int dflash2_select_plan(int S, int n, int d, int K, int R, int dtype, int* plan_out);
 
 /*
  * dflash2_project for callers that cannot allocate device memory: plugins and
@@ -297,11 +319,14 @@ int dflash2_chain(const int32_t* cand_ids, const float* unary, const float* edge
  *   out[i] = XOR of the 32-bit words of row ids[i] of table
  * where table is [rows, row_bytes] bytes and an id outside [0, rows) is
  * clamped into range.  Reads every gathered byte once; writes 4 bytes per id.
+ * The rows are fetched as the edge kernels fetch codebook rows: one CTA per
+ * SM with its ids staged in shared memory, 16-byte cp.async copies into a
+ * shared-memory ring.
  *   table  device memory, rows * row_bytes bytes, 16-byte aligned
  *   ids    [n_ids] int32 device;  out [n_ids] uint32 device, disjoint from both
  * n_ids == 0 launches nothing.
  * INVALID_ARG: NULL pointer; rows <= 0; n_ids < 0; row_bytes not a power of
- * two in [16, 1024]; misalignment; out overlapping table or ids.
+ * two in [16, 512]; misalignment; out overlapping table or ids.
  */
 int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const int32_t* ids,
                          int n_ids, uint32_t* out, void* stream);

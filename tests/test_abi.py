@@ -228,7 +228,7 @@ def _probe(L, tb=P[0], rows=1000, rb=256, ids=P[1], n=64, out=P[2]):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(tb=NULL), 1), (dict(ids=NULL), 1), (dict(out=NULL), 1), (dict(rows=0), 1),
-    (dict(n=-1), 1), (dict(rb=8), 1), (dict(rb=96), 1), (dict(rb=2048), 1),
+    (dict(n=-1), 1), (dict(rb=8), 1), (dict(rb=96), 1), (dict(rb=1024), 1),
     (dict(tb=ctypes.c_void_p(0x10000004)), 1),
     (dict(out=P[0]), 1),                       # out inside the table
 ])

@@ -5,9 +5,10 @@ runtime that owns the device pool, a decode loop where an allocation call may
 not run).  For them the library carries its own fixed split-K workspace.  This
 test calls that entry point through the C ABI, twice in a row on different
 inputs (the shared workspace keeps the previous call's contents), and checks
-it against dflash2_project within the bf16 test tolerance.  It also checks
-that shapes needing more than the fixed workspace are refused cleanly.
-This file is collected last on purpose.
+it against dflash2_project within the bf16 test tolerance, and against the
+fp64 oracle on a split-K shape and on a shape whose 256-column tiles need no
+workspace at all.  It also checks that shapes needing more than the fixed
+workspace are refused cleanly.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -16,6 +17,7 @@ import pytest
 import torch
 
 import dflash2_draft_head_gb300 as df2
+import oracle
 from helpers import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -73,3 +75,31 @@ def test_noalloc_refuses_oversized_shapes(L):
     assert b"workspace" in L.dflash2_last_error()
     torch.cuda.synchronize()
     assert float(u.abs().max()) == 0.0  # nothing was launched
+
+
+def _host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("shape", ["split", "wide256"])
+def test_noalloc_matches_oracle(L, shape):
+    if shape == "split":  # one draft block: split-K over a cluster, workspace in use
+        P, d, R = 16, 5120, 128
+        assert L.dflash2_project_workspace_bytes(P, d, R) > 0
+    else:  # one 128-row tile per SM, R > 128: 256-column tiles, no split, no workspace
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        P, d, R = 128 * sms, 512, 256
+        assert L.dflash2_project_workspace_bytes(P, d, R) == 0
+    for seed in (5, 6):
+        h, W = _inputs(P, d, R, seed)
+        u = torch.full((P, R), float("nan"), device="cuda")
+        assert _call(L.dflash2_project_noalloc, h, W, u) == 0, L.dflash2_last_error()
+        torch.cuda.synchronize()
+        if P <= 64:
+            rows = np.arange(P)
+        else:
+            rnd = np.random.default_rng(seed).integers(0, P, 256)
+            rows = np.unique(np.r_[0:8, P - 8:P, rnd])
+        ref = oracle.project(_host(h)[rows], _host(W))
+        assert_close(u.cpu().numpy()[rows], ref, "bf16", f"noalloc {shape} seed={seed}")
+    assert df2.take_device_faults() == 0
