@@ -90,7 +90,7 @@ struct SelParams {
     int drain_stage;   // first edge stage that overlaps the outgoing partial buffer
     uint32_t pstage_bytes;  // HTILE + R * 128
     uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
-    uint32_t off_P, off_out, off_U, off_lr, off_ids, off_bar;  // off_out is relative to region P
+    uint32_t off_P, off_out, off_U, off_un, off_lr, off_ids, off_bar;  // off_out: relative to region P
     uint32_t red_stride;    // floats per row of the partial buffers (R + 4)
 };
 
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const float* recv_f = reinterpret_cast<const float*>(smem + p.off_P);        // [CS-1][own_max][R+4]
     float* out_f = reinterpret_cast<float*>(smem + p.off_P + p.off_out);        // [MR][R+4]
     float* uslice = reinterpret_cast<float*>(smem + p.off_U);                   // [own][R]
+    float* unslice = reinterpret_cast<float*>(smem + p.off_un);                 // [own][K]
     int* lr_ring = reinterpret_cast<int*>(smem + p.off_lr);                     // [LR_SLOTS][32]
     int* id_ring = reinterpret_cast<int*>(smem + p.off_ids);                    // [2][256]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
@@ -395,6 +396,14 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             }
         }
         pit += kb1 - kb0;
+        // the epilogue warps, idle until the partial is ready, stage the unary
+        // scores of this CTA's own positions (read again per tile in phase D)
+        if (warp >= 4 && warp < 8) {
+            const int n4 = (o_hi - o_lo) * K / 4;
+            const float4* src = reinterpret_cast<const float4*>(p.unary + (size_t)pa * K);
+            for (int qd = tid - 128; qd < n4; qd += 128)
+                reinterpret_cast<float4*>(unslice)[qd] = __ldg(src + qd);
+        }
 
         // ================= phase B: the split-d partial, then one cluster barrier
         const int ew = warp - 4;  // tensor-memory lane quadrant of warps 4..7
@@ -466,20 +475,57 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + cc) = acc;
             }
         }
-        __syncthreads();  // u slice complete; the receive slots are free
+        // unit 0 (copied into region E under the projection) is gated by every
+        // thread of the CTA: its copies are complete (each gather thread waits for
+        // its own), and the barrier makes them and the u slice visible to all
+        if (warp >= 8) cp_wait_pending(0);
+        __syncthreads();  // u slice complete; the receive slots are free; unit 0 landed
+        if (nunits > 0) {
+            const int t0rows = min(TP, e_hi - e_lo) << p.log2K;
+            const int* lr = lr_ring;  // tile 0's table (slot 0)
+            const int col0 = 0;
+            const int cpr = 8 * p.nkb_e;
+            if (!*abort_flag) {
+                for (int qd = tid; qd < t0rows * cpr; qd += SEL_THREADS) {
+                    const int row = qd >> log2cpr;
+                    const int kb = (qd >> 3) & (p.nkb_e - 1);
+                    const int ch = qd & 7;
+                    const int col = col0 + kb * 64 + ch * 8;
+                    const float4* ur =
+                        reinterpret_cast<const float4*>(uslice + (size_t)lr[row >> p.log2K] * R + col);
+                    const float4 u0 = ur[0];
+                    const float4 u1 = ur[1];
+                    const uint32_t off =
+                        sE + (uint32_t)(kb * KB_OP + row * 128 + ((ch ^ (row & 7)) << 4));
+                    const uint4 a = lds_v4(off);
+                    const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
+                    const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
+                    uint4 g;
+                    g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
+                    g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
+                    g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
+                    g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
+                    st_shared_v4(off, g);
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
 
         // ================= phase D: the edge tiles of this CTA's positions
         if (warp >= 8) {
-            // gather + gate: unit 0 was issued in phase A; each unit is gated as
-            // soon as its rows have landed, and only then are later units issued
-            // (up to estages - 1 ahead), so the tensor core starts on unit 0
+            // gather + gate: unit 0 is gated already; each later unit is gated as
+            // soon as its rows have landed, and only then are further units issued
+            // (up to estages - 1 ahead)
             const int ahead = p.estages - 1;
             int issued = nunits > 0 ? 1 : 0;
             for (int j = 0; j < nunits; ++j) {
                 if (issued == j) issue_unit(issued++);
-                cp_wait_pending(issued - j - 1);
-                gate_unit(j);
-                fence_proxy_async_smem();
+                if (j > 0) {
+                    cp_wait_pending(issued - j - 1);
+                    gate_unit(j);
+                    fence_proxy_async_smem();
+                }
                 mbar_arrive(ready0 + 8 * (j % p.estages));
                 while (issued < nunits && issued <= j + ahead) issue_unit(issued++);
             }
@@ -516,13 +562,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             __syncwarp();
         } else if (warp >= 4) {
             // epilogue: one thread per predecessor row of the tile; its unary
-            // scores are loaded before the accumulator is ready (two 16-column
-            // chunks ahead)
+            // scores come from the staged slice
             const int r = ew * 32 + lane;
             const int pslot = r & (K - 1);
             const int blk0 = r & ~(K - 1);
             const int colbase = K >= 32 ? blk0 : 32 * ew;  // warp-uniform
-            const int nchunk = (K >= 32 ? K : 32) >> 4;     // 16-column chunks: even, >= 2
+            const int nchunk = (K >= 32 ? K : 32) >> 4;     // 16-column chunks
             for (int t = 0; t < ntile; ++t) {
                 const int bb = t & 1;
                 const int e0 = e_lo + t * TP;
@@ -534,51 +579,59 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     s = e / nm1;
                     i = e - s * nm1 + 1;
                 }
-                const float* un = p.unary + ((size_t)s * p.n + i) * K;
+                // unary row of this transition's position (staged in phase A)
+                const float* un = unslice + (size_t)(valid ? (s * p.n + i - pa) : 0) * K;
                 float* erow = (p.edges_out != nullptr && valid)
                                   ? p.edges_out + ((size_t)e * K + pslot) * K
                                   : nullptr;
-                float ua0[16], ua1[16];
-                auto load_u = [&](float (&ua)[16], int ch) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int c = colbase + ch * 16 + jj - blk0;
-                        ua[jj] = (valid && c >= 0 && c < K) ? __ldg(un + c) : 0.f;
-                    }
-                };
-                auto use_chunk = [&](const float (&ua)[16], int ch, float& best, int& arg) {
+                wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
+                tc_fence_after();
+                float best = 0.f;
+                int arg = -1;
+#pragma unroll 1
+                for (int ch = 0; ch < nchunk; ++ch) {
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(tmem + ((uint32_t)(ew * 32) << 16) +
                                            (uint32_t)(EACC + bb * 128 + colbase + ch * 16),
                                        v);
                     tmem_ld_wait();
-                    if (valid) {
+                    const int c0 = colbase + ch * 16 - blk0;  // slot of column jj = 0
+                    if (valid && c0 + 16 > 0 && c0 < K) {
+                        // every read in bounds (slot masked into the row), so the 16
+                        // shared loads issue together; slots outside this lane's
+                        // block are masked out of the argmax
+                        float ev[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            ev[jj] = __uint_as_float(v[jj]) + un[(c0 + jj) & (K - 1)];
+                        if (erow != nullptr) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (c0 + jj >= 0 && c0 + jj < K) erow[c0 + jj] = ev[jj];
+                        }
+                        // argmax by a tree over index order: on equal values the
+                        // left (lower) slot is kept, as in a scan with a strict ">"
+                        float bv[16];
+                        int bi[16];
 #pragma unroll
                         for (int jj = 0; jj < 16; ++jj) {
-                            const int c = colbase + ch * 16 + jj - blk0;
-                            if (c >= 0 && c < K) {
-                                const float ev = __uint_as_float(v[jj]) + ua[jj];
-                                if (erow != nullptr) erow[c] = ev;
-                                if (c == 0 || ev > best) {
-                                    best = ev;
-                                    arg = c;
+                            const bool in = c0 + jj >= 0 && c0 + jj < K;
+                            bv[jj] = in ? ev[jj] : -INFINITY;
+                            bi[jj] = in ? c0 + jj : K;
+                        }
+#pragma unroll
+                        for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 2 * w)
+                                if (bv[jj + w] > bv[jj] || (bi[jj] == K && bi[jj + w] < K)) {
+                                    bv[jj] = bv[jj + w];
+                                    bi[jj] = bi[jj + w];
                                 }
-                            }
+                        if (arg < 0 || bv[0] > best) {  // chunks come in slot order
+                            best = bv[0];
+                            arg = bi[0];
                         }
                     }
-                };
-                load_u(ua0, 0);
-                load_u(ua1, 1);
-                wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
-                tc_fence_after();
-                float best = 0.f;
-                int arg = 0;
-#pragma unroll 1
-                for (int ch = 0; ch < nchunk; ch += 2) {
-                    use_chunk(ua0, ch, best, arg);
-                    if (ch + 2 < nchunk) load_u(ua0, ch + 2);
-                    use_chunk(ua1, ch + 1, best, arg);
-                    if (ch + 3 < nchunk) load_u(ua1, ch + 3);
                 }
                 if (valid) {
                     p.best_slot[(size_t)e * K + pslot] = arg;
@@ -636,7 +689,7 @@ struct Plan {
     bool ok = false;
     int CS = 0, NC = 0, MR = 0, nrb = 0, own_max = 0, pstages = 0, estages = 0, nkb_e = 0, nhalf = 0;
     int drain_stage = 0;
-    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_lr = 0;
+    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_un = 0, off_lr = 0;
     uint32_t off_ids = 0, off_bar = 0, red_stride = 0;
     size_t smem = 0;
 };
@@ -653,7 +706,7 @@ int g_plan_next = 0;
 // then the receive slots [CS-1][own_max] and the outgoing partial [MR] (rows of
 // R + 4 floats), then edge stages 1..estages-1.  Then the u slice, the local
 // u-row ring, the id ring and the barriers.
-bool layout(int R, int CS, int MR, size_t max_smem, Plan* q) {
+bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     q->nkb_e = R >= 128 ? 2 : 1;
     q->nhalf = R / (64 * q->nkb_e);
     q->estage_bytes = 2u * (uint32_t)q->nkb_e * KB_OP;
@@ -665,13 +718,15 @@ bool layout(int R, int CS, int MR, size_t max_smem, Plan* q) {
     const size_t off_out = (recv_bytes + 1023) & ~(size_t)1023;
     const size_t red_end = off_out + (size_t)MR * row_bytes;
     const size_t u_bytes = (size_t)q->own_max * R * 4;
+    const size_t un_bytes = (size_t)q->own_max * K * 4;
     const size_t bar_bytes = 8 * (2 * 8 + 3 + 2 * 4 + 4) + 16;
     for (int ps = 6; ps >= 2; --ps) {
         size_t regionP = (size_t)ps * q->pstage_bytes;
         if (regionP < red_end) regionP = (red_end + 1023) & ~(size_t)1023;
         const int es = 1 + (int)std::min<size_t>(3, regionP / q->estage_bytes);
         const size_t off_U = q->estage_bytes + regionP;
-        const size_t off_lr = off_U + ((u_bytes + 15) & ~(size_t)15);
+        const size_t off_un = off_U + ((u_bytes + 15) & ~(size_t)15);
+        const size_t off_lr = off_un + ((un_bytes + 15) & ~(size_t)15);
         const size_t off_ids = off_lr + LR_SLOTS * 32 * 4;
         const size_t off_bar = off_ids + 2 * 2 * EROWS * 4;
         const size_t total = 1024 + off_bar + bar_bytes;
@@ -681,6 +736,7 @@ bool layout(int R, int CS, int MR, size_t max_smem, Plan* q) {
             q->off_P = q->estage_bytes;
             q->off_out = (uint32_t)off_out;
             q->off_U = (uint32_t)off_U;
+            q->off_un = (uint32_t)off_un;
             q->off_lr = (uint32_t)off_lr;
             q->off_ids = (uint32_t)off_ids;
             q->off_bar = (uint32_t)off_bar;
@@ -741,7 +797,7 @@ Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
         // the largest row block whose layout fits (owned rows <= 32)
         int mr_fit = std::min(128, 32 * CS);
         Plan probe;
-        while (mr_fit > 0 && !layout(R, CS, mr_fit, max_smem, &probe)) --mr_fit;
+        while (mr_fit > 0 && !layout(R, K, CS, mr_fit, max_smem, &probe)) --mr_fit;
         if (mr_fit == 0) continue;
         // a row block per cluster when the rows allow it, else waves of full blocks
         const int MR = std::min(mr_fit, (P + ncmax - 1) / ncmax);
@@ -749,7 +805,7 @@ Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
         const int NC = std::min(ncmax, nrb);
         const int waves = (nrb + NC - 1) / NC;
         Plan q;
-        if (!layout(R, CS, MR, max_smem, &q)) continue;
+        if (!layout(R, K, CS, MR, max_smem, &q)) continue;
         const double kpc = (double)kblocks / CS;
         const double h_b = MR * kpc * 128.0;
         const double w_b = R * kpc * 128.0;
@@ -831,6 +887,7 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     p.off_P = pl.off_P;
     p.off_out = pl.off_out;
     p.off_U = pl.off_U;
+    p.off_un = pl.off_un;
     p.off_lr = pl.off_lr;
     p.off_ids = pl.off_ids;
     p.off_bar = pl.off_bar;
