@@ -51,6 +51,10 @@ TRAFFIC = {
         "sha": "ba528104f498b57b66ed7ce720e829e70da5c4cdac4644f7ceaa22e20a4d59db",  # capture taken before a comment-only edit of the file
         "bytes": 8 * (311424512 + 3649536),
     },
+    ("batched_256x16_d5120", "select"): {
+        "sha": "e9b14497aa801678e415732d889b63706c75bb9344cb20e89554b9a05da59529",
+        "bytes": 69823232 + 1617920,
+    },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
         "bytes": 52396288 + 3153408,

@@ -298,9 +298,23 @@ __device__ __forceinline__ void conv_point(const float2 (&bw)[T][NP], const floa
         acc[q] = make_float2(0.f, 0.f);
         odd[q] = make_float2(0.f, 0.f);
     }
+    // 4-channel threads (long filters) read a position's taps as 16-byte vectors
+    // (the tap rows are 16-byte aligned: DSTR and T are multiples of 4)
+    constexpr bool kVecTaps = NP == 2 && T % 4 == 0;
+    float dvv[T];
+    if constexpr (kVecTaps) {
+#pragma unroll
+        for (int t = 0; t < T; t += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dtl + t);
+            dvv[t] = d4.x;
+            dvv[t + 1] = d4.y;
+            dvv[t + 2] = d4.z;
+            dvv[t + 3] = d4.w;
+        }
+    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        const float dv = dtl[t];
+        const float dv = kVecTaps ? dvv[t] : dtl[t];
         const float2 d2 = make_float2(dv, dv);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -485,7 +499,29 @@ __global__ void __launch_bounds__(NP == 4 ? 160 : 288, NP == 4 ? 4 : 2)
         {
             const __nv_bfloat16* dsrc = reinterpret_cast<const __nv_bfloat16*>(
                 smem + (size_t)st * p.stage_bytes + (size_t)(T - 1 + PL) * p.row_bytes);
-            if constexpr (kLanesOverGroups) {
+            if (p.G % 8 == 0) {
+                // 16-byte reads of 8 consecutive groups of one (l, t) row of the
+                // staged [l][t][G] block (G % 8 == 0 keeps them aligned), lanes over
+                // (l, t) so each of the 8 scattered stores hits consecutive words
+                const int g8_lo = g_lo & ~7;
+                const int n8 = (g_lo + ng - g8_lo + 7) >> 3;
+                const uint32_t src0 = smem_u32(dsrc);
+                for (int q = tid; q < PL * T * n8; q += nthr) {
+                    const int lt = q % (PL * T);
+                    const int gb = g8_lo + (q / (PL * T)) * 8;
+                    const uint4 raw = (lt / T) < nl
+                                          ? lds_v4(src0 + (uint32_t)(lt * p.G + gb) * 2u)
+                                          : make_uint4(0, 0, 0, 0);
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int gg = gb + k - g_lo;
+                        if (gg >= 0 && gg < ng)
+                            dt[gg * DSTR + lt] = __uint_as_float((k & 1) ? (w[k >> 1] & 0xFFFF0000u)
+                                                                         : (w[k >> 1] << 16));
+                    }
+                }
+            } else if constexpr (kLanesOverGroups) {
                 // lanes walk groups (contiguous in the staged [l][t][G] block),
                 // warps walk (l, t)
                 const int lane = tid & 31;
