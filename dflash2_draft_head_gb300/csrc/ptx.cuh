@@ -46,14 +46,33 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Bounded wait: polls the phase until it completes or `limit_ns` nanoseconds
-// of the global timer have passed; returns whether the phase completed.
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended in hardware until the phase completes or about `hint_ns` have
+// passed, so waiting warps leave the issue slots to the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms per suspended try_wait
+
+// Bounded wait: waits for the phase until it completes or `limit_ns`
+// nanoseconds of the global timer have passed (plus at most one suspend
+// hint); returns whether the phase completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
@@ -353,12 +372,25 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_suspend(uint32_t bar, uint32_t parity,
+                                                              uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity,
                                                           uint64_t limit_ns) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (mbar_try_wait_cluster_suspend(bar, parity, kSuspendHintNs)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }

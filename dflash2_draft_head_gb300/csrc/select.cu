@@ -31,14 +31,18 @@
 //    contiguous run of transitions).  Tiles of 128/K transitions hold 128
 //    predecessor rows of A and 128 candidate rows of B (one edge stage per 128
 //    ranks).  8 gather warps copy the rows by token id with 16-byte cp.async
-//    straight into the tensor core's 128-byte-swizzle K-major layout; the
-//    first stage's copies are issued at kernel start, under the projection,
-//    and every later tile's rows are prefetched into L2 then.  Each gather
-//    thread later gates exactly the A chunks it copied itself (no hand-off):
-//    A (.) u in fp32, rounded to bf16, in place.  One thread issues
-//    tcgen05.mma (M = N = 128) into one of two tensor-memory accumulators; 4
-//    epilogue warps read back only each transition's K x K diagonal block,
-//    add unary, keep the running argmax (lowest slot on ties) and store.
+//    straight into the tensor core's 128-byte-swizzle K-major layout and only
+//    issue copies (completion is counted on the stage's mbarrier by
+//    cp.async.mbarrier.arrive.noinc): a warp that also read back what it
+//    copied would stall its own next copies.  The first stage's copies are
+//    issued at kernel start, under the projection, and every later tile's
+//    rows are prefetched into L2 then.  4 gate warps form A (.) u in place
+//    (fp32 product, rounded to bf16) once a stage has landed, fence the async
+//    proxy and meet at a named barrier, after which one of their threads
+//    issues tcgen05.mma (M = N = 128) into one of two tensor-memory
+//    accumulators; 4 epilogue warps read back only each transition's K x K
+//    diagonal block, add unary, keep the running argmax (lowest slot on ties)
+//    and store.
 // Every wait on an mbarrier is bounded by the global timer; on a timeout the
 // kernel sets DF2_FLAG_TIMEOUT and runs to completion without hanging.
 #include <cuda.h>
@@ -90,11 +94,9 @@ struct SelParams {
     int drain_stage;   // first edge stage that overlaps the outgoing partial buffer
     uint32_t pstage_bytes;  // HTILE + R * 128
     uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
-    uint32_t off_P, off_out, off_U, off_un, off_lr, off_ids, off_bar;  // off_out: relative to region P
+    uint32_t off_P, off_out, off_U, off_un, off_ids, off_bar;  // off_out: relative to region P
     uint32_t red_stride;    // floats per row of the partial buffers (R + 4)
 };
-
-constexpr int LR_SLOTS = 4;  // tiles whose local u-row table is kept (ring)
 
 __device__ __forceinline__ int checked_id(int id, int V, bool& bad) {
     if (id < 0 || id >= V) {
@@ -113,16 +115,19 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&b);
 }
 
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Waits until at most `pending` of this thread's cp.async groups are outstanding.
-__device__ __forceinline__ void cp_wait_pending(int pending) {
-    switch (pending) {
-        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    }
+// One 16-byte chunk of a gathered A row (8 bf16) times 8 fp32 gate values:
+// products in fp32 (round to nearest), each rounded once to bf16.
+__device__ __forceinline__ uint4 gate_chunk(uint4 a, float4 u0, float4 u1) {
+    const float2 p0 = __fmul2_rn(bf16x2_to_f2(a.x), make_float2(u0.x, u0.y));
+    const float2 p1 = __fmul2_rn(bf16x2_to_f2(a.y), make_float2(u0.z, u0.w));
+    const float2 p2 = __fmul2_rn(bf16x2_to_f2(a.z), make_float2(u1.x, u1.y));
+    const float2 p3 = __fmul2_rn(bf16x2_to_f2(a.w), make_float2(u1.z, u1.w));
+    uint4 g;
+    g.x = f2_to_bf16x2(p0.x, p0.y);
+    g.y = f2_to_bf16x2(p1.x, p1.y);
+    g.z = f2_to_bf16x2(p2.x, p2.y);
+    g.w = f2_to_bf16x2(p3.x, p3.y);
+    return g;
 }
 
 __device__ __forceinline__ void mbar_inval(uint32_t bar) {
@@ -148,7 +153,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     float* out_f = reinterpret_cast<float*>(smem + p.off_P + p.off_out);        // [MR][R+4]
     float* uslice = reinterpret_cast<float*>(smem + p.off_U);                   // [own][R]
     float* unslice = reinterpret_cast<float*>(smem + p.off_un);                 // [own][K]
-    int* lr_ring = reinterpret_cast<int*>(smem + p.off_lr);                     // [LR_SLOTS][32]
     int* id_ring = reinterpret_cast<int*>(smem + p.off_ids);                    // [2][256]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     const uint32_t full0 = smem_u32(bars);
@@ -156,8 +160,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const uint32_t accum = empty0 + 8 * p.pstages;
     const uint32_t recv = accum + 8;
     const uint32_t drained = recv + 8;
-    const uint32_t ready0 = drained + 8;
-    const uint32_t sfree0 = ready0 + 8 * p.estages;
+    const uint32_t landed0 = drained + 8;  // [estages]: a unit's copies have landed
+    const uint32_t sfree0 = landed0 + 8 * p.estages;
     const uint32_t tfull0 = sfree0 + 8 * p.estages;
     const uint32_t tempty0 = tfull0 + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.pstages + 3 + 2 * p.estages + 4);
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
     auto init_edge_bars = [&]() {
         for (int i = 0; i < p.estages; ++i) {
-            mbar_init(ready0 + 8 * i, SEL_GTHREADS);
+            mbar_init(landed0 + 8 * i, SEL_GTHREADS);
             mbar_init(sfree0 + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -270,25 +274,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         int id_next = warp >= 8 ? load_id(0) : 0;
 
         // ---- gather issue of edge unit j (tile j / nhalf, rank half j % nhalf).
-        //      A new tile's ids go to slot t & 1 of the id ring and its local u-row
-        //      table to slot t % LR_SLOTS; the named barrier makes both visible to
-        //      all gather threads (and shows every slot being overwritten has
-        //      been read by all of them); then the next tile's id is loaded while
-        //      this one's rows are in flight.
+        //      A new tile's ids go to slot t & 1 of the id ring; the named barrier
+        //      makes them visible to all gather threads (and shows that the slot
+        //      being overwritten, last read while issuing tile t - 2, has been
+        //      read by all of them); then the next tile's id is loaded while this
+        //      one's rows are in flight.  The thread's arrive on landed[stage]
+        //      fires once all its copies so far have completed.
         auto issue_unit = [&](int j) {
             const int st = j % p.estages;
             const int t = j / p.nhalf;
             const int half = j - t * p.nhalf;
-            const int e0 = e_lo + t * TP;
-            const int cnt = min(TP, e_hi - e0);
+            const int cnt = min(TP, e_hi - (e_lo + t * TP));
             int* ids = id_ring + (t & 1) * 2 * EROWS;
             if (half == 0) {
                 ids[gtid] = id_next;
-                if (gtid < cnt) {
-                    const int e = e0 + gtid;
-                    const int s = e / nm1;
-                    lr_ring[(t % LR_SLOTS) * 32 + gtid] = s * p.n + (e - s * nm1) + 1 - pa;
-                }
                 named_bar_sync(1, SEL_GTHREADS);
                 id_next = load_id(t + 1);
             }
@@ -303,42 +302,25 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             const uint32_t sbB = sb + (uint32_t)(p.nkb_e * KB_OP);
             const int col = half * 64 * p.nkb_e + g_col;
             if (!*abort_flag) {
-                for (int k = 0, row = g_r0; row < rows_valid; ++k, row += row_step) {
-                    const uint32_t o = (uint32_t)(k * row_step * 128);
-                    cp_async16(sb + o, p.A + (size_t)ids[row] * R + col);
-                    cp_async16(sbB + o, p.B + (size_t)ids[EROWS + row] * R + col);
+                // the unit's ids first (at most 8 rows per thread), then its copies
+                int ia[8], ib[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int row = g_r0 + k * row_step;
+                    ia[k] = row < rows_valid ? ids[row] : 0;
+                    ib[k] = row < rows_valid ? ids[EROWS + row] : 0;
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int row = g_r0 + k * row_step;
+                    if (row < rows_valid) {
+                        const uint32_t o = (uint32_t)(k * row_step * 128);
+                        cp_async16(sb + o, p.A + (size_t)ia[k] * R + col);
+                        cp_async16(sbB + o, p.B + (size_t)ib[k] * R + col);
+                    }
                 }
             }
-            cp_commit();
-        };
-
-        // ---- gate of edge unit j in place: each thread its own A chunks,
-        //      A (.) u in fp32, rounded to bf16
-        auto gate_unit = [&](int j) {
-            const int st = j % p.estages;
-            const int t = j / p.nhalf;
-            const int half = j - t * p.nhalf;
-            const int rows_valid = min(TP, e_hi - (e_lo + t * TP)) << p.log2K;
-            const uint32_t sb = estage_base(st) + g_off;
-            const int col = half * 64 * p.nkb_e + g_col;
-            const int* lr = lr_ring + (t % LR_SLOTS) * 32;
-            if (*abort_flag) return;
-            for (int k = 0, row = g_r0; row < rows_valid; ++k, row += row_step) {
-                const float4* ur =
-                    reinterpret_cast<const float4*>(uslice + (size_t)lr[row >> p.log2K] * R + col);
-                const float4 u0 = ur[0];
-                const float4 u1 = ur[1];
-                const uint32_t off = sb + (uint32_t)(k * row_step * 128);
-                const uint4 a = lds_v4(off);
-                const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
-                const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
-                uint4 g;
-                g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
-                g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
-                g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
-                g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
-                st_shared_v4(off, g);
-            }
+            cp_async_mbar_arrive_noinc(landed0 + 8 * st);
         };
 
         // ================= phase A: projection of the row block (+ early gathers)
@@ -406,16 +388,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         }
 
         // ================= phase B: the split-d partial, then one cluster barrier
-        const int ew = warp - 4;  // tensor-memory lane quadrant of warps 4..7
+        // Every warp moves a quarter of the columns of its tensor-memory lane
+        // quadrant (warp % 4) into the outgoing partial buffer.
         if (tid == 0 && CS > 1)
             mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * row_bytes);
-        if (warp >= 4 && warp < 8) {
+        {
+            const int q = warp & 3;
+            const int cw = R >> 2;
+            const int c_lo = (warp >> 2) * cw;
             wait(accum, (uint32_t)rbi & 1u);
             tc_fence_after();
-            const int row = ew * 32 + lane;
-            for (int c0 = 0; c0 < R; c0 += 16) {
+            const int row = q * 32 + lane;
+            for (int c0 = c_lo; c0 < c_lo + cw; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)c0, v);
+                tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
                 tmem_ld_wait();
                 if (row < rows) {
                     float4* dst = reinterpret_cast<float4*>(out_f + (size_t)row * p.red_stride + c0);
@@ -460,6 +446,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 const int lr = qd / c4;
                 const int cc = (qd - lr * c4) * 4;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
                 for (int src = 0; src < CS; ++src) {  // rank order: deterministic
                     const float* srow =
                         src == rank ? out_f + (size_t)(o_lo + lr) * p.red_stride
@@ -475,99 +462,106 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + cc) = acc;
             }
         }
-        // unit 0 (copied into region E under the projection) is gated by every
-        // thread of the CTA: its copies are complete (each gather thread waits for
-        // its own), and the barrier makes them and the u slice visible to all
-        if (warp >= 8) cp_wait_pending(0);
-        __syncthreads();  // u slice complete; the receive slots are free; unit 0 landed
-        if (nunits > 0) {
-            const int t0rows = min(TP, e_hi - e_lo) << p.log2K;
-            const int* lr = lr_ring;  // tile 0's table (slot 0)
-            const int col0 = 0;
-            const int cpr = 8 * p.nkb_e;
-            if (!*abort_flag) {
-                for (int qd = tid; qd < t0rows * cpr; qd += SEL_THREADS) {
-                    const int row = qd >> log2cpr;
-                    const int kb = (qd >> 3) & (p.nkb_e - 1);
-                    const int ch = qd & 7;
-                    const int col = col0 + kb * 64 + ch * 8;
-                    const float4* ur =
-                        reinterpret_cast<const float4*>(uslice + (size_t)lr[row >> p.log2K] * R + col);
-                    const float4 u0 = ur[0];
-                    const float4 u1 = ur[1];
-                    const uint32_t off =
-                        sE + (uint32_t)(kb * KB_OP + row * 128 + ((ch ^ (row & 7)) << 4));
-                    const uint4 a = lds_v4(off);
-                    const float2 a0 = bf16x2_to_f2(a.x), a1 = bf16x2_to_f2(a.y);
-                    const float2 a2 = bf16x2_to_f2(a.z), a3 = bf16x2_to_f2(a.w);
-                    uint4 g;
-                    g.x = f2_to_bf16x2(a0.x * u0.x, a0.y * u0.y);
-                    g.y = f2_to_bf16x2(a1.x * u0.z, a1.y * u0.w);
-                    g.z = f2_to_bf16x2(a2.x * u1.x, a2.y * u1.y);
-                    g.w = f2_to_bf16x2(a3.x * u1.z, a3.y * u1.w);
-                    st_shared_v4(off, g);
-                }
-            }
-            fence_proxy_async_smem();
-        }
-        __syncthreads();
+        __syncthreads();  // u slice complete; the receive slots are free
 
         // ================= phase D: the edge tiles of this CTA's positions
         if (warp >= 8) {
-            // gather + gate: unit 0 is gated already; each later unit is gated as
-            // soon as its rows have landed, and only then are further units issued
-            // (up to estages - 1 ahead)
-            const int ahead = p.estages - 1;
-            int issued = nunits > 0 ? 1 : 0;
-            for (int j = 0; j < nunits; ++j) {
-                if (issued == j) issue_unit(issued++);
-                if (j > 0) {
-                    cp_wait_pending(issued - j - 1);
-                    gate_unit(j);
-                    fence_proxy_async_smem();
-                }
-                mbar_arrive(ready0 + 8 * (j % p.estages));
-                while (issued < nunits && issued <= j + ahead) issue_unit(issued++);
-            }
+            // gather: issue only; a stage is refilled once the MMA has consumed its
+            // previous unit (unit 0 was issued in phase A)
+            for (int j = 1; j < nunits; ++j) issue_unit(j);
             cp_async_wait_all();
             if (!drained_ok) wait(drained, (uint32_t)rbi & 1u);  // before region P is reused
-        } else if (warp == 1) {
-            if (lane == 0) {  // MMA issuer
-                constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-                for (int t = 0; t < ntile; ++t) {
-                    const int bb = t & 1;
-                    if (t >= 2) wait(tempty0 + 8 * bb, (((uint32_t)(t >> 1)) - 1u) & 1u);
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(EACC + bb * 128);
-                    for (int half = 0; half < p.nhalf; ++half) {
-                        const int j = t * p.nhalf + half;
-                        const int st = j % p.estages;
-                        wait(ready0 + 8 * st, ((uint32_t)(j / p.estages)) & 1u);
+        } else if (warp < 4) {
+            // gate: thread gt owns chunk column c of rows rg*cpr .. rg*cpr + cpr - 1
+            // (within one transition when K >= cpr, so u is read once per unit);
+            // A (.) u in fp32, rounded to bf16, in place; proxy fence; the named
+            // barrier shows the whole unit gated, and one thread issues its MMAs
+            const int cpr = 8 * p.nkb_e;
+            const int c = tid & (cpr - 1);
+            const int rg = tid >> log2cpr;
+            const int ch = c & 7;
+            const uint32_t c_off = (uint32_t)((c >> 3) * KB_OP);
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+            for (int j = 0; j < nunits; ++j) {
+                const int st = j % p.estages;
+                const int t = j / p.nhalf;
+                const int half = j - t * p.nhalf;
+                const int e0 = e_lo + t * TP;
+                const int rows_valid = min(TP, e_hi - e0) << p.log2K;
+                wait(landed0 + 8 * st, ((uint32_t)(j / p.estages)) & 1u);
+                const uint32_t sb = estage_base(st) + c_off;
+                const int col = half * 64 * p.nkb_e + c * 8;
+                if (!*abort_flag) {
+                    // four rows at a time (independent chains, so the loads and the
+                    // arithmetic of the four overlap); rows_valid is a multiple of
+                    // K >= 4, so a group is either wholly valid or wholly past the
+                    // end, and it lies within one transition
+                    int tr_cur = -1;
+                    float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 u1 = u0;
+                    for (int k0 = 0; k0 < cpr; k0 += 4) {
+                        const int row0 = rg * cpr + k0;
+                        if (row0 >= rows_valid) break;
+                        const int tr = row0 >> p.log2K;
+                        if (tr != tr_cur) {  // this transition's u row (local to the CTA)
+                            tr_cur = tr;
+                            const int e = e0 + tr;
+                            const int s = e / nm1;
+                            const int lr = s * p.n + (e - s * nm1) + 1 - pa;
+                            const float4* ur = reinterpret_cast<const float4*>(uslice + (size_t)lr * R + col);
+                            u0 = ur[0];
+                            u1 = ur[1];
+                        }
+                        uint32_t off[4];
+                        uint4 a[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int row = row0 + q;
+                            off[q] = sb + (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) a[q] = lds_v4(off[q]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) st_shared_v4(off[q], gate_chunk(a[q], u0, u1));
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(2, 128);
+                if (warp == 1) {
+                    if (lane == 0) {  // MMA issue for unit j
+                        const int bb = t & 1;
+                        if (half == 0 && t >= 2) wait(tempty0 + 8 * bb, (((uint32_t)(t >> 1)) - 1u) & 1u);
                         tc_fence_after();
+                        const uint32_t d = tmem + (uint32_t)(EACC + bb * 128);
                         const uint32_t sa = estage_base(st);
-                        const uint32_t sbb = sa + (uint32_t)(p.nkb_e * KB_OP);
+                        // the start-address field holds address / 16 and never
+                        // carries (shared addresses < 2^18), so a descriptor for
+                        // sa + off is the one for sa plus off / 16
+                        const uint64_t da = sw128_desc(sa);
+                        const uint64_t db = sw128_desc(sa + (uint32_t)(p.nkb_e * KB_OP));
                         if (!*abort_flag) {
                             for (int kb = 0; kb < p.nkb_e; ++kb)
 #pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    tc_mma_bf16(d, sw128_desc(sa + kb * KB_OP + 32 * k),
-                                                sw128_desc(sbb + kb * KB_OP + 32 * k), idesc,
+                                for (int k = 0; k < 4; ++k) {
+                                    const uint64_t step = (uint64_t)((kb * KB_OP + 32 * k) >> 4);
+                                    tc_mma_bf16(d, da + step, db + step, idesc,
                                                 (half > 0 || kb > 0 || k > 0) ? 1u : 0u);
+                                }
                         }
                         tc_commit(sfree0 + 8 * st);
+                        if (half == p.nhalf - 1) tc_commit(tfull0 + 8 * bb);
                     }
-                    tc_commit(tfull0 + 8 * bb);
+                    __syncwarp();
                 }
             }
-            __syncwarp();
-        } else if (warp >= 4) {
-            // epilogue: one thread per predecessor row of the tile; its unary
-            // scores come from the staged slice
+        } else {
+            // epilogue (warps 4-7): one thread per predecessor row of the tile; its
+            // unary scores come from the staged slice
+            const int ew = warp - 4;  // tensor-memory lane quadrant
             const int r = ew * 32 + lane;
             const int pslot = r & (K - 1);
             const int blk0 = r & ~(K - 1);
-            const int colbase = K >= 32 ? blk0 : 32 * ew;  // warp-uniform
-            const int nchunk = (K >= 32 ? K : 32) >> 4;     // 16-column chunks
+            const uint32_t lane_base = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)EACC;
             for (int t = 0; t < ntile; ++t) {
                 const int bb = t & 1;
                 const int e0 = e_lo + t * TP;
@@ -584,52 +578,114 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 float* erow = (p.edges_out != nullptr && valid)
                                   ? p.edges_out + ((size_t)e * K + pslot) * K
                                   : nullptr;
-                wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
-                tc_fence_after();
+                const uint32_t acc_base = lane_base + (uint32_t)(bb * 128);
                 float best = 0.f;
                 int arg = -1;
-#pragma unroll 1
-                for (int ch = 0; ch < nchunk; ++ch) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem + ((uint32_t)(ew * 32) << 16) +
-                                           (uint32_t)(EACC + bb * 128 + colbase + ch * 16),
-                                       v);
-                    tmem_ld_wait();
-                    const int c0 = colbase + ch * 16 - blk0;  // slot of column jj = 0
-                    if (valid && c0 + 16 > 0 && c0 < K) {
-                        // every read in bounds (slot masked into the row), so the 16
-                        // shared loads issue together; slots outside this lane's
-                        // block are masked out of the argmax
-                        float ev[16];
+                if (K >= 16) {
+                    // the lane's own block in chunks of 16 slots (columns blk0 + 16 ch):
+                    // no masking; for K = 16 the warp's two blocks come from one
+                    // 32-column load and each lane keeps its half
+                    const float4* un4 = reinterpret_cast<const float4*>(un);
+                    float4 uq[4];
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            ev[jj] = __uint_as_float(v[jj]) + un[(c0 + jj) & (K - 1)];
-                        if (erow != nullptr) {
+                    for (int q = 0; q < 4; ++q) uq[q] = un4[q];  // before the accumulator is ready
+                    wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < (K >> 4); ++ch) {
+                        if (ch > 0) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) uq[q] = un4[4 * ch + q];
+                        }
+                        float ev[16];
+                        if (K == 16) {
+                            uint32_t v[32];
+                            tmem_ld_32x32b_x32(acc_base + (uint32_t)(32 * ew), v);
+                            tmem_ld_wait();
+                            const bool hi = (lane & 16) != 0;
 #pragma unroll
                             for (int jj = 0; jj < 16; ++jj)
-                                if (c0 + jj >= 0 && c0 + jj < K) erow[c0 + jj] = ev[jj];
+                                ev[jj] = __uint_as_float(hi ? v[16 + jj] : v[jj]);
+                        } else {
+                            uint32_t v[16];
+                            tmem_ld_32x32b_x16(acc_base + (uint32_t)(blk0 + 16 * ch), v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) ev[jj] = __uint_as_float(v[jj]);
                         }
-                        // argmax by a tree over index order: on equal values the
-                        // left (lower) slot is kept, as in a scan with a strict ">"
-                        float bv[16];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            ev[4 * q] += uq[q].x;
+                            ev[4 * q + 1] += uq[q].y;
+                            ev[4 * q + 2] += uq[q].z;
+                            ev[4 * q + 3] += uq[q].w;
+                        }
+                        if (erow != nullptr) {  // the caller's buffer: no alignment assumed
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) erow[16 * ch + jj] = ev[jj];
+                        }
+                        // argmax by a tree over slot order: on equal values the left
+                        // (lower) slot is kept, as in a scan with a strict ">"
                         int bi[16];
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const bool in = c0 + jj >= 0 && c0 + jj < K;
-                            bv[jj] = in ? ev[jj] : -INFINITY;
-                            bi[jj] = in ? c0 + jj : K;
-                        }
+                        for (int jj = 0; jj < 16; ++jj) bi[jj] = 16 * ch + jj;
 #pragma unroll
                         for (int w = 1; w < 16; w <<= 1)
 #pragma unroll
                             for (int jj = 0; jj < 16; jj += 2 * w)
-                                if (bv[jj + w] > bv[jj] || (bi[jj] == K && bi[jj + w] < K)) {
-                                    bv[jj] = bv[jj + w];
+                                if (ev[jj + w] > ev[jj]) {
+                                    ev[jj] = ev[jj + w];
                                     bi[jj] = bi[jj + w];
                                 }
-                        if (arg < 0 || bv[0] > best) {  // chunks come in slot order
-                            best = bv[0];
+                        if (arg < 0 || ev[0] > best) {  // chunks come in slot order
+                            best = ev[0];
                             arg = bi[0];
+                        }
+                    }
+                } else {
+                    // K = 4 or 8: a warp's 32 columns hold several blocks; each lane
+                    // masks the slots outside its own
+                    wait(tfull0 + 8 * bb, ((uint32_t)(t >> 1)) & 1u);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(acc_base + (uint32_t)(32 * ew + ch * 16), v);
+                        tmem_ld_wait();
+                        const int c0 = 32 * ew + ch * 16 - blk0;  // slot of column jj = 0
+                        if (valid && c0 + 16 > 0 && c0 < K) {
+                            // every read in bounds (slot masked into the row), so the 16
+                            // shared loads issue together; slots outside this lane's
+                            // block are masked out of the argmax
+                            float ev[16];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                ev[jj] = __uint_as_float(v[jj]) + un[(c0 + jj) & (K - 1)];
+                            if (erow != nullptr) {
+#pragma unroll
+                                for (int jj = 0; jj < 16; ++jj)
+                                    if (c0 + jj >= 0 && c0 + jj < K) erow[c0 + jj] = ev[jj];
+                            }
+                            float bv[16];
+                            int bi[16];
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const bool in = c0 + jj >= 0 && c0 + jj < K;
+                                bv[jj] = in ? ev[jj] : -INFINITY;
+                                bi[jj] = in ? c0 + jj : K;
+                            }
+#pragma unroll
+                            for (int w = 1; w < 16; w <<= 1)
+#pragma unroll
+                                for (int jj = 0; jj < 16; jj += 2 * w)
+                                    if (bv[jj + w] > bv[jj] || (bi[jj] == K && bi[jj + w] < K)) {
+                                        bv[jj] = bv[jj + w];
+                                        bi[jj] = bi[jj + w];
+                                    }
+                            if (arg < 0 || bv[0] > best) {  // chunks come in slot order
+                                best = bv[0];
+                                arg = bi[0];
+                            }
                         }
                     }
                 }
@@ -650,7 +706,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         if (rb + nclusters < p.nrb) {
             if (tid == 0) {
                 for (int i = 0; i < p.estages; ++i) {
-                    mbar_inval(ready0 + 8 * i);
+                    mbar_inval(landed0 + 8 * i);
                     mbar_inval(sfree0 + 8 * i);
                 }
                 for (int i = 0; i < 2; ++i) {
@@ -689,7 +745,7 @@ struct Plan {
     bool ok = false;
     int CS = 0, NC = 0, MR = 0, nrb = 0, own_max = 0, pstages = 0, estages = 0, nkb_e = 0, nhalf = 0;
     int drain_stage = 0;
-    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_un = 0, off_lr = 0;
+    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_un = 0;
     uint32_t off_ids = 0, off_bar = 0, red_stride = 0;
     size_t smem = 0;
 };
@@ -704,8 +760,8 @@ int g_plan_next = 0;
 // Shared-memory layout for a cluster size and row-block height; false when it
 // does not fit.  Region E = edge stage 0.  Region P = the projection's TMA ring,
 // then the receive slots [CS-1][own_max] and the outgoing partial [MR] (rows of
-// R + 4 floats), then edge stages 1..estages-1.  Then the u slice, the local
-// u-row ring, the id ring and the barriers.
+// R + 4 floats), then edge stages 1..estages-1.  Then the u slice, the unary
+// slice, the id ring and the barriers.
 bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     q->nkb_e = R >= 128 ? 2 : 1;
     q->nhalf = R / (64 * q->nkb_e);
@@ -726,8 +782,7 @@ bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
         const int es = 1 + (int)std::min<size_t>(3, regionP / q->estage_bytes);
         const size_t off_U = q->estage_bytes + regionP;
         const size_t off_un = off_U + ((u_bytes + 15) & ~(size_t)15);
-        const size_t off_lr = off_un + ((un_bytes + 15) & ~(size_t)15);
-        const size_t off_ids = off_lr + LR_SLOTS * 32 * 4;
+        const size_t off_ids = off_un + ((un_bytes + 15) & ~(size_t)15);
         const size_t off_bar = off_ids + 2 * 2 * EROWS * 4;
         const size_t total = 1024 + off_bar + bar_bytes;
         if (total <= max_smem && es >= 2) {
@@ -737,7 +792,6 @@ bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
             q->off_out = (uint32_t)off_out;
             q->off_U = (uint32_t)off_U;
             q->off_un = (uint32_t)off_un;
-            q->off_lr = (uint32_t)off_lr;
             q->off_ids = (uint32_t)off_ids;
             q->off_bar = (uint32_t)off_bar;
             // first edge stage in region P whose bytes overlap the outgoing partial
@@ -888,7 +942,6 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     p.off_out = pl.off_out;
     p.off_U = pl.off_U;
     p.off_un = pl.off_un;
-    p.off_lr = pl.off_lr;
     p.off_ids = pl.off_ids;
     p.off_bar = pl.off_bar;
     p.drain_stage = pl.drain_stage;
