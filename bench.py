@@ -42,8 +42,8 @@ P_MIN = 0.05  # draft-probability cut of the chain readout line
 # sha256 of the kernel source they were taken on (null when the source changed).
 TRAFFIC = {
     ("batched_256x16_d5120", "dynconv"): {
-        "sha": "47572124d5f40e41464a543ea1c97502bb69257dab6c86207b28879788e5e683",
-        "bytes": 51192576 + 2756096,  # dram__bytes_read.sum + dram__bytes_write.sum
+        "sha": "e9197ae2ff306d3620f91b165556f0d75e0efd53ff770d9554c96506d6a3ee70",
+        "bytes": 51192064 + 3260160,  # dram__bytes_read.sum + dram__bytes_write.sum
     },
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
@@ -52,8 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311424512 + 3649536),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "e9b14497aa801678e415732d889b63706c75bb9344cb20e89554b9a05da59529",
-        "bytes": 69823232 + 1617920,
+        "sha": "b2f7bd295117698f168d41f4f62ac5a9f589194fc622a5bdbae457eae896f5a3",
+        "bytes": 69819648 + 1421824,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
