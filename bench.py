@@ -717,6 +717,23 @@ def main():
         t_topk = _timed_eager(K_iso, stream, flush, [(f_topk, topk_args)], L)[0]
     topk_b = P * w.V * 4 + P * w.K * 8
     topk_us = 1000.0 * statistics.mean(t_topk)
+    # the same extraction for one draft block (one sequence's n rows): the decode
+    # case, latency-bound; fp32 and bf16 rows
+    blk = {}
+    for lname, lt in (("f32", logits[:w.n]), ("bf16", logits[:w.n].to(torch.bfloat16))):
+        lt = lt.contiguous()
+        b_args = (ptr(lt), w.n, w.V, w.K, 1 if lname == "bf16" else 0, ptr(tk_ids), ptr(tk_vals),
+                  sp)
+        _call(f_topk, b_args, L)
+        if record_ext is not None:
+            tb = _timed_graph(K_iso, stream, flush, [(f_topk, b_args)], record_ext, L)[0]
+        else:
+            tb = _timed_eager(K_iso, stream, flush, [(f_topk, b_args)], L)[0]
+        bb = w.n * w.V * (2 if lname == "bf16" else 4) + w.n * w.K * 8
+        bu = 1000.0 * statistics.mean(tb)
+        blk[lname] = {"us": bu, "bytes": bb, "GB/s": bb / bu / 1e3,
+                      "frac_hbm": bb / bu / 1e3 / _peaks()[0]}
+        del lt
     del logits
     # delta predictor (delta = x . Wc^T, the conv's taps from its input), bf16 on
     # the tensor cores; the conv inputs of the step
@@ -965,6 +982,9 @@ def main():
                      "rows": P, "V": w.V, "K": w.K, "logits": "f32",
                      "GB/s": topk_b / topk_us / 1e3, "frac_hbm": topk_b / topk_us / 1e3 / hbm,
                      "note": "not part of the timed step; candidate extraction before it"},
+            "topk_draft_block": {"isolated": True, "steps": K_iso, "rows": w.n, "V": w.V,
+                                 "K": w.K, **blk,
+                                 "note": "one sequence's draft block (the decode case)"},
         },
         "gather_ceiling": gather,
         "workloads": workloads,

@@ -1557,9 +1557,211 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
     if (cs > 1) cluster_sync();
 }
 
+// ---------------------------------------------------------------- few rows
+// topk_rows_kernel (K <= 32, rows few enough that one cluster per row fits the
+// GPU at once, as for a draft block's 16 rows): the per-row fixed costs of the
+// streaming kernels (seeding, queue hand-offs, the joint selection) dominate
+// there, so this kernel reads its chunk of the row into registers in one go
+// and selects in a few block-wide steps:
+//  1. CTA r of the row's cluster owns elements [r*chunk, (r+1)*chunk) (chunk a
+//     multiple of one 16-byte vector); thread t holds vectors t, t + 512, ...
+//     (at most VPT), all loaded up front with 16-byte read-only loads;
+//  2. each thread's best key (NaN skipped); the 512 keys are sorted by warp
+//     bitonic sorts and pairwise bitonic merges, and the K-th largest, tau,
+//     bounds the chunk's K-th best key from below (the K thread maxima at or
+//     above it are K distinct elements);
+//  3. every element with key >= tau joins a shared candidate list: only the K
+//     threads whose maximum is at or above tau can contribute, so the list
+//     holds at most K times a thread's element count; up to 512 candidates
+//     are sorted by the same warp sorts and merges, only as many lists as they
+//     fill (more, only possible for adversarial chunks, are first cut to the K
+//     best by an exact select);
+//  4. the other ranks store their sorted lists into rank 0's shared memory
+//     (distributed shared memory) before one cluster barrier; rank 0 merges
+//     them pairwise and writes the row from the sorted result.
+// Keys, ties, NaN and the sign of zero follow the streaming kernels exactly.
+constexpr int kRowsMaxK = 32;
+constexpr int kRowsThreads = 512;                  // the first kNC run the exact select
+constexpr int kRowsVpts[5] = {4, 8, 12, 16, 20};   // 16-byte vectors per thread
+constexpr int kRowsMaxVpt = 20;
+constexpr int kRowsCap = kRowsMaxK * kRowsMaxVpt * 8;  // candidate keys at most (bf16)
+
+struct RowsSmem {
+    uint64_t cand[kRowsCap];
+    uint64_t lists[kRowsThreads];          // sorted keys, 16 x 32
+    uint64_t merge[8 * 32];                // rank r's sorted top 32 (rank 0's copy)
+    uint64_t tmp[kRowsMaxK];
+    uint32_t hist[256];
+    Ctl ctl;
+};
+
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// Pairwise merges of n (a power of two, <= 16) descending 32-key lists held at
+// lists[32*w .. 32*w + 31] into the sorted top 32 at lists[0 .. 31];
+// block-collective (every thread calls it).
+__device__ __forceinline__ void rows_merge_lists(uint64_t* lists, int n) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+#pragma unroll 1
+    for (int step = 1; step < n; step <<= 1) {
+        if ((warp & (2 * step - 1)) == 0 && warp + step < n) {
+            const uint64_t m = warp_merge_desc(lists[warp * 32 + lane], lists[(warp + step) * 32 + lane]);
+            __syncwarp();
+            lists[warp * 32 + lane] = m;
+        }
+        __syncthreads();
+    }
+}
+
+// Element j (in index order) of a 16-byte vector: fp32 4 per vector, bf16 8.
+template <bool BF16>
+__device__ __forceinline__ float rows_elem(const uint4& w, int j) {
+    const uint32_t q = j < (BF16 ? 2 : 1) ? w.x : j < (BF16 ? 4 : 2) ? w.y : j < (BF16 ? 6 : 3) ? w.z : w.w;
+    if constexpr (BF16) return __uint_as_float((j & 1) ? (q & 0xFFFF0000u) : (q << 16));
+    return __uint_as_float(q);
+}
+
+template <bool BF16, int VPT>
+__global__ void __launch_bounds__(kRowsThreads, 1) topk_rows_kernel(const TopkParams p) {
+    constexpr int EPV = BF16 ? 8 : 4;  // elements per 16-byte vector
+    extern __shared__ __align__(16) uint8_t rows_smem_raw[];
+    RowsSmem& sm = *reinterpret_cast<RowsSmem*>(rows_smem_raw);
+    const int tid = threadIdx.x;
+    const int P = p.cs;
+    const int rank = P > 1 ? (int)cluster_ctarank() : 0;
+    const int row = blockIdx.x / P;
+    const int K = p.K;
+    // chunk: a multiple of EPV elements (the launcher checked that the row
+    // starts are 16-byte aligned and that a chunk fits VPT vectors per thread)
+    const int chunk = ((p.V + P - 1) / P + EPV - 1) / EPV * EPV;
+    const int c0 = min(p.V, rank * chunk);
+    const int c1 = min(p.V, c0 + chunk);
+    const int nvec = (c1 - c0) / EPV;  // V is a multiple of EPV
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.logits) +
+                                                      ((size_t)row * p.V + c0) * (BF16 ? 2 : 4));
+
+    // 1. the thread's vectors (NaN words past the end: never candidates)
+    constexpr uint32_t kNaNWord = BF16 ? 0x7FC07FC0u : 0x7FC00000u;
+    uint4 w[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = tid + kRowsThreads * k;
+        w[k] = v < nvec ? ldg_nc_v4(src + v) : make_uint4(kNaNWord, kNaNWord, kNaNWord, kNaNWord);
+    }
+    if (tid == 0) sm.ctl.count = 0u;
+
+    // 2. the thread's best key (0: no non-NaN element), then tau.  Over
+    // increasing indices a strict ">" keeps the first of equal values (-0 and
+    // +0 compare equal, as the keys order them) and skips NaN; a thread whose
+    // non-NaN elements are all -inf sets nothing and takes its first one.
+    float mx = -INFINITY;
+    int bi = -1, first = -1;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) {
+            const float x = rows_elem<BF16>(w[k], j);
+            const int idx = c0 + (tid + kRowsThreads * k) * EPV + j;
+            if (x > mx) {
+                mx = x;
+                bi = idx;
+            }
+            if (first < 0 && x == x) first = idx;
+        }
+    if (bi < 0) bi = first;  // all -inf (mx stays -inf), or none (bi = -1)
+    const uint64_t best = bi < 0 ? 0ull : make_key(mx, (uint32_t)bi);
+    sm.lists[tid] = warp_sort_desc(best);
+    __syncthreads();
+    rows_merge_lists(sm.lists, kRowsThreads / 32);
+    // tau = the K-th key; with fewer than K thread maxima (key 0) every non-NaN
+    // element passes: the bound (-inf, last index) below every key
+    const uint64_t tau = sm.lists[K - 1];
+    const float tv = tau == 0 ? -INFINITY : key_value(tau);
+    const uint32_t ti = tau == 0 ? 0xFFFFFFFFu : key_index(tau);
+
+    // 3. candidates: key >= tau, i.e. value > tv, or value == tv (-0 == +0)
+    // at an index <= ti; a compare per element into a mask, the exact test and
+    // the append only for the rare vectors with an element at or above tv
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) m |= (rows_elem<BF16>(w[k], j) >= tv ? 1u : 0u) << j;
+        if (m != 0) {
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) {
+                if (!((m >> j) & 1u)) continue;
+                const float x = rows_elem<BF16>(w[k], j);
+                const uint32_t idx = (uint32_t)(c0 + (tid + kRowsThreads * k) * EPV + j);
+                if (x > tv || idx <= ti) {
+                    const uint32_t pos = atomicAdd(&sm.ctl.count, 1u);
+                    if (pos < (uint32_t)kRowsCap)
+                        sm.cand[pos] = make_key(x, idx);
+                    else
+                        atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    int M = min((int)sm.ctl.count, kRowsCap);
+    // the CTA's K best, sorted: at most 512 candidates are sorted directly
+    // (one key per thread, missing ones as key 0); more (only for adversarial
+    // chunks) are first cut to the K best by the exact radix / counting select
+    if (M > kRowsThreads) {
+        if (tid < kNC) select_keep(sm.cand, M, K, sm.tmp, sm.hist, &sm.ctl);
+        M = K;
+        __syncthreads();
+    }
+    // sorted lists of 32 (the last padded with key 0), merged pairwise
+    int nl = 1;
+    while (nl * 32 < M) nl <<= 1;
+    if ((tid >> 5) < nl) sm.lists[tid] = warp_sort_desc(tid < M ? sm.cand[tid] : 0ull);
+    __syncthreads();
+    rows_merge_lists(sm.lists, nl);
+
+    // 4. the cluster's sorted lists meet in rank 0, which merges them
+    const uint64_t* top = sm.lists;
+    if (P > 1) {
+        if (rank == 0) {
+            if (tid < 32) sm.merge[tid] = sm.lists[tid];
+        } else if (tid < 32) {
+            const uint32_t a = smem_u32(sm.merge) + (uint32_t)((rank * 32 + tid) * 8);
+            st_cluster_u64(map_cluster(a, 0u), sm.lists[tid]);
+        }
+        cluster_sync();  // release / acquire: the lists are in rank 0
+        if (rank != 0) return;
+        rows_merge_lists(sm.merge, P);
+        top = sm.merge;
+    }
+    // 5. the row, straight from the sorted list (key 0: fewer than K entries)
+    if (tid < K) {
+        const uint64_t k = top[tid];
+        int32_t id = -1;
+        float v = __uint_as_float(0x7FC00000u);
+        if (k != 0) {
+            id = (int32_t)key_index(k);
+            v = key_value(k);  // exact, except that the key folded -0 onto +0
+            if ((uint32_t)id >= (uint32_t)p.V) {  // not reachable with distinct keys
+                atomicOr(&g_topk_fault, (unsigned)DF2_FLAG_OVERFLOW);
+                id = -1;
+                v = __uint_as_float(0x7FC00000u);
+            } else if (v == 0.f) {
+                v = load_logit<BF16>(p.logits, (size_t)row * p.V + (uint32_t)id);
+            }
+        }
+        p.ids[(size_t)row * K + tid] = id;
+        p.vals[(size_t)row * K + tid] = v;
+    }
+}
+
 struct DeviceInfo {
     bool ready = false;
     int max_clusters[2][2][4] = {};  // [async][bf16][log2 cs]: clusters resident at once
+    int rows_clusters[2][5][4] = {};  // few-row kernel: [bf16][VPT index][log2 cluster size]
 };
 
 std::mutex g_mu;
@@ -1600,7 +1802,39 @@ cudaError_t query_device(DeviceInfo& d) {
         e = query_kernel(topk_async_kernel<false>, kASmem, kAThreads, d.max_clusters[1][0]);
     if (e == cudaSuccess)
         e = query_kernel(topk_async_kernel<true>, kASmem, kAThreads, d.max_clusters[1][1]);
+    constexpr uint32_t rs = (uint32_t)sizeof(RowsSmem);
+#define DF2_ROWS_Q(BF, I)                                                                         \
+    if (e == cudaSuccess)                                                                         \
+        e = query_kernel(topk_rows_kernel<BF, kRowsVpts[I]>, rs, kRowsThreads,                    \
+                         d.rows_clusters[BF ? 1 : 0][I]);
+    DF2_ROWS_Q(false, 0) DF2_ROWS_Q(false, 1) DF2_ROWS_Q(false, 2) DF2_ROWS_Q(false, 3)
+    DF2_ROWS_Q(false, 4) DF2_ROWS_Q(true, 0) DF2_ROWS_Q(true, 1) DF2_ROWS_Q(true, 2)
+    DF2_ROWS_Q(true, 3) DF2_ROWS_Q(true, 4)
+#undef DF2_ROWS_Q
     return e;
+}
+
+template <bool BF16>
+cudaError_t launch_rows(const TopkParams& p, int vi, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(p.rows * p.cs), 1, 1);
+    cfg.blockDim = dim3(kRowsThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(RowsSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.cs > 1 ? 1 : 0;
+    switch (vi) {
+        case 0: return cudaLaunchKernelEx(&cfg, topk_rows_kernel<BF16, kRowsVpts[0]>, p);
+        case 1: return cudaLaunchKernelEx(&cfg, topk_rows_kernel<BF16, kRowsVpts[1]>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, topk_rows_kernel<BF16, kRowsVpts[2]>, p);
+        case 3: return cudaLaunchKernelEx(&cfg, topk_rows_kernel<BF16, kRowsVpts[3]>, p);
+        default: return cudaLaunchKernelEx(&cfg, topk_rows_kernel<BF16, kRowsVpts[4]>, p);
+    }
 }
 
 cudaError_t launch_any(const TopkLaunch& a, cudaStream_t stream) {
@@ -1610,6 +1844,7 @@ cudaError_t launch_any(const TopkLaunch& a, cudaStream_t stream) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const bool async = a.K <= kAsyncMaxK;
     int maxc[4];
+    int rows_cs = 0, rows_vi = 0;  // the few-row kernel's cluster size and vectors per thread
     {
         std::lock_guard<std::mutex> lk(g_mu);
         DeviceInfo& d = g_info[dev];
@@ -1619,6 +1854,29 @@ cudaError_t launch_any(const TopkLaunch& a, cudaStream_t stream) {
             d.ready = true;
         }
         for (int l = 0; l < 4; ++l) maxc[l] = d.max_clusters[async ? 1 : 0][a.bf16 ? 1 : 0][l];
+        // few rows, small K: one cluster per row if the whole batch fits at once
+        // (the largest cluster, for the most parallel reads), each CTA's chunk
+        // in its registers, 16-byte aligned
+        const int esz = a.bf16 ? 2 : 4;
+        if (a.K <= kRowsMaxK && (a.V * esz) % 16 == 0 &&
+            reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) {
+            for (int l = 3; l >= 0 && rows_cs == 0; --l) {
+                const int P = 1 << l;
+                const long long vecs = ((long long)(a.V + P - 1) / P * esz + 15) / 16 + 1;
+                const long long vpt = (vecs + kRowsThreads - 1) / kRowsThreads;
+                int vi = 0;
+                while (vi < 5 && kRowsVpts[vi] < vpt) ++vi;
+                if (vi == 5) break;  // smaller clusters: longer chunks
+                if (a.rows <= d.rows_clusters[a.bf16 ? 1 : 0][vi][l]) {
+                    rows_cs = P;
+                    rows_vi = vi;
+                }
+            }
+        }
+    }
+    if (rows_cs > 0) {
+        const TopkParams rp{a.logits, a.rows, a.V, a.K, rows_cs, a.ids, a.vals};
+        return a.bf16 ? launch_rows<true>(rp, rows_vi, stream) : launch_rows<false>(rp, rows_vi, stream);
     }
     // cluster size: the fewest waves of the longest per-CTA chunk, plus a fixed
     // per-row cost (seeding, selection, merge) worth about 8192 elements
