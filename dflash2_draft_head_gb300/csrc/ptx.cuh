@@ -160,12 +160,6 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
     return v;
 }
 
-// Asks L2 to fetch the 128-byte line holding `p` (kept with evict-last priority);
-// nothing is returned to the SM.
-__device__ __forceinline__ void prefetch_l2_last(const void* p) {
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -35,11 +35,10 @@
 //    issue copies (completion is counted on the stage's mbarrier by
 //    cp.async.mbarrier.arrive.noinc): a warp that also read back what it
 //    copied would stall its own next copies.  The first stage's copies are
-//    issued at kernel start, under the projection, and every later tile's
-//    rows are prefetched into L2 then.  4 gate warps form A (.) u in place
-//    (fp32 product, rounded to bf16) once a stage has landed, fence the async
-//    proxy and meet at a named barrier, after which one of their threads
-//    issues tcgen05.mma (M = N = 128) into one of two tensor-memory
+//    issued at kernel start, under the projection.  4 gate warps form
+//    A (.) u in place (fp32 product, rounded to bf16) once a stage has landed,
+//    fence the async proxy and meet at a named barrier, after which one of
+//    their threads issues tcgen05.mma (M = N = 128) into one of two tensor-memory
 //    accumulators; 4 epilogue warps read back only each transition's K x K
 //    diagonal block, add unary, keep the running argmax (lowest slot on ties)
 //    and store.
@@ -362,20 +361,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             }
             __syncwarp();
         } else if (warp >= 8) {
-            if (nunits > 0) issue_unit(0);  // region E is free: start the first gathers now
-            // The later tiles' rows cannot land in shared memory yet (region P is
-            // the projection's ring): ask L2 for them now, so that their gathers
-            // in phase D hit L2 while HBM serves this phase.
-            if (!*abort_flag) {
-                const int lines = R / 64;  // 128-byte lines per bf16 row
-#pragma unroll 2
-                for (int qd = gtid; qd < (ntile - 1) * 2 * EROWS; qd += SEL_GTHREADS) {
-                    const int id = id_of(1 + qd / (2 * EROWS), qd & (2 * EROWS - 1));
-                    if (id < 0) continue;
-                    const __nv_bfloat16* row = ((qd & (2 * EROWS - 1)) < EROWS ? p.A : p.B) + (size_t)id * R;
-                    for (int l = 0; l < lines; ++l) prefetch_l2_last(row + l * 64);
-                }
-            }
+            // region E is free: the first unit's gathers run under the projection.
+            // The later units are gathered in phase D straight from HBM: asking
+            // L2 for their rows here (prefetch) measured no faster on the batched
+            // and wide workloads, whose edge phase is bound by the gate and MMA
+            // chain, and 2 us slower on a single draft block.
+            if (nunits > 0) issue_unit(0);
         }
         pit += kb1 - kb0;
         // the epilogue warps, idle until the partial is ready, stage the unary
