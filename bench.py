@@ -52,8 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311424512 + 3649536),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "b2f7bd295117698f168d41f4f62ac5a9f589194fc622a5bdbae457eae896f5a3",
-        "bytes": 69819648 + 1421824,
+        "sha": "db9a25287a30dc5515d512261d00c9a9b376a288ac0c73f8f57447f3d0db6f28",
+        "bytes": 69812736 + 1130240,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
