@@ -30,6 +30,10 @@
 // or an 8-bit-digit radix select) and tighten the threshold to the K-th value;
 // elements tested later have larger indices, so the strict test x > tau is
 // exact there.
+// topk_rows_kernel (K <= 32, few 16-byte-aligned rows, one cluster per row all
+// resident at once, as for one draft block): no streaming; each CTA holds its
+// chunk of the row in registers and selects in a few block-wide steps (see the
+// section header further down).
 // NaN entries never pass a test; rows with fewer than K other entries get
 // id -1 and value NaN in the remaining slots.
 #include <cuda_runtime.h>
