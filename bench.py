@@ -48,8 +48,8 @@ TRAFFIC = {
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
     ("batched_256x16_d5120", "topk"): {
-        "sha": "ba528104f498b57b66ed7ce720e829e70da5c4cdac4644f7ceaa22e20a4d59db",  # capture taken before a comment-only edit of the file
-        "bytes": 8 * (311424512 + 3649536),
+        "sha": "51944453c7adcd3de91c05c4fcfa47165324136335a91958d79abf62d059e449",
+        "bytes": 8 * (311331840 + 3218176),
     },
     ("batched_256x16_d5120", "select"): {
         "sha": "db9a25287a30dc5515d512261d00c9a9b376a288ac0c73f8f57447f3d0db6f28",
