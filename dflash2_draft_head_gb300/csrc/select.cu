@@ -34,12 +34,13 @@
 //    straight into the tensor core's 128-byte-swizzle K-major layout and only
 //    issue copies (completion is counted on the stage's mbarrier by
 //    cp.async.mbarrier.arrive.noinc): a warp that also read back what it
-//    copied would stall its own next copies.  The first stage's copies are
-//    issued at kernel start, under the projection.  4 gate warps form
-//    A (.) u in place (fp32 product, rounded to bf16) once a stage has landed,
-//    fence the async proxy and meet at a named barrier, after which one of
-//    their threads issues tcgen05.mma (M = N = 128) into one of two tensor-memory
-//    accumulators; 4 epilogue warps read back only each transition's K x K
+//    copied would stall its own next copies.  The projection's TMA ring spans
+//    the edge stages' memory; the first stage's copies are issued as soon as
+//    the projection's MMAs are done, under the exchange of partials.  4 gate
+//    warps form A (.) u in place (fp32 product, rounded to bf16) once a stage
+//    has landed, fence the async proxy and meet at a named barrier, after
+//    which one of their threads issues tcgen05.mma (M = N = 128) into one of
+//    two tensor-memory accumulators; 4 epilogue warps read back only each transition's K x K
 //    diagonal block, add unary, keep the running argmax (lowest slot on ties)
 //    and store.
 // Every wait on an mbarrier is bounded by the global timer; on a timeout the
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     wait(empty0 + 8 * st, (((uint32_t)(it / p.pstages)) & 1u) ^ 1u);
                     if (*abort_flag) continue;
                     const uint32_t fb = full0 + 8 * st;
-                    const uint32_t dst = sP + (uint32_t)st * p.pstage_bytes;
+                    const uint32_t dst = sE + (uint32_t)st * p.pstage_bytes;
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(dst, &tmH, fb, kb * 64, row0);
                     tma_load_2d(dst + HTILE, &tmW, fb, kb * 64, 0);
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     const int st = it % p.pstages;
                     wait(full0 + 8 * st, ((uint32_t)(it / p.pstages)) & 1u);
                     tc_fence_after();
-                    const uint32_t a0 = sP + (uint32_t)st * p.pstage_bytes;
+                    const uint32_t a0 = sE + (uint32_t)st * p.pstage_bytes;
                     const uint32_t b0 = a0 + HTILE;
                     if (!*abort_flag) {
 #pragma unroll
@@ -361,12 +362,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             }
             __syncwarp();
         } else if (warp >= 8) {
-            // region E is free: the first unit's gathers run under the projection.
-            // The later units are gathered in phase D straight from HBM: asking
-            // L2 for their rows here (prefetch) measured no faster on the batched
-            // and wide workloads, whose edge phase is bound by the gate and MMA
-            // chain, and 2 us slower on a single draft block.
-            if (nunits > 0) issue_unit(0);
         }
         pit += kb1 - kb0;
         // the epilogue warps, idle until the partial is ready, stage the unary
@@ -427,13 +422,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                                    (uint32_t)(d_hi - d_lo) * row_bytes, map_cluster(recv, (uint32_t)dst));
                 }
             }
-            wait(recv, (uint32_t)rbi & 1u);
-            if (tid < CS && tid != rank) mbar_arrive_remote(map_cluster(drained, (uint32_t)tid));
+            if (warp < 8) {
+                wait(recv, (uint32_t)rbi & 1u);
+                if (tid < CS && tid != rank) mbar_arrive_remote(map_cluster(drained, (uint32_t)tid));
+            }
         }
+        // every MMA has read its stage, so region E (the ring's first stages) is
+        // free: the gather warps copy the first unit's rows while warps 0-7 sum
+        // the partials.  The later units are gathered in phase D straight from
+        // HBM (an L2 prefetch of their rows measured no faster).
+        if (warp >= 8 && nunits > 0) issue_unit(0);
         {
             const int own = o_hi - o_lo;
             const int c4 = R >> 2;
-            for (int qd = tid; qd < own * c4; qd += SEL_THREADS) {
+            for (int qd = warp < 8 ? tid : own * c4; qd < own * c4; qd += 256) {
                 const int lr = qd / c4;
                 const int cc = (qd - lr * c4) * 4;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         // ================= phase D: the edge tiles of this CTA's positions
         if (warp >= 8) {
             // gather: issue only; a stage is refilled once the MMA has consumed its
-            // previous unit (unit 0 was issued in phase A)
+            // previous unit (unit 0 was issued in phase C)
             for (int j = 1; j < nunits; ++j) issue_unit(j);
             cp_async_wait_all();
             if (!drained_ok) wait(drained, (uint32_t)rbi & 1u);  // before region P is reused
@@ -749,10 +751,11 @@ int g_plan_count = 0;
 int g_plan_next = 0;
 
 // Shared-memory layout for a cluster size and row-block height; false when it
-// does not fit.  Region E = edge stage 0.  Region P = the projection's TMA ring,
-// then the receive slots [CS-1][own_max] and the outgoing partial [MR] (rows of
-// R + 4 floats), then edge stages 1..estages-1.  Then the u slice, the unary
-// slice, the id ring and the barriers.
+// does not fit.  Region E = edge stage 0.  Region P = the receive slots
+// [CS-1][own_max] and the outgoing partial [MR] (rows of R + 4 floats), and edge
+// stages 1..estages-1.  The projection's TMA ring spans regions E and P (it is
+// drained before either is used).  Then the u slice, the unary slice, the id
+// ring and the barriers.
 bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     q->nkb_e = R >= 128 ? 2 : 1;
     q->nhalf = R / (64 * q->nkb_e);
@@ -767,16 +770,18 @@ bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     const size_t u_bytes = (size_t)q->own_max * R * 4;
     const size_t un_bytes = (size_t)q->own_max * K * 4;
     const size_t bar_bytes = 8 * (2 * 8 + 3 + 2 * 4 + 4) + 16;
-    for (int ps = 6; ps >= 2; --ps) {
-        size_t regionP = (size_t)ps * q->pstage_bytes;
-        if (regionP < red_end) regionP = (red_end + 1023) & ~(size_t)1023;
-        const int es = 1 + (int)std::min<size_t>(3, regionP / q->estage_bytes);
+    // Region P holds the reduction buffers, then edge stages 1 .. es-1; the
+    // projection's TMA ring (phase A only) spans regions E and P from offset 0.
+    for (int es = 4; es >= 2; --es) {
+        const size_t regionP =
+            std::max((red_end + 1023) & ~(size_t)1023, (size_t)(es - 1) * q->estage_bytes);
         const size_t off_U = q->estage_bytes + regionP;
+        const int ps = (int)std::min<size_t>(6, off_U / q->pstage_bytes);
         const size_t off_un = off_U + ((u_bytes + 15) & ~(size_t)15);
         const size_t off_ids = off_un + ((un_bytes + 15) & ~(size_t)15);
         const size_t off_bar = off_ids + 2 * 2 * EROWS * 4;
         const size_t total = 1024 + off_bar + bar_bytes;
-        if (total <= max_smem && es >= 2) {
+        if (total <= max_smem && ps >= 2) {
             q->pstages = ps;
             q->estages = es;
             q->off_P = q->estage_bytes;
