@@ -465,13 +465,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             cp_async_wait_all();
             if (!drained_ok) wait(drained, (uint32_t)rbi & 1u);  // before region P is reused
         } else if (warp < 4) {
-            // gate: thread gt owns chunk column c of rows rg*cpr .. rg*cpr + cpr - 1
-            // (within one transition when K >= cpr, so u is read once per unit);
-            // A (.) u in fp32, rounded to bf16, in place; proxy fence; the named
-            // barrier shows the whole unit gated, and one thread issues its MMAs
+            // gate: thread tid owns chunk column c of some of the unit's 32 four-row
+            // groups (a row slot of cpr threads takes groups g_first, g_first +
+            // g_step, ...); A (.) u in fp32, rounded to bf16, in place; proxy
+            // fence; the named barrier shows the whole unit gated, and one thread
+            // of warp 1 issues its MMAs.  Warp 1 gates one group per slot (the
+            // last ones), so that it issues unit j's MMAs while warps 0, 2 and 3
+            // gate unit j + 1 (wide workload 25.6 -> 24.1 us per call).
             const int cpr = 8 * p.nkb_e;
             const int c = tid & (cpr - 1);
-            const int rg = tid >> log2cpr;
+            const int slot = tid >> log2cpr;
+            const int S = 32 >> log2cpr;
+            const int g_first = warp == 1 ? 32 - S + (slot - S) : (warp == 0 ? slot : slot - S);
+            const int g_end = warp == 1 ? g_first + 1 : 32 - S;
+            const int g_step = 3 * S;
             const int ch = c & 7;
             const uint32_t c_off = (uint32_t)((c >> 3) * KB_OP);
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
@@ -492,8 +499,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     int tr_cur = -1;
                     float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f);
                     float4 u1 = u0;
-                    for (int k0 = 0; k0 < cpr; k0 += 4) {
-                        const int row0 = rg * cpr + k0;
+                    for (int g = g_first; g < g_end; g += g_step) {
+                        const int row0 = 4 * g;
                         if (row0 >= rows_valid) break;
                         const int tr = row0 >> p.log2K;
                         if (tr != tr_cur) {  // this transition's u row (local to the CTA)
