@@ -52,8 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311331840 + 3218176),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "db9a25287a30dc5515d512261d00c9a9b376a288ac0c73f8f57447f3d0db6f28",
-        "bytes": 69812736 + 1130240,
+        "sha": "96fb6ce966790235323346b8486bdeae9ae9d02370fc2ce8ed003ef056b314eb",
+        "bytes": 69799936 + 1084416,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
