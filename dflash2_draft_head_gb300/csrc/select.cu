@@ -17,7 +17,9 @@
 //    thread-block cluster of CS CTAs (one CTA per SM).  The cluster splits d:
 //    CTA r streams k-blocks [r*kb/CS, (r+1)*kb/CS) of its row block of h and
 //    of W through a TMA ring (128-byte swizzle) into tcgen05.mma (M = 128,
-//    N = R) with the fp32 partial in tensor memory.
+//    N = R) with the fp32 partial in tensor memory.  Up to three warps issue
+//    the MMAs, taking the k-blocks in turn, each into its own accumulator; the
+//    accumulators are summed in issuer order when the partial is drained.
 //  - The partial tiles are reduced through distributed shared memory: CTA r
 //    owns rows [r*MR/CS, (r+1)*MR/CS) of the block; after one cluster barrier
 //    every CTA pushes each owner's rows of its partial with one bulk
@@ -88,6 +90,7 @@ struct SelParams {
     int kblocks;       // 64-column k-blocks of d
     int own_max;       // most rows a CTA owns after the reduction
     int pstages;       // projection TMA stages
+    int nmma;          // projection MMA issuers (warps 1..nmma), one accumulator each
     int estages;       // edge stages: stage 0 is region E, the others live in region P
     int nkb_e;         // 64-rank k-blocks per edge stage (1 or 2)
     int nhalf;         // edge stages per tile (R / (64 * nkb_e))
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
         }
-        mbar_init(accum, 1);
+        mbar_init(accum, (uint32_t)p.nmma);
         mbar_init(recv, 1);
         mbar_init(drained, CS > 1 ? CS - 1 : 1);
         init_edge_bars();
@@ -324,11 +327,14 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         };
 
         // ================= phase A: projection of the row block (+ early gathers)
-        if (warp == 0) {
-            if (lane == 0) {  // TMA producer
+        if (warp == 0 || warp == 8) {
+            // TMA producers: warp 0 takes the even k-blocks, warp 8 (idle until the
+            // gathers) the odd ones; each load instruction holds its issuing thread
+            // for a while, so one thread alone falls behind the ring
+            if (lane == 0) {
                 const uint32_t tx = (uint32_t)p.MR * 128u + (uint32_t)R * 128u;
-                int it = pit;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                for (int kb = kb0 + (warp == 8 ? 1 : 0); kb < kb1; kb += 2) {
+                    const int it = pit + (kb - kb0);
                     const int st = it % p.pstages;
                     wait(empty0 + 8 * st, (((uint32_t)(it / p.pstages)) & 1u) ^ 1u);
                     if (*abort_flag) continue;
@@ -340,11 +346,16 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 }
             }
             __syncwarp();
-        } else if (warp == 1) {
-            if (lane == 0) {  // MMA issuer
+        } else if (warp <= p.nmma) {
+            // MMA issuers: warp q + 1 takes k-blocks kb0 + q, kb0 + q + nmma, ... into
+            // its own accumulator (columns q*R ..); one issuing thread alone spends
+            // longer per k-block (waits, four MMAs, a commit) than the ring needs
+            if (lane == 0) {
+                const int q = warp - 1;
                 const uint32_t idesc = idesc_bf16_f32(128, R);
-                int it = pit;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const uint32_t dq = tmem + (uint32_t)(q * R);
+                for (int kb = kb0 + q; kb < kb1; kb += p.nmma) {
+                    const int it = pit + (kb - kb0);
                     const int st = it % p.pstages;
                     wait(full0 + 8 * st, ((uint32_t)(it / p.pstages)) & 1u);
                     tc_fence_after();
@@ -353,12 +364,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     if (!*abort_flag) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            tc_mma_bf16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
-                                        idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                            tc_mma_bf16(dq, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                        idesc, (kb > kb0 + q || k > 0) ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8 * st);
                 }
-                tc_commit(accum);
+                tc_commit(accum);  // every issuer arrives once, with or without k-blocks
             }
             __syncwarp();
         } else if (warp >= 8) {
@@ -375,7 +386,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
         // ================= phase B: the split-d partial, then one cluster barrier
         // Every warp moves a quarter of the columns of its tensor-memory lane
-        // quadrant (warp % 4) into the outgoing partial buffer.
+        // quadrant (warp % 4) into the outgoing partial buffer, summing the
+        // issuers' accumulators in issuer order (deterministic).
         if (tid == 0 && CS > 1)
             mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * row_bytes);
         {
@@ -385,16 +397,29 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             wait(accum, (uint32_t)rbi & 1u);
             tc_fence_after();
             const int row = q * 32 + lane;
+            const int nacc = min(p.nmma, kb1 - kb0);  // accumulators that received MMAs
             for (int c0 = c_lo; c0 < c_lo + cw; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-                tmem_ld_wait();
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
+                float f[16];
+                {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(ta, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+                }
+                for (int a = 1; a < nacc; ++a) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(ta + (uint32_t)(a * R), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) f[j] += __uint_as_float(v[j]);
+                }
                 if (row < rows) {
                     float4* dst = reinterpret_cast<float4*>(out_f + (size_t)row * p.red_stride + c0);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
                 }
             }
             fence_proxy_async_smem();  // the partial -> visible to the bulk copies
@@ -936,6 +961,10 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     p.kblocks = (a.d + 63) / 64;
     p.own_max = pl.own_max;
     p.pstages = pl.pstages;
+    // three issuers where their accumulators fit in the 512 tensor-memory columns
+    // (R = 64, 128: three; R = 256: two); the projection's accumulators are drained
+    // before the edge accumulators (columns EACC ..) are first written
+    p.nmma = std::min(3, 512 / a.R);
     p.estages = pl.estages;
     p.nkb_e = pl.nkb_e;
     p.nhalf = pl.nhalf;
