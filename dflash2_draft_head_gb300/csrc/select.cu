@@ -84,6 +84,10 @@ struct SelParams {
     int32_t* err_flag;
     int S, n, K, R, V, P;
     int log2K;
+    int log2R;
+    uint32_t nm1_magic;  // floor((2^32 - 1) / (n - 1)): e / (n - 1) without a divide
+    uint32_t ps_magic;   // the same for pstages
+    uint32_t es_magic;   // the same for estages
     int CS;            // CTAs per cluster (split of d)
     int MR;            // rows per row block
     int nrb;           // row blocks
@@ -135,6 +139,16 @@ __device__ __forceinline__ uint4 gate_chunk(uint4 a, float4 u0, float4 u1) {
 
 __device__ __forceinline__ void mbar_inval(uint32_t bar) {
     asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// floor(e / d) for 0 <= e < 2^31, d >= 1, with m = floor((2^32 - 1) / d): the
+// high half of e * m is the quotient or one less (one correction step).  The
+// hardware has no integer divide; the compiler's division sequence sat on the
+// critical path of the per-row loops below.
+__device__ __forceinline__ int div_by(int e, int d, uint32_t m) {
+    int q = (int)__umulhi((uint32_t)e, m);
+    if (e - q * d >= d) ++q;
+    return q;
 }
 
 // Number of transitions (s, i >= 1) whose target position lies before position q.
@@ -266,7 +280,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             const int e0 = e_lo + t * TP;
             if ((r >> p.log2K) >= min(TP, e_hi - e0)) return -1;
             const int e = e0 + (r >> p.log2K);
-            const int s = e / nm1;
+            const int s = div_by(e, nm1, p.nm1_magic);
             const int i = e - s * nm1 + 1 - (g < EROWS ? 1 : 0);
             return checked_id(p.cand_ids[((size_t)s * p.n + i) * K + (r & (K - 1))], p.V, bad);
         };
@@ -284,8 +298,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         //      one's rows are in flight.  The thread's arrive on landed[stage]
         //      fires once all its copies so far have completed.
         auto issue_unit = [&](int j) {
-            const int st = j % p.estages;
-            const int t = j / p.nhalf;
+            const int use = div_by(j, p.estages, p.es_magic);  // uses of the stage so far
+            const int st = j - use * p.estages;
+            const int t = j >> (p.nhalf - 1);                  // nhalf is 1 or 2
             const int half = j - t * p.nhalf;
             const int cnt = min(TP, e_hi - (e_lo + t * TP));
             int* ids = id_ring + (t & 1) * 2 * EROWS;
@@ -295,7 +310,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 id_next = load_id(t + 1);
             }
             if (j >= p.estages)  // the stage's previous unit has been consumed by the MMA
-                wait(sfree0 + 8 * st, (uint32_t)((j / p.estages) - 1) & 1u);
+                wait(sfree0 + 8 * st, (uint32_t)(use - 1) & 1u);
             if (st >= p.drain_stage && !drained_ok) {  // the outgoing partial has been sent
                 wait(drained, (uint32_t)rbi & 1u);
                 drained_ok = true;
@@ -335,8 +350,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 const uint32_t tx = (uint32_t)p.MR * 128u + (uint32_t)R * 128u;
                 for (int kb = kb0 + (warp == 8 ? 1 : 0); kb < kb1; kb += 2) {
                     const int it = pit + (kb - kb0);
-                    const int st = it % p.pstages;
-                    wait(empty0 + 8 * st, (((uint32_t)(it / p.pstages)) & 1u) ^ 1u);
+                    const int use = div_by(it, p.pstages, p.ps_magic);
+                    const int st = it - use * p.pstages;
+                    wait(empty0 + 8 * st, ((uint32_t)use & 1u) ^ 1u);
                     if (*abort_flag) continue;
                     const uint32_t fb = full0 + 8 * st;
                     const uint32_t dst = sE + (uint32_t)st * p.pstage_bytes;
@@ -356,8 +372,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 const uint32_t dq = tmem + (uint32_t)(q * R);
                 for (int kb = kb0 + q; kb < kb1; kb += p.nmma) {
                     const int it = pit + (kb - kb0);
-                    const int st = it % p.pstages;
-                    wait(full0 + 8 * st, ((uint32_t)(it / p.pstages)) & 1u);
+                    const int use = div_by(it, p.pstages, p.ps_magic);
+                    const int st = it - use * p.pstages;
+                    wait(full0 + 8 * st, (uint32_t)use & 1u);
                     tc_fence_after();
                     const uint32_t a0 = sE + (uint32_t)st * p.pstage_bytes;
                     const uint32_t b0 = a0 + HTILE;
@@ -458,26 +475,33 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         // HBM (an L2 prefetch of their rows measured no faster).
         if (warp >= 8 && nunits > 0) issue_unit(0);
         {
+            // (row, 4-column group) items; R is a power of two, so no divides
             const int own = o_hi - o_lo;
-            const int c4 = R >> 2;
-            for (int qd = warp < 8 ? tid : own * c4; qd < own * c4; qd += 256) {
-                const int lr = qd / c4;
-                const int cc = (qd - lr * c4) * 4;
+            const int l2c4 = p.log2R - 2;
+            const int nq = own << l2c4;
+            const uint32_t out_a = smem_u32(out_f) + (uint32_t)o_lo * row_bytes;
+            const uint32_t recv_a = smem_u32(recv_f);
+            const uint32_t us_a = smem_u32(uslice);
+            for (int qd = warp < 8 ? tid : nq; qd < nq; qd += 256) {
+                const int lr = qd >> l2c4;
+                const uint32_t cb = (uint32_t)(qd & ((1 << l2c4) - 1)) * 16u;  // byte column
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
                 for (int src = 0; src < CS; ++src) {  // rank order: deterministic
-                    const float* srow =
-                        src == rank ? out_f + (size_t)(o_lo + lr) * p.red_stride
-                                    : recv_f + ((size_t)(src < rank ? src : src - 1) * p.own_max + lr) *
-                                                   p.red_stride;
-                    const float4 v = *reinterpret_cast<const float4*>(srow + cc);
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
+                    const uint32_t a =
+                        src == rank ? out_a + (uint32_t)lr * row_bytes + cb
+                                    : recv_a + (uint32_t)((src < rank ? src : src - 1) * p.own_max + lr) *
+                                                   row_bytes + cb;
+                    const uint4 v = lds_v4(a);
+                    acc.x += __uint_as_float(v.x);
+                    acc.y += __uint_as_float(v.y);
+                    acc.z += __uint_as_float(v.z);
+                    acc.w += __uint_as_float(v.w);
                 }
-                *reinterpret_cast<float4*>(uslice + (size_t)lr * R + cc) = acc;
-                *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + cc) = acc;
+                st_shared_v4(us_a + ((uint32_t)(lr * R) << 2) + cb,
+                             make_uint4(__float_as_uint(acc.x), __float_as_uint(acc.y),
+                                        __float_as_uint(acc.z), __float_as_uint(acc.w)));
+                *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + (cb >> 2)) = acc;
             }
         }
         __syncthreads();  // u slice complete; the receive slots are free
@@ -508,12 +532,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             const uint32_t c_off = (uint32_t)((c >> 3) * KB_OP);
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             for (int j = 0; j < nunits; ++j) {
-                const int st = j % p.estages;
-                const int t = j / p.nhalf;
+                const int use = div_by(j, p.estages, p.es_magic);
+                const int st = j - use * p.estages;
+                const int t = j >> (p.nhalf - 1);
                 const int half = j - t * p.nhalf;
                 const int e0 = e_lo + t * TP;
                 const int rows_valid = min(TP, e_hi - e0) << p.log2K;
-                wait(landed0 + 8 * st, ((uint32_t)(j / p.estages)) & 1u);
+                wait(landed0 + 8 * st, (uint32_t)use & 1u);
                 const uint32_t sb = estage_base(st) + c_off;
                 const int col = half * 64 * p.nkb_e + c * 8;
                 if (!*abort_flag) {
@@ -530,12 +555,15 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                         const int tr = row0 >> p.log2K;
                         if (tr != tr_cur) {  // this transition's u row (local to the CTA)
                             tr_cur = tr;
+                            // transition e = s*(n-1) + i-1 scores position s*n + i = e + s + 1
                             const int e = e0 + tr;
-                            const int s = e / nm1;
-                            const int lr = s * p.n + (e - s * nm1) + 1 - pa;
-                            const float4* ur = reinterpret_cast<const float4*>(uslice + (size_t)lr * R + col);
-                            u0 = ur[0];
-                            u1 = ur[1];
+                            const int lr = e + div_by(e, nm1, p.nm1_magic) + 1 - pa;
+                            const uint32_t ua = smem_u32(uslice) + ((uint32_t)(lr * R + col) << 2);
+                            const uint4 w0 = lds_v4(ua), w1 = lds_v4(ua + 16);
+                            u0 = make_float4(__uint_as_float(w0.x), __uint_as_float(w0.y),
+                                             __uint_as_float(w0.z), __uint_as_float(w0.w));
+                            u1 = make_float4(__uint_as_float(w1.x), __uint_as_float(w1.y),
+                                             __uint_as_float(w1.z), __uint_as_float(w1.w));
                         }
                         uint32_t off[4];
                         uint4 a[4];
@@ -595,7 +623,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 const int e = e0 + (r >> p.log2K);
                 int s = 0, i = 1;
                 if (valid) {
-                    s = e / nm1;
+                    s = div_by(e, nm1, p.nm1_magic);
                     i = e - s * nm1 + 1;
                 }
                 // unary row of this transition's position (staged in phase A)
@@ -955,6 +983,12 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     int l2 = 0;
     while ((1 << l2) < a.K) ++l2;
     p.log2K = l2;
+    int lr2 = 0;
+    while ((1 << lr2) < a.R) ++lr2;
+    p.log2R = lr2;
+    p.nm1_magic = 0xFFFFFFFFu / (uint32_t)(a.n - 1);  // n >= 2 on this path
+    p.ps_magic = 0xFFFFFFFFu / (uint32_t)pl.pstages;
+    p.es_magic = 0xFFFFFFFFu / (uint32_t)pl.estages;
     p.CS = pl.CS;
     p.MR = pl.MR;
     p.nrb = pl.nrb;
