@@ -10,9 +10,13 @@
 //    every CTA streams its K range through a 6-stage TMA pipeline of
 //    128x64 bf16 tiles of h and W, stored in the 128-byte-swizzle K-major
 //    layout that the tensor core reads directly;
-//  - one thread issues tcgen05.mma (M=128, N=128, K=16) and frees a stage with
-//    tcgen05.commit; one thread drives TMA;
-//  - epilogue: tcgen05.ld of the partial tile into the CTA's shared memory,
+//  - two producer threads (warps 0 and 2) drive TMA for the even and the odd
+//    k-blocks, and two issuing threads (warps 1 and 3) issue tcgen05.mma
+//    (M=128, N=128, K=16) for them into two accumulators, freeing each stage
+//    with tcgen05.commit; a single thread issuing loads or MMAs for every
+//    k-block is slower per k-block than the TMA ring;
+//  - epilogue: tcgen05.ld of both accumulators (summed, even + odd) and of the
+//    partial tile into the CTA's shared memory,
 //    a cluster barrier, then CTA r sums rows [r*128/split, (r+1)*128/split)
 //    over all CTAs of the cluster through distributed shared memory in a
 //    fixed order (deterministic) and writes fp32 u.  No global workspace.
@@ -118,12 +122,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(accum, 1);
+        mbar_init(accum, 2);  // one commit from each MMA issuer
         mbar_init(recv, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), BN);
+        tmem_alloc(smem_u32(tmem_slot), 2 * BN);  // even and odd k-block accumulators
         tmem_relinquish();
     }
     tc_fence_before();
@@ -136,9 +140,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     griddep_wait();
     griddep_launch_dependents();
 
-    if (warp == 0 && lane == 0) {
-        // TMA producer
-        for (int it = 0; it < nkb; ++it) {
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        // TMA producers: warp 0 loads the even k-blocks, warp 2 the odd ones
+        for (int it = warp >> 1; it < nkb; it += 2) {
             const int s = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
             if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitNs)) {
@@ -152,10 +156,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tma_load_2d(dst, &tmA, fb, kx, m_tile * BM);
             tma_load_2d(dst + A_BYTES, &tmB, fb, kx, n_tile * BN);
         }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+        // MMA issuers: warp 1 the even k-blocks into columns [0, BN), warp 3 the
+        // odd ones into [BN, 2 BN)
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-        for (int it = 0; it < nkb; ++it) {
+        const int q = warp >> 1;
+        const uint32_t dq = tmem + (uint32_t)(q * BN);
+        for (int it = q; it < nkb; it += 2) {
             const int s = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
             if (!mbar_wait_bounded(full0 + 8 * s, ph, kWaitNs)) {
@@ -167,11 +174,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-                tc_mma_bf16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc,
-                            (it > 0 || k > 0) ? 1u : 0u);
+                tc_mma_bf16(dq, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc,
+                            (it > q || k > 0) ? 1u : 0u);
             tc_commit(empty0 + 8 * s);
         }
-        tc_commit(accum);
+        tc_commit(accum);  // arrives even when this issuer had no k-block
     }
     __syncwarp();
 
@@ -180,30 +187,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!mbar_wait_bounded(accum, 0, kWaitNs)) ok = false;
     tc_fence_after();
     const int row = warp * 32 + lane;
+    // 32 columns of this thread's row: the even accumulator plus the odd one (in
+    // that order; the odd one is empty when there is a single k-block)
+    auto load_acc = [&](int c0, float (&f)[32]) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (nkb > 1) {
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(BN + c0), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(v[j]);
+        }
+    };
     if constexpr (SPLIT == 1) {
         // no split: each thread writes its own row straight from TMEM
         const int grow = m_tile * BM + row;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            tmem_ld_wait();
+            float f[32];
+            load_acc(c0, f);
             const int gcol = n_tile * BN + c0;
             if (grow < p.P) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     if (gcol + 4 * j < p.R)
                         store_out4(p, (size_t)grow * p.R + gcol + 4 * j,
-                                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                               __uint_as_float(v[4 * j + 2]),
-                                               __uint_as_float(v[4 * j + 3])));
+                                   make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]));
             }
         }
         tc_fence_before();
         __syncthreads();
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(tmem, BN);
+            tmem_dealloc(tmem, 2 * BN);
         }
     } else if (p.ws != nullptr) {
         // Split-K reduction through an L2-resident workspace.  CTA r of the
@@ -216,14 +235,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float* red = reinterpret_cast<float*>(stages);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            tmem_ld_wait();
+            float f[32];
+            load_acc(c0, f);
             float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
         }
         __syncthreads();
         const size_t tile = (size_t)m_tile * gridDim.z + n_tile;
@@ -261,7 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(tmem, BN);
+            tmem_dealloc(tmem, 2 * BN);
         }
     } else {
         // Split-K reduction through distributed shared memory.  CTA r of the
@@ -278,14 +295,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (threadIdx.x == 0) mbar_arrive_expect_tx(recv, (SPLIT - 1) * SLICE);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
-            tmem_ld_wait();
+            float f[32];
+            load_acc(c0, f);
             float4* dst = reinterpret_cast<float4*>(red + (size_t)row * RED_STRIDE + c0);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
         }
         fence_proxy_async_smem();  // partial tile -> visible to the copy engine
         tc_fence_before();
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         cluster_sync();  // the slices this CTA sent have all been received
         if (warp == 1) {
             tc_fence_after();
-            tmem_dealloc(tmem, BN);
+            tmem_dealloc(tmem, 2 * BN);
         }
     }
     if (!ok) atomicOr(&g_fault_word, (unsigned)DF2_FLAG_TIMEOUT);
