@@ -272,30 +272,29 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         const int nunits = ntile * p.nhalf;
         bool drained_ok = CS == 1;  // this row block's outgoing partial no longer read
 
-        // ---- ids of tile t for gather slot g: g < 128 the predecessor id of row
-        //      g (from position i-1), else the candidate id of row g-128
-        auto id_of = [&](int t, int g) -> int {
-            if (t >= ntile) return -1;
-            const int r = g & (EROWS - 1);
+        // ---- raw id of tile t for this gather thread's slot g = gtid: g < 128 the
+        //      predecessor id of row g (from position i-1), else the candidate id
+        //      of row g-128; 0 for rows past the tile.  It is range-checked only
+        //      where it is stored (checked_id), one tile later, so the load's
+        //      latency never holds up a unit's copies.
+        auto raw_id = [&](int t) -> int {
+            if (t >= ntile) return 0;
+            const int r = gtid & (EROWS - 1);
             const int e0 = e_lo + t * TP;
-            if ((r >> p.log2K) >= min(TP, e_hi - e0)) return -1;
+            if ((r >> p.log2K) >= min(TP, e_hi - e0)) return 0;
             const int e = e0 + (r >> p.log2K);
             const int s = div_by(e, nm1, p.nm1_magic);
-            const int i = e - s * nm1 + 1 - (g < EROWS ? 1 : 0);
-            return checked_id(p.cand_ids[((size_t)s * p.n + i) * K + (r & (K - 1))], p.V, bad);
+            const int i = e - s * nm1 + 1 - (gtid < EROWS ? 1 : 0);
+            return p.cand_ids[((size_t)s * p.n + i) * K + (r & (K - 1))];
         };
-        auto load_id = [&](int t) -> int {
-            const int id = id_of(t, gtid);
-            return id < 0 ? 0 : id;
-        };
-        int id_next = warp >= 8 ? load_id(0) : 0;
+        int id_next = warp >= 8 ? raw_id(0) : 0;
 
         // ---- gather issue of edge unit j (tile j / nhalf, rank half j % nhalf).
         //      A new tile's ids go to slot t & 1 of the id ring; the named barrier
         //      makes them visible to all gather threads (and shows that the slot
         //      being overwritten, last read while issuing tile t - 2, has been
-        //      read by all of them); then the next tile's id is loaded while this
-        //      one's rows are in flight.  The thread's arrive on landed[stage]
+        //      read by all of them); the next tile's id is loaded after this
+        //      unit's copies are issued.  The thread's arrive on landed[stage]
         //      fires once all its copies so far have completed.
         auto issue_unit = [&](int j) {
             const int use = div_by(j, p.estages, p.es_magic);  // uses of the stage so far
@@ -305,9 +304,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             const int cnt = min(TP, e_hi - (e_lo + t * TP));
             int* ids = id_ring + (t & 1) * 2 * EROWS;
             if (half == 0) {
-                ids[gtid] = id_next;
+                ids[gtid] = checked_id(id_next, p.V, bad);
                 named_bar_sync(1, SEL_GTHREADS);
-                id_next = load_id(t + 1);
             }
             if (j >= p.estages)  // the stage's previous unit has been consumed by the MMA
                 wait(sfree0 + 8 * st, (uint32_t)(use - 1) & 1u);
@@ -339,6 +337,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 }
             }
             cp_async_mbar_arrive_noinc(landed0 + 8 * st);
+            if (half == p.nhalf - 1) id_next = raw_id(t + 1);
         };
 
         // ================= phase A: projection of the row block (+ early gathers)
