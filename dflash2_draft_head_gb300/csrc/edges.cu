@@ -42,11 +42,21 @@ struct EParams {
     const float* unary;
     int S, n, K, R, V;
     int E;  // transitions = S * (n - 1)
+    uint32_t nm1_magic;  // floor((2^32 - 1) / (n - 1)) (1 when n = 1: no transitions)
     float* edges_out;
     int32_t* best_slot;
     float* best_score;
     int32_t* err_flag;
 };
+
+// floor(e / d) for 0 <= e < 2^31, d >= 1, with m = floor((2^32 - 1) / d): the
+// high half of e * m is the quotient or one less (one correction step), so the
+// per-row index math needs no integer divide (which the hardware lacks).
+__device__ __forceinline__ int div_by(int e, int d, uint32_t m) {
+    int q = (int)__umulhi((uint32_t)e, m);
+    if (e - q * d >= d) ++q;
+    return q;
+}
 
 __device__ __forceinline__ int checked_id(int id, int V, bool& bad) {
     if (id < 0 || id >= V) {
@@ -397,13 +407,15 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
 
     if (warp >= 9) {
         // ------------------------------------------------ gather (EP_GWARPS warps)
-        // ids and u-row indices are double-buffered by tile parity and the next
-        // tile's ids are prefetched into registers while this tile is issued.
+        // ids and u-row indices are double-buffered by tile parity; the next
+        // tile's raw ids are loaded into registers after this tile's copies are
+        // issued and range-checked only where they are stored, one tile later,
+        // so no copy waits on an id round trip.
         const int gtid = tid - 9 * 32;
         const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(p.A);
         const __nv_bfloat16* B = static_cast<const __nv_bfloat16*>(p.B);
         bool bad = false;
-        auto load_id = [&](int idx, int& id, int& ur) {  // thread gtid < 256: one id
+        auto load_id = [&](int idx, int& id, int& ur) {  // thread gtid < 256: one raw id
             id = 0;
             ur = 0;
             if (idx >= tl_list.n_items || gtid >= 2 * TROWS) return;
@@ -413,10 +425,10 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
             const int tt = r >> log2K;
             if (tt < cnt) {
                 const int e = e0 + tt;
-                const int s = e / nm1;
-                const int i = e % nm1 + 1;
+                const int s = div_by(e, nm1, p.nm1_magic);
+                const int i = e - s * nm1 + 1;
                 const int pos = s * p.n + i - (gtid < TROWS ? 1 : 0);
-                id = checked_id(p.cand_ids[(size_t)pos * K + (r & (K - 1))], p.V, bad);
+                id = p.cand_ids[(size_t)pos * K + (r & (K - 1))];
                 ur = s * p.n + i;
             }
         };
@@ -434,13 +446,12 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
             // finished that before the barrier of tile tl-1 below, which this
             // warp has passed, so the slot is free without another barrier
             if (gtid < TROWS) {
-                idp[gtid] = id_next;
+                idp[gtid] = checked_id(id_next, p.V, bad);
                 if ((gtid & (K - 1)) == 0) urw[gtid >> log2K] = ur_next;
             } else if (gtid < 2 * TROWS) {
-                idc[gtid - TROWS] = id_next;
+                idc[gtid - TROWS] = checked_id(id_next, p.V, bad);
             }
             named_bar_sync(1, EP_GTHREADS);
-            load_id(idx + gridDim.x, id_next, ur_next);  // prefetch the next tile's id
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int st = it % EP_STAGES;
                 wait(empty0 + 8 * st, (((uint32_t)(it / EP_STAGES)) & 1u) ^ 1u);
@@ -470,6 +481,7 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
                 }
                 cp_async_mbar_arrive_noinc(full0 + 8 * st);
             }
+            load_id(idx + gridDim.x, id_next, ur_next);  // the next tile's raw ids
         }
         if (bad && p.err_flag != nullptr) atomicOr(p.err_flag, DF2_FLAG_BAD_ID);
     } else if (warp >= 4 && warp < 8) {
@@ -556,8 +568,8 @@ __global__ void __launch_bounds__(EP_THREADS, 1)
             const int e = e0 + (r >> log2K);
             int s = 0, i = 1;
             if (valid) {
-                s = e / nm1;
-                i = e % nm1 + 1;
+                s = div_by(e, nm1, p.nm1_magic);
+                i = e - s * nm1 + 1;
             }
             const float* un = p.unary + ((size_t)s * p.n + i) * K;
             float* erow =
@@ -699,6 +711,7 @@ EParams make_params(const EdgesArgs& a) {
     p.R = a.R;
     p.V = a.V;
     p.E = a.S * (a.n - 1);
+    p.nm1_magic = a.n > 1 ? 0xFFFFFFFFu / (uint32_t)(a.n - 1) : 1u;
     p.edges_out = a.edges_out;
     p.best_slot = a.best_slot;
     p.best_score = a.best_score;
