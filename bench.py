@@ -52,8 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311331840 + 3218176),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "96fb6ce966790235323346b8486bdeae9ae9d02370fc2ce8ed003ef056b314eb",
-        "bytes": 69799936 + 1084416,
+        "sha": "b021f08e109a6c10d045beb1c068741e8a8721fdf5f96e818ba142ebff585f54",
+        "bytes": 69800192 + 1122560,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
@@ -443,6 +443,34 @@ def _timed_eager(K, stream, flush, calls, L, ends_only=False):
     return t[0] if ends_only else t
 
 
+def _back_to_back_us(stream, flush, calls, L, reps=20, iters=10):
+    """Per-call device time of `calls` when launched back to back from a CUDA graph:
+    a graph of `reps` (L2 flush + calls) minus a graph of `reps` flushes, each timed
+    with two CUDA events around `iters` replays (median); no timing event sits
+    between the calls, so the launch gaps the per-call events add are left out."""
+    import torch
+
+    def graph_us(cl):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                flush.zero_()
+                for f, a in cl:
+                    _call(f, a, L)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        g.replay()
+        ts = []
+        for _ in range(iters):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return 1000.0 * statistics.median(ts) / reps
+    return graph_us(calls) - graph_us([])
+
+
 def _timer(stream, record_ext, L):
     """timer(K, flush, calls, ends_only=False): the graph timer when timing events
     can be recorded inside a capture, else eager launches."""
@@ -690,6 +718,9 @@ def main():
     # the same step with an event between the two calls: each call's share
     t_conv, t_sel = timer(K_iso, flush, calls)
     sel_plan = _select_fused(L, w0)
+    # each call's device time launched back to back (no event between the calls)
+    b2b_conv = _back_to_back_us(stream, flush, [(f_conv, conv_args)], L)
+    b2b_sel = _back_to_back_us(stream, flush, [(f_sel, sel_args)], L)
     # the projection and the edge kernel on their own (the path dflash2_select
     # takes for shapes the one-kernel selector does not run)
     iso_calls = [(f_proj, proj_args), (f_edge, edge_args)]
@@ -897,10 +928,11 @@ def main():
     if sel_us >= conv_us:
         dom = {"kernel": "dflash2_select" + ("" if sel_plan["fused"] else " (project + edges)"),
                "bytes": proj_b + edge_b, "us": sel_us,
-               "traffic": _traffic("select", "select.cu") if sel_plan["fused"] else None}
+               "traffic": _traffic("select", "select.cu") if sel_plan["fused"] else None,
+               "b2b": b2b_sel}
     else:
         dom = {"kernel": "dflash2_dynconv", "bytes": conv_b, "us": conv_us,
-               "traffic": _traffic("dynconv", "dynconv.cu")}
+               "traffic": _traffic("dynconv", "dynconv.cu"), "b2b": b2b_conv}
     achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
     traffic = _traffic("dynconv", "dynconv.cu")
     tk_sha = hashlib.sha256(open(os.path.join(ROOT, "dflash2_draft_head_gb300", "csrc",
@@ -920,7 +952,9 @@ def main():
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": dom["traffic"], "bytes_per_launch": dom["bytes"],
                      "us_per_launch": dom["us"], "peak_source": src,
-                     "timing": "live, an event between the step's two calls"},
+                     "timing": "live, an event between the step's two calls",
+                     "back_to_back_us": dom["b2b"],
+                     "frac_back_to_back": dom["bytes"] / dom["b2b"] / 1e3 / hbm},
         "roofline_step": {"bound": "hbm", "bytes_per_step": conv_b + proj_b + edge_b,
                           "us_per_step": 1000.0 * total_ms / K,
                           "achieved": (conv_b + proj_b + edge_b) / (1000.0 * total_ms / K) / 1e3,
@@ -953,10 +987,14 @@ def main():
         "kernels": {
             "dynconv": {"us": conv_us, "bytes": conv_b, "GB/s": conv_b / conv_us / 1e3,
                         "frac_hbm": conv_b / conv_us / 1e3 / hbm,
+                        "back_to_back_us": b2b_conv,
+                        "frac_hbm_back_to_back": conv_b / b2b_conv / 1e3 / hbm,
                         "positions_per_s": positions / (conv_us * 1e-6)},
             "select": {"us": sel_us, "bytes": proj_b + edge_b,
                        "GB/s": (proj_b + edge_b) / sel_us / 1e3,
                        "frac_hbm": (proj_b + edge_b) / sel_us / 1e3 / hbm,
+                       "back_to_back_us": b2b_sel,
+                       "frac_hbm_back_to_back": (proj_b + edge_b) / b2b_sel / 1e3 / hbm,
                        "plan": sel_plan,
                        "note": "dflash2_select in the step (one kernel when plan.fused)"},
             "project": {"isolated": True, "steps": K_iso, "us": proj_us, "bytes": proj_b,
