@@ -17,7 +17,10 @@
 //   1. delta, split-K over the cluster: every CTA streams its channel slice of
 //      the tile's x rows and of Wc through a TMA ring (128-byte swizzle,
 //      K-major) into tcgen05.mma (M = 128 positions, N = T*G rounded up to 16,
-//      fp32 accumulation in tensor memory);
+//      fp32 accumulation in tensor memory); two producer threads issue the
+//      loads of the even and the odd k-blocks and two threads their MMAs, into
+//      two accumulators summed when drained (one thread issuing every load or
+//      every MMA is slower per k-block than the ring);
 //   2. the partial tiles go to shared memory, column-major (tcgen05.ld by all
 //      warps); after a cluster barrier each CTA sums, in rank order
 //      (deterministic), the columns its own channel slice needs -- taps t*G+g
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(NT, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(accum, 1);
+        mbar_init(accum, 2);  // one commit from each MMA issuer
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -203,10 +206,20 @@ __global__ void __launch_bounds__(NT, 1)
     griddep_launch_dependents();
 
     // ---------------------------------------------------------------- 1. delta on the tensor cores
-    if (warp == 0 && lane == 0) {
-        for (int it = 0; it < nkb; ++it) {
-            const int s = it % p.stages;
-            const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+    // producers: warp 0 the even k-blocks, warp 2 the odd ones; issuers: warp 1 the
+    // even ones into columns [0, NP), warp 3 the odd ones into [NP, 2 NP).  The
+    // ring stage and its phase advance by two k-blocks per step.
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        int s = warp >> 1;  // stages >= 2
+        uint32_t ph = 0;
+        for (int it = warp >> 1; it < nkb; it += 2) {
+            if (it >= 2) {
+                s += 2;
+                while (s >= p.stages) {
+                    s -= p.stages;
+                    ph ^= 1u;
+                }
+            }
             if (!mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, kWaitNs)) {
                 ok = false;
                 break;
@@ -218,11 +231,20 @@ __global__ void __launch_bounds__(NT, 1)
             tma_load_2d(dst, &tmX, fb, kx, m_tile * kBM);
             tma_load_2d(dst + kABytes, &tmW, fb, kx, 0);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
         const uint32_t idesc = idesc_bf16_f32(kBM, p.NP);
-        for (int it = 0; it < nkb; ++it) {
-            const int s = it % p.stages;
-            const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+        const int q = warp >> 1;
+        const uint32_t dq = tmem + (uint32_t)(q * p.NP);
+        int s = q;
+        uint32_t ph = 0;
+        for (int it = q; it < nkb; it += 2) {
+            if (it >= 2) {
+                s += 2;
+                while (s >= p.stages) {
+                    s -= p.stages;
+                    ph ^= 1u;
+                }
+            }
             if (!mbar_wait_bounded(full0 + 8 * s, ph, kWaitNs)) {
                 ok = false;
                 break;
@@ -232,11 +254,11 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t b0 = a0 + kABytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-                tc_mma_bf16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc,
-                            (it > 0 || k > 0) ? 1u : 0u);
+                tc_mma_bf16(dq, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc,
+                            (it > q || k > 0) ? 1u : 0u);
             tc_commit(empty0 + 8 * s);
         }
-        tc_commit(accum);
+        tc_commit(accum);  // arrives even when this issuer had no k-block
     }
     __syncwarp();
 
@@ -253,12 +275,22 @@ __global__ void __launch_bounds__(NT, 1)
         const int row = (warp & 3) * 32 + lane;
 #pragma unroll 1
         for (int c0 = (warp >> 2) * 32; c0 < p.TG; c0 += (NT / 128) * 32) {
+            const uint32_t ta = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c0;
             uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c0, v);
+            float f[32];
+            tmem_ld_32x32b_x32(ta, v);
             tmem_ld_wait();
 #pragma unroll
+            for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+            if (nkb > 1) {  // plus the odd k-blocks' accumulator
+                tmem_ld_32x32b_x32(ta + (uint32_t)p.NP, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] += __uint_as_float(v[j]);
+            }
+#pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (c0 + j < p.TG) red[(size_t)(c0 + j) * kBM + row] = __uint_as_float(v[j]);
+                if (c0 + j < p.TG) red[(size_t)(c0 + j) * kBM + row] = f[j];
         }
     }
     tc_fence_before();
@@ -642,7 +674,7 @@ bool plan_dynconv_pred(const DynconvPredArgs& a, int num_sms, size_t max_smem, D
             r.ring_bytes = (uint32_t)ring;
             r.ds_bytes = (uint32_t)ds_bytes;
             r.smem_bytes = total;
-            r.tmem_cols = pow2_at_least((unsigned)r.NP);
+            r.tmem_cols = pow2_at_least(2u * (unsigned)r.NP);  // two accumulators
             *plan = r;
             return true;
         }
