@@ -130,6 +130,15 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint3
         : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory (addresses from
+// mapa), completing 16 bytes of transaction count on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -98,10 +98,11 @@ struct SelParams {
     int estages;       // edge stages: stage 0 is region E, the others live in region P
     int nkb_e;         // 64-rank k-blocks per edge stage (1 or 2)
     int nhalf;         // edge stages per tile (R / (64 * nkb_e))
-    int drain_stage;   // first edge stage that overlaps the outgoing partial buffer
+    int n_early;       // edge units gathered while the partials are exchanged
+    int sorder;        // physical edge stage of ring slot i: bits [4i, 4i+4)
     uint32_t pstage_bytes;  // HTILE + R * 128
     uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
-    uint32_t off_P, off_out, off_U, off_un, off_ids, off_bar;  // off_out: relative to region P
+    uint32_t off_P, off_U, off_un, off_ids, off_bar;
     uint32_t red_stride;    // floats per row of the partial buffers (R + 4)
 };
 
@@ -166,8 +167,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sE = smem_u32(smem);
     const uint32_t sP = sE + p.off_P;
-    const float* recv_f = reinterpret_cast<const float*>(smem + p.off_P);        // [CS-1][own_max][R+4]
-    float* out_f = reinterpret_cast<float*>(smem + p.off_P + p.off_out);        // [MR][R+4]
+    // receive area (region P from offset 0): [CS][own_max][R+4] fp32, slot src holds
+    // CTA src's partial of this CTA's rows (its own partial at slot rank)
     float* uslice = reinterpret_cast<float*>(smem + p.off_U);                   // [own][R]
     float* unslice = reinterpret_cast<float*>(smem + p.off_un);                 // [own][K]
     int* id_ring = reinterpret_cast<int*>(smem + p.off_ids);                    // [2][256]
@@ -176,12 +177,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const uint32_t empty0 = full0 + 8 * p.pstages;
     const uint32_t accum = empty0 + 8 * p.pstages;
     const uint32_t recv = accum + 8;
-    const uint32_t drained = recv + 8;
-    const uint32_t landed0 = drained + 8;  // [estages]: a unit's copies have landed
+    const uint32_t landed0 = recv + 8;  // [estages]: a unit's copies have landed
     const uint32_t sfree0 = landed0 + 8 * p.estages;
     const uint32_t tfull0 = sfree0 + 8 * p.estages;
     const uint32_t tempty0 = tfull0 + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.pstages + 3 + 2 * p.estages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.pstages + 2 + 2 * p.estages + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x;
@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         }
         mbar_init(accum, (uint32_t)p.nmma);
         mbar_init(recv, 1);
-        mbar_init(drained, CS > 1 ? CS - 1 : 1);
         init_edge_bars();
         *abort_flag = 0;
         fence_mbar_init();
@@ -242,6 +241,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     auto estage_base = [&](int st) -> uint32_t {
         return st == 0 ? sE : sP + (uint32_t)(st - 1) * p.estage_bytes;
     };
+    // ring slot i of the edge units -> physical stage (the stages clear of the
+    // receive area come first, so they can be filled during the exchange)
+    auto phys = [&](int i) -> int { return (p.sorder >> (4 * i)) & 15; };
 
     // A gather thread's place in an edge stage never changes: chunk ch (16 bytes)
     // of k-block kb of rows r0, r0 + row_step, ...; so the 128-byte swizzle of
@@ -270,7 +272,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         const int e_hi = trans_before(pb, p.n);
         const int ntile = (e_hi - e_lo + TP - 1) / TP;
         const int nunits = ntile * p.nhalf;
-        bool drained_ok = CS == 1;  // this row block's outgoing partial no longer read
 
         // ---- raw id of tile t for this gather thread's slot g = gtid: g < 128 the
         //      predecessor id of row g (from position i-1), else the candidate id
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         //      fires once all its copies so far have completed.
         auto issue_unit = [&](int j) {
             const int use = div_by(j, p.estages, p.es_magic);  // uses of the stage so far
-            const int st = j - use * p.estages;
+            const int st = phys(j - use * p.estages);
             const int t = j >> (p.nhalf - 1);                  // nhalf is 1 or 2
             const int half = j - t * p.nhalf;
             const int cnt = min(TP, e_hi - (e_lo + t * TP));
@@ -309,10 +310,6 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             }
             if (j >= p.estages)  // the stage's previous unit has been consumed by the MMA
                 wait(sfree0 + 8 * st, (uint32_t)(use - 1) & 1u);
-            if (st >= p.drain_stage && !drained_ok) {  // the outgoing partial has been sent
-                wait(drained, (uint32_t)rbi & 1u);
-                drained_ok = true;
-            }
             const int rows_valid = cnt << p.log2K;
             const uint32_t sb = estage_base(st) + g_off;
             const uint32_t sbB = sb + (uint32_t)(p.nkb_e * KB_OP);
@@ -400,20 +397,39 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 reinterpret_cast<float4*>(unslice)[qd] = __ldg(src + qd);
         }
 
-        // ================= phase B: the split-d partial, then one cluster barrier
-        // Every warp moves a quarter of the columns of its tensor-memory lane
-        // quadrant (warp % 4) into the outgoing partial buffer, summing the
-        // issuers' accumulators in issuer order (deterministic).
+        // ================= phase B: one cluster barrier, then the split-d partials
+        // The barrier shows every CTA of the cluster done with its projection
+        // (its ring drained, so its receive area is free).  Warps 0-7 then move
+        // the accumulators (summed in issuer order: deterministic) straight from
+        // tensor memory to the owners of the rows: warp w takes lane quadrant
+        // w % 4 and half of the columns; a row another CTA owns goes into that
+        // CTA's receive slot with asynchronous remote stores (st.async) that
+        // complete on its receive barrier, an own row into the own slot.  No
+        // outgoing copy of the partial is kept, so the receive area is the only
+        // exchange memory and the edge stages clear of it take the first units'
+        // gathers meanwhile (warps 8-15).
         if (tid == 0 && CS > 1)
-            mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * row_bytes);
-        {
+            mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * (uint32_t)R * 4u);
+        wait(accum, (uint32_t)rbi & 1u);
+        tc_fence_before();
+        if (CS > 1)
+            cluster_sync();
+        else
+            __syncthreads();
+        tc_fence_after();
+        if (warp < 8) {
             const int q = warp & 3;
-            const int cw = R >> 2;
+            const int cw = R >> 1;
             const int c_lo = (warp >> 2) * cw;
-            wait(accum, (uint32_t)rbi & 1u);
-            tc_fence_after();
             const int row = q * 32 + lane;
             const int nacc = min(p.nmma, kb1 - kb0);  // accumulators that received MMAs
+            // owner X of the row: X*rows/CS <= row < (X+1)*rows/CS
+            int X = 0;
+            while (X + 1 < CS && (X + 1) * rows < (row + 1) * CS) ++X;
+            const int lr = row - X * rows / CS;
+            const uint32_t dst = sP + ((uint32_t)(rank * p.own_max + lr)) * row_bytes;
+            const uint32_t rdst = X == rank ? dst : map_cluster(dst, (uint32_t)X);
+            const uint32_t rbar = map_cluster(recv, (uint32_t)X);
             for (int c0 = c_lo; c0 < c_lo + cw; c0 += 16) {
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
                 float f[16];
@@ -422,96 +438,67 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     tmem_ld_32x32b_x16(ta, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+                    for (int jj = 0; jj < 16; ++jj) f[jj] = __uint_as_float(v[jj]);
                 }
                 for (int a = 1; a < nacc; ++a) {
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(ta + (uint32_t)(a * R), v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] += __uint_as_float(v[j]);
+                    for (int jj = 0; jj < 16; ++jj) f[jj] += __uint_as_float(v[jj]);
                 }
                 if (row < rows) {
-                    float4* dst = reinterpret_cast<float4*>(out_f + (size_t)row * p.red_stride + c0);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const uint4 w4 = make_uint4(__float_as_uint(f[4 * jj]), __float_as_uint(f[4 * jj + 1]),
+                                                    __float_as_uint(f[4 * jj + 2]), __float_as_uint(f[4 * jj + 3]));
+                        const uint32_t off = (uint32_t)(c0 + 4 * jj) * 4u;
+                        if (X == rank)
+                            st_shared_v4(dst + off, w4);
+                        else
+                            st_async_v4(rdst + off, w4, rbar);
+                    }
                 }
             }
-            fence_proxy_async_smem();  // the partial -> visible to the bulk copies
-        }
-        tc_fence_before();
-        if (CS > 1)
-            cluster_sync();  // #1: every partial is written; every receive slot is free
-        else
-            __syncthreads();
-
-        // ================= phase C: owners receive their rows' partials and sum
-        // Each CTA pushes the rows other CTAs own with one bulk shared-to-shared
-        // copy per owner.  Once an owner has received all of them it tells every
-        // sender (remote arrive on its "drained" barrier) that its buffer has been
-        // read; a sender waits for that only before it reuses the buffer.
-        if (CS > 1) {
-            if (tid < CS && tid != rank) {
-                const int dst = tid;
-                const int d_lo = dst * rows / CS;
-                const int d_hi = (dst + 1) * rows / CS;
-                if (d_hi > d_lo) {
-                    const uint32_t slot = (uint32_t)(rank < dst ? rank : rank - 1);
-                    bulk_s2cluster(map_cluster(sP + slot * (uint32_t)p.own_max * row_bytes, (uint32_t)dst),
-                                   sP + p.off_out + (uint32_t)d_lo * row_bytes,
-                                   (uint32_t)(d_hi - d_lo) * row_bytes, map_cluster(recv, (uint32_t)dst));
-                }
-            }
-            if (warp < 8) {
-                wait(recv, (uint32_t)rbi & 1u);
-                if (tid < CS && tid != rank) mbar_arrive_remote(map_cluster(drained, (uint32_t)tid));
-            }
-        }
-        // every MMA has read its stage, so region E (the ring's first stages) is
-        // free: the gather warps copy the first unit's rows while warps 0-7 sum
-        // the partials.  The later units are gathered in phase D straight from
-        // HBM (an L2 prefetch of their rows measured no faster).
-        if (warp >= 8 && nunits > 0) issue_unit(0);
-        {
+            tc_fence_before();       // the accumulators are read before any later MMA
+            named_bar_sync(3, 256);  // own rows in place
+            // ================= phase C: the owner sums its rows' partials
+            if (CS > 1) wait(recv, (uint32_t)rbi & 1u);
             // (row, 4-column group) items; R is a power of two, so no divides
             const int own = o_hi - o_lo;
             const int l2c4 = p.log2R - 2;
             const int nq = own << l2c4;
-            const uint32_t out_a = smem_u32(out_f) + (uint32_t)o_lo * row_bytes;
-            const uint32_t recv_a = smem_u32(recv_f);
             const uint32_t us_a = smem_u32(uslice);
-            for (int qd = warp < 8 ? tid : nq; qd < nq; qd += 256) {
-                const int lr = qd >> l2c4;
+            for (int qd = tid; qd < nq; qd += 256) {
+                const int l = qd >> l2c4;
                 const uint32_t cb = (uint32_t)(qd & ((1 << l2c4) - 1)) * 16u;  // byte column
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
                 for (int src = 0; src < CS; ++src) {  // rank order: deterministic
-                    const uint32_t a =
-                        src == rank ? out_a + (uint32_t)lr * row_bytes + cb
-                                    : recv_a + (uint32_t)((src < rank ? src : src - 1) * p.own_max + lr) *
-                                                   row_bytes + cb;
-                    const uint4 v = lds_v4(a);
+                    const uint4 v = lds_v4(sP + (uint32_t)(src * p.own_max + l) * row_bytes + cb);
                     acc.x += __uint_as_float(v.x);
                     acc.y += __uint_as_float(v.y);
                     acc.z += __uint_as_float(v.z);
                     acc.w += __uint_as_float(v.w);
                 }
-                st_shared_v4(us_a + ((uint32_t)(lr * R) << 2) + cb,
+                st_shared_v4(us_a + ((uint32_t)(l * R) << 2) + cb,
                              make_uint4(__float_as_uint(acc.x), __float_as_uint(acc.y),
                                         __float_as_uint(acc.z), __float_as_uint(acc.w)));
-                *reinterpret_cast<float4*>(p.u + (size_t)(pa + lr) * R + (cb >> 2)) = acc;
+                *reinterpret_cast<float4*>(p.u + (size_t)(pa + l) * R + (cb >> 2)) = acc;
             }
+        } else {
+            // every MMA has read its stage: the edge stages clear of the receive
+            // area are free, and the first units' rows are gathered meanwhile
+            for (int jj = 0; jj < p.n_early && jj < nunits; ++jj) issue_unit(jj);
         }
         __syncthreads();  // u slice complete; the receive slots are free
 
         // ================= phase D: the edge tiles of this CTA's positions
         if (warp >= 8) {
             // gather: issue only; a stage is refilled once the MMA has consumed its
-            // previous unit (unit 0 was issued in phase C)
-            for (int j = 1; j < nunits; ++j) issue_unit(j);
+            // previous unit (the first n_early units were issued in phase B)
+            for (int j = p.n_early; j < nunits; ++j) issue_unit(j);
             cp_async_wait_all();
-            if (!drained_ok) wait(drained, (uint32_t)rbi & 1u);  // before region P is reused
         } else if (warp < 4) {
             // gate: thread tid owns chunk column c of some of the unit's 32 four-row
             // groups (a row slot of cpr threads takes groups g_first, g_first +
@@ -532,7 +519,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
             for (int j = 0; j < nunits; ++j) {
                 const int use = div_by(j, p.estages, p.es_magic);
-                const int st = j - use * p.estages;
+                const int st = phys(j - use * p.estages);
                 const int t = j >> (p.nhalf - 1);
                 const int half = j - t * p.nhalf;
                 const int e0 = e_lo + t * TP;
@@ -796,8 +783,8 @@ struct PlanKey {
 struct Plan {
     bool ok = false;
     int CS = 0, NC = 0, MR = 0, nrb = 0, own_max = 0, pstages = 0, estages = 0, nkb_e = 0, nhalf = 0;
-    int drain_stage = 0;
-    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_out = 0, off_U = 0, off_un = 0;
+    int n_early = 0, sorder = 0;
+    uint32_t pstage_bytes = 0, estage_bytes = 0, off_P = 0, off_U = 0, off_un = 0;
     uint32_t off_ids = 0, off_bar = 0, red_stride = 0;
     size_t smem = 0;
 };
@@ -810,11 +797,12 @@ int g_plan_count = 0;
 int g_plan_next = 0;
 
 // Shared-memory layout for a cluster size and row-block height; false when it
-// does not fit.  Region E = edge stage 0.  Region P = the receive slots
-// [CS-1][own_max] and the outgoing partial [MR] (rows of R + 4 floats), and edge
-// stages 1..estages-1.  The projection's TMA ring spans regions E and P (it is
-// drained before either is used).  Then the u slice, the unary slice, the id
-// ring and the barriers.
+// does not fit.  Region E = edge stage 0.  Region P = the receive area
+// [CS][own_max] (rows of R + 4 floats) from offset 0, and edge stages
+// 1..estages-1.  The projection's TMA ring spans regions E and P (it is drained
+// before either is used).  Then the u slice, the unary slice, the id ring and
+// the barriers.  The edge ring visits stage 0 and the region-P stages clear of
+// the receive area first: those take units while the partials are exchanged.
 bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     q->nkb_e = R >= 128 ? 2 : 1;
     q->nhalf = R / (64 * q->nkb_e);
@@ -823,17 +811,15 @@ bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
     q->red_stride = (uint32_t)R + 4u;
     q->own_max = (MR + CS - 1) / CS;
     const size_t row_bytes = (size_t)q->red_stride * 4;
-    const size_t recv_bytes = (size_t)(CS - 1) * q->own_max * row_bytes;
-    const size_t off_out = (recv_bytes + 1023) & ~(size_t)1023;
-    const size_t red_end = off_out + (size_t)MR * row_bytes;
+    const size_t recv_bytes = (size_t)CS * q->own_max * row_bytes;
     const size_t u_bytes = (size_t)q->own_max * R * 4;
     const size_t un_bytes = (size_t)q->own_max * K * 4;
-    const size_t bar_bytes = 8 * (2 * 8 + 3 + 2 * 4 + 4) + 16;
-    // Region P holds the reduction buffers, then edge stages 1 .. es-1; the
+    const size_t bar_bytes = 8 * (2 * 8 + 2 + 2 * 4 + 4) + 16;
+    // Region P holds the receive area, then edge stages 1 .. es-1; the
     // projection's TMA ring (phase A only) spans regions E and P from offset 0.
     for (int es = 4; es >= 2; --es) {
         const size_t regionP =
-            std::max((red_end + 1023) & ~(size_t)1023, (size_t)(es - 1) * q->estage_bytes);
+            std::max((recv_bytes + 1023) & ~(size_t)1023, (size_t)(es - 1) * q->estage_bytes);
         const size_t off_U = q->estage_bytes + regionP;
         const int ps = (int)std::min<size_t>(6, off_U / q->pstage_bytes);
         const size_t off_un = off_U + ((u_bytes + 15) & ~(size_t)15);
@@ -844,13 +830,21 @@ bool layout(int R, int K, int CS, int MR, size_t max_smem, Plan* q) {
             q->pstages = ps;
             q->estages = es;
             q->off_P = q->estage_bytes;
-            q->off_out = (uint32_t)off_out;
             q->off_U = (uint32_t)off_U;
             q->off_un = (uint32_t)off_un;
             q->off_ids = (uint32_t)off_ids;
             q->off_bar = (uint32_t)off_bar;
-            // first edge stage in region P whose bytes overlap the outgoing partial
-            q->drain_stage = CS > 1 ? 1 + (int)(off_out / q->estage_bytes) : es;
+            // ring order: stage 0, the region-P stages that start at or past the end
+            // of the receive area, then the others
+            int order[4], n = 0;
+            order[n++] = 0;
+            for (int st = 1; st < es; ++st)
+                if ((size_t)(st - 1) * q->estage_bytes >= recv_bytes) order[n++] = st;
+            q->n_early = n;
+            for (int st = 1; st < es; ++st)
+                if ((size_t)(st - 1) * q->estage_bytes < recv_bytes) order[n++] = st;
+            q->sorder = 0;
+            for (int i = 0; i < es; ++i) q->sorder |= order[i] << (4 * i);
             q->smem = total;
             return true;
         }
@@ -1004,12 +998,12 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     p.pstage_bytes = pl.pstage_bytes;
     p.estage_bytes = pl.estage_bytes;
     p.off_P = pl.off_P;
-    p.off_out = pl.off_out;
     p.off_U = pl.off_U;
     p.off_un = pl.off_un;
     p.off_ids = pl.off_ids;
     p.off_bar = pl.off_bar;
-    p.drain_stage = pl.drain_stage;
+    p.n_early = pl.n_early;
+    p.sorder = pl.sorder;
     p.red_stride = pl.red_stride;
     cudaError_t e = cudaFuncSetAttribute(select_fused_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
