@@ -165,6 +165,14 @@ int run_edges(const int32_t* cand_ids, const float* u, const void* A, const void
     df2::EdgesArgs a{cand_ids, u, A, B, unary, S, n, K, R, V, edges_out, best_slot, best_score,
                      err_flag};
     cudaError_t e;
+    if (dtype == DF2_BF16) {
+        // the one-kernel selector's edge phase where it covers the shapes
+        bool launched = false;
+        e = df2::launch_select_edges(a, stream, num_sms_of_current_device(),
+                                     max_smem_optin_of_current_device(), &launched);
+        if (e != cudaSuccess) return cuda_fail(e, "edges launch");
+        if (launched) return DF2_OK;
+    }
     if (dtype == DF2_BF16 && df2::edges_tc_supported(K, R))
         e = df2::launch_edges_bf16_tc(a, u_only_dependency, stream);
     else

@@ -150,6 +150,11 @@ bool select_fused_supported(int K, int R, int d, int n);
 // shapes; the caller then runs the projection and the edge kernel separately.
 cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int num_sms,
                                 size_t max_smem, bool* launched);
+// The edge scores and argmax alone with the one-kernel selector's edge phase (u
+// given; the same shapes as launch_select_fused with any d).  Sets *launched =
+// false when the shapes are not covered; the caller then runs an edge kernel.
+cudaError_t launch_select_edges(const EdgesArgs& a, cudaStream_t stream, int num_sms,
+                                size_t max_smem, bool* launched);
 // Whether launch_select_fused runs for these shapes, and its cluster layout.
 bool select_fused_plan(int S, int n, int d, int K, int R, int num_sms, size_t max_smem,
                        int* cluster_size, int* clusters, int* rows_per_block);

@@ -99,6 +99,7 @@ struct SelParams {
     int nkb_e;         // 64-rank k-blocks per edge stage (1 or 2)
     int nhalf;         // edge stages per tile (R / (64 * nkb_e))
     int n_early;       // edge units gathered while the partials are exchanged
+    int edges_only;    // u is an input: no projection, no exchange (clusters of one)
     int sorder;        // physical edge stage of ring slot i: bits [4i, 4i+4)
     uint32_t pstage_bytes;  // HTILE + R * 128
     uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
@@ -209,8 +210,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         }
     };
     if (tid == 0) {
-        prefetch_tmap(&tmH);
-        prefetch_tmap(&tmW);
+        if (!p.edges_only) {
+            prefetch_tmap(&tmH);
+            prefetch_tmap(&tmW);
+        }
         for (int i = 0; i < p.pstages; ++i) {
             mbar_init(full0 + 8 * i, 1);
             mbar_init(empty0 + 8 * i, 1);
@@ -338,54 +341,56 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         };
 
         // ================= phase A: projection of the row block (+ early gathers)
-        if (warp == 0 || warp == 8) {
-            // TMA producers: warp 0 takes the even k-blocks, warp 8 (idle until the
-            // gathers) the odd ones; each load instruction holds its issuing thread
-            // for a while, so one thread alone falls behind the ring
-            if (lane == 0) {
-                const uint32_t tx = (uint32_t)p.MR * 128u + (uint32_t)R * 128u;
-                for (int kb = kb0 + (warp == 8 ? 1 : 0); kb < kb1; kb += 2) {
-                    const int it = pit + (kb - kb0);
-                    const int use = div_by(it, p.pstages, p.ps_magic);
-                    const int st = it - use * p.pstages;
-                    wait(empty0 + 8 * st, ((uint32_t)use & 1u) ^ 1u);
-                    if (*abort_flag) continue;
-                    const uint32_t fb = full0 + 8 * st;
-                    const uint32_t dst = sE + (uint32_t)st * p.pstage_bytes;
-                    mbar_arrive_expect_tx(fb, tx);
-                    tma_load_2d(dst, &tmH, fb, kb * 64, row0);
-                    tma_load_2d(dst + HTILE, &tmW, fb, kb * 64, 0);
-                }
-            }
-            __syncwarp();
-        } else if (warp <= p.nmma) {
-            // MMA issuers: warp q + 1 takes k-blocks kb0 + q, kb0 + q + nmma, ... into
-            // its own accumulator (columns q*R ..); one issuing thread alone spends
-            // longer per k-block (waits, four MMAs, a commit) than the ring needs
-            if (lane == 0) {
-                const int q = warp - 1;
-                const uint32_t idesc = idesc_bf16_f32(128, R);
-                const uint32_t dq = tmem + (uint32_t)(q * R);
-                for (int kb = kb0 + q; kb < kb1; kb += p.nmma) {
-                    const int it = pit + (kb - kb0);
-                    const int use = div_by(it, p.pstages, p.ps_magic);
-                    const int st = it - use * p.pstages;
-                    wait(full0 + 8 * st, (uint32_t)use & 1u);
-                    tc_fence_after();
-                    const uint32_t a0 = sE + (uint32_t)st * p.pstage_bytes;
-                    const uint32_t b0 = a0 + HTILE;
-                    if (!*abort_flag) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma_bf16(dq, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
-                                        idesc, (kb > kb0 + q || k > 0) ? 1u : 0u);
+        if (!p.edges_only) {
+            if (warp == 0 || warp == 8) {
+                // TMA producers: warp 0 takes the even k-blocks, warp 8 (idle until the
+                // gathers) the odd ones; each load instruction holds its issuing thread
+                // for a while, so one thread alone falls behind the ring
+                if (lane == 0) {
+                    const uint32_t tx = (uint32_t)p.MR * 128u + (uint32_t)R * 128u;
+                    for (int kb = kb0 + (warp == 8 ? 1 : 0); kb < kb1; kb += 2) {
+                        const int it = pit + (kb - kb0);
+                        const int use = div_by(it, p.pstages, p.ps_magic);
+                        const int st = it - use * p.pstages;
+                        wait(empty0 + 8 * st, ((uint32_t)use & 1u) ^ 1u);
+                        if (*abort_flag) continue;
+                        const uint32_t fb = full0 + 8 * st;
+                        const uint32_t dst = sE + (uint32_t)st * p.pstage_bytes;
+                        mbar_arrive_expect_tx(fb, tx);
+                        tma_load_2d(dst, &tmH, fb, kb * 64, row0);
+                        tma_load_2d(dst + HTILE, &tmW, fb, kb * 64, 0);
                     }
-                    tc_commit(empty0 + 8 * st);
                 }
-                tc_commit(accum);  // every issuer arrives once, with or without k-blocks
+                __syncwarp();
+            } else if (warp <= p.nmma) {
+                // MMA issuers: warp q + 1 takes k-blocks kb0 + q, kb0 + q + nmma, ... into
+                // its own accumulator (columns q*R ..); one issuing thread alone spends
+                // longer per k-block (waits, four MMAs, a commit) than the ring needs
+                if (lane == 0) {
+                    const int q = warp - 1;
+                    const uint32_t idesc = idesc_bf16_f32(128, R);
+                    const uint32_t dq = tmem + (uint32_t)(q * R);
+                    for (int kb = kb0 + q; kb < kb1; kb += p.nmma) {
+                        const int it = pit + (kb - kb0);
+                        const int use = div_by(it, p.pstages, p.ps_magic);
+                        const int st = it - use * p.pstages;
+                        wait(full0 + 8 * st, (uint32_t)use & 1u);
+                        tc_fence_after();
+                        const uint32_t a0 = sE + (uint32_t)st * p.pstage_bytes;
+                        const uint32_t b0 = a0 + HTILE;
+                        if (!*abort_flag) {
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_bf16(dq, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                            idesc, (kb > kb0 + q || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit(empty0 + 8 * st);
+                    }
+                    tc_commit(accum);  // every issuer arrives once, with or without k-blocks
+                }
+                __syncwarp();
+            } else if (warp >= 8) {
             }
-            __syncwarp();
-        } else if (warp >= 8) {
         }
         pit += kb1 - kb0;
         // the epilogue warps, idle until the partial is ready, stage the unary
@@ -397,99 +402,118 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 reinterpret_cast<float4*>(unslice)[qd] = __ldg(src + qd);
         }
 
-        // ================= phase B: one cluster barrier, then the split-d partials
-        // The barrier shows every CTA of the cluster done with its projection
-        // (its ring drained, so its receive area is free).  Warps 0-7 then move
-        // the accumulators (summed in issuer order: deterministic) straight from
-        // tensor memory to the owners of the rows: warp w takes lane quadrant
-        // w % 4 and half of the columns; a row another CTA owns goes into that
-        // CTA's receive slot with asynchronous remote stores (st.async) that
-        // complete on its receive barrier, an own row into the own slot.  No
-        // outgoing copy of the partial is kept, so the receive area is the only
-        // exchange memory and the edge stages clear of it take the first units'
-        // gathers meanwhile (warps 8-15).
-        if (tid == 0 && CS > 1)
-            mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * (uint32_t)R * 4u);
-        wait(accum, (uint32_t)rbi & 1u);
-        tc_fence_before();
-        if (CS > 1)
-            cluster_sync();
-        else
-            __syncthreads();
-        tc_fence_after();
-        if (warp < 8) {
-            const int q = warp & 3;
-            const int cw = R >> 1;
-            const int c_lo = (warp >> 2) * cw;
-            const int row = q * 32 + lane;
-            const int nacc = min(p.nmma, kb1 - kb0);  // accumulators that received MMAs
-            // owner X of the row: X*rows/CS <= row < (X+1)*rows/CS
-            int X = 0;
-            while (X + 1 < CS && (X + 1) * rows < (row + 1) * CS) ++X;
-            const int lr = row - X * rows / CS;
-            const uint32_t dst = sP + ((uint32_t)(rank * p.own_max + lr)) * row_bytes;
-            const uint32_t rdst = X == rank ? dst : map_cluster(dst, (uint32_t)X);
-            const uint32_t rbar = map_cluster(recv, (uint32_t)X);
-            for (int c0 = c_lo; c0 < c_lo + cw; c0 += 16) {
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
-                float f[16];
-                {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(ta, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) f[jj] = __uint_as_float(v[jj]);
+        if (p.edges_only) {
+            // u is the caller's: warps 0-7 copy this CTA's rows of it on chip while
+            // the gather warps issue the first units (every edge stage is free)
+            if (warp < 8) {
+                const int l2c4 = p.log2R - 2;
+                const int nq = (o_hi - o_lo) << l2c4;
+                const uint32_t us_a = smem_u32(uslice);
+                const float4* ug = reinterpret_cast<const float4*>(p.u + (size_t)pa * R);
+                for (int qd = tid; qd < nq; qd += 256) {
+                    const float4 v = __ldg(ug + qd);
+                    st_shared_v4(us_a + (uint32_t)qd * 16u,
+                                 make_uint4(__float_as_uint(v.x), __float_as_uint(v.y),
+                                            __float_as_uint(v.z), __float_as_uint(v.w)));
                 }
-                for (int a = 1; a < nacc; ++a) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(ta + (uint32_t)(a * R), v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) f[jj] += __uint_as_float(v[jj]);
-                }
-                if (row < rows) {
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const uint4 w4 = make_uint4(__float_as_uint(f[4 * jj]), __float_as_uint(f[4 * jj + 1]),
-                                                    __float_as_uint(f[4 * jj + 2]), __float_as_uint(f[4 * jj + 3]));
-                        const uint32_t off = (uint32_t)(c0 + 4 * jj) * 4u;
-                        if (X == rank)
-                            st_shared_v4(dst + off, w4);
-                        else
-                            st_async_v4(rdst + off, w4, rbar);
-                    }
-                }
-            }
-            tc_fence_before();       // the accumulators are read before any later MMA
-            named_bar_sync(3, 256);  // own rows in place
-            // ================= phase C: the owner sums its rows' partials
-            if (CS > 1) wait(recv, (uint32_t)rbi & 1u);
-            // (row, 4-column group) items; R is a power of two, so no divides
-            const int own = o_hi - o_lo;
-            const int l2c4 = p.log2R - 2;
-            const int nq = own << l2c4;
-            const uint32_t us_a = smem_u32(uslice);
-            for (int qd = tid; qd < nq; qd += 256) {
-                const int l = qd >> l2c4;
-                const uint32_t cb = (uint32_t)(qd & ((1 << l2c4) - 1)) * 16u;  // byte column
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                for (int src = 0; src < CS; ++src) {  // rank order: deterministic
-                    const uint4 v = lds_v4(sP + (uint32_t)(src * p.own_max + l) * row_bytes + cb);
-                    acc.x += __uint_as_float(v.x);
-                    acc.y += __uint_as_float(v.y);
-                    acc.z += __uint_as_float(v.z);
-                    acc.w += __uint_as_float(v.w);
-                }
-                st_shared_v4(us_a + ((uint32_t)(l * R) << 2) + cb,
-                             make_uint4(__float_as_uint(acc.x), __float_as_uint(acc.y),
-                                        __float_as_uint(acc.z), __float_as_uint(acc.w)));
-                *reinterpret_cast<float4*>(p.u + (size_t)(pa + l) * R + (cb >> 2)) = acc;
+            } else {
+                for (int jj = 0; jj < p.n_early && jj < nunits; ++jj) issue_unit(jj);
             }
         } else {
-            // every MMA has read its stage: the edge stages clear of the receive
-            // area are free, and the first units' rows are gathered meanwhile
-            for (int jj = 0; jj < p.n_early && jj < nunits; ++jj) issue_unit(jj);
+            // ================= phase B: one cluster barrier, then the split-d partials
+            // The barrier shows every CTA of the cluster done with its projection
+            // (its ring drained, so its receive area is free).  Warps 0-7 then move
+            // the accumulators (summed in issuer order: deterministic) straight from
+            // tensor memory to the owners of the rows: warp w takes lane quadrant
+            // w % 4 and half of the columns; a row another CTA owns goes into that
+            // CTA's receive slot with asynchronous remote stores (st.async) that
+            // complete on its receive barrier, an own row into the own slot.  No
+            // outgoing copy of the partial is kept, so the receive area is the only
+            // exchange memory and the edge stages clear of it take the first units'
+            // gathers meanwhile (warps 8-15).
+            if (tid == 0 && CS > 1)
+                mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * (uint32_t)R * 4u);
+            wait(accum, (uint32_t)rbi & 1u);
+            tc_fence_before();
+            if (CS > 1)
+                cluster_sync();
+            else
+                __syncthreads();
+            tc_fence_after();
+            if (warp < 8) {
+                const int q = warp & 3;
+                const int cw = R >> 1;
+                const int c_lo = (warp >> 2) * cw;
+                const int row = q * 32 + lane;
+                const int nacc = min(p.nmma, kb1 - kb0);  // accumulators that received MMAs
+                // owner X of the row: X*rows/CS <= row < (X+1)*rows/CS
+                int X = 0;
+                while (X + 1 < CS && (X + 1) * rows < (row + 1) * CS) ++X;
+                const int lr = row - X * rows / CS;
+                const uint32_t dst = sP + ((uint32_t)(rank * p.own_max + lr)) * row_bytes;
+                const uint32_t rdst = X == rank ? dst : map_cluster(dst, (uint32_t)X);
+                const uint32_t rbar = map_cluster(recv, (uint32_t)X);
+                for (int c0 = c_lo; c0 < c_lo + cw; c0 += 16) {
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0;
+                    float f[16];
+                    {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(ta, v);
+                        tmem_ld_wait();
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) f[jj] = __uint_as_float(v[jj]);
+                    }
+                    for (int a = 1; a < nacc; ++a) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(ta + (uint32_t)(a * R), v);
+                        tmem_ld_wait();
+    #pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) f[jj] += __uint_as_float(v[jj]);
+                    }
+                    if (row < rows) {
+    #pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const uint4 w4 = make_uint4(__float_as_uint(f[4 * jj]), __float_as_uint(f[4 * jj + 1]),
+                                                        __float_as_uint(f[4 * jj + 2]), __float_as_uint(f[4 * jj + 3]));
+                            const uint32_t off = (uint32_t)(c0 + 4 * jj) * 4u;
+                            if (X == rank)
+                                st_shared_v4(dst + off, w4);
+                            else
+                                st_async_v4(rdst + off, w4, rbar);
+                        }
+                    }
+                }
+                tc_fence_before();       // the accumulators are read before any later MMA
+                named_bar_sync(3, 256);  // own rows in place
+                // ================= phase C: the owner sums its rows' partials
+                if (CS > 1) wait(recv, (uint32_t)rbi & 1u);
+                // (row, 4-column group) items; R is a power of two, so no divides
+                const int own = o_hi - o_lo;
+                const int l2c4 = p.log2R - 2;
+                const int nq = own << l2c4;
+                const uint32_t us_a = smem_u32(uslice);
+                for (int qd = tid; qd < nq; qd += 256) {
+                    const int l = qd >> l2c4;
+                    const uint32_t cb = (uint32_t)(qd & ((1 << l2c4) - 1)) * 16u;  // byte column
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll 4
+                    for (int src = 0; src < CS; ++src) {  // rank order: deterministic
+                        const uint4 v = lds_v4(sP + (uint32_t)(src * p.own_max + l) * row_bytes + cb);
+                        acc.x += __uint_as_float(v.x);
+                        acc.y += __uint_as_float(v.y);
+                        acc.z += __uint_as_float(v.z);
+                        acc.w += __uint_as_float(v.w);
+                    }
+                    st_shared_v4(us_a + ((uint32_t)(l * R) << 2) + cb,
+                                 make_uint4(__float_as_uint(acc.x), __float_as_uint(acc.y),
+                                            __float_as_uint(acc.z), __float_as_uint(acc.w)));
+                    *reinterpret_cast<float4*>(p.u + (size_t)(pa + l) * R + (cb >> 2)) = acc;
+                }
+            } else {
+                // every MMA has read its stage: the edge stages clear of the receive
+                // area are free, and the first units' rows are gathered meanwhile
+                for (int jj = 0; jj < p.n_early && jj < nunits; ++jj) issue_unit(jj);
+            }
         }
         __syncthreads();  // u slice complete; the receive slots are free
 
@@ -928,12 +952,36 @@ Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
     return best;
 }
 
+// Edges only (u given): one CTA per cluster, rows cut so that every SM gets a
+// row block (at most 128 rows, fewer if the layout needs it), every edge stage
+// free from the start.
+Plan make_edges_plan(int P, int R, int K, int sms, size_t max_smem) {
+    Plan best;
+    int MR = std::min(128, (P + sms - 1) / sms);
+    Plan q;
+    while (MR > 0 && !layout(R, K, 1, MR, max_smem, &q)) --MR;
+    if (MR == 0) return best;
+    best = q;
+    best.ok = true;
+    best.CS = 1;
+    best.MR = MR;
+    best.nrb = (P + MR - 1) / MR;
+    best.NC = std::min(best.nrb, sms);
+    best.n_early = best.estages;
+    best.sorder = 0;
+    for (int i = 0; i < best.estages; ++i) best.sorder |= i << (4 * i);
+    if (best.smem < kMinSmem) best.smem = kMinSmem;
+    return best;
+}
+
+// d = 0 keys the edges-only plans (a projection always has d > 0).
 Plan get_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
     const PlanKey key{P, d, R, K, n, sms};
     std::lock_guard<std::mutex> lk(g_plan_mu);
     for (int i = 0; i < g_plan_count; ++i)
         if (g_plan_keys[i] == key) return g_plans[i];
-    const Plan pl = make_plan(P, d, R, K, n, sms, max_smem);
+    const Plan pl = d == 0 ? make_edges_plan(P, R, K, sms, max_smem)
+                           : make_plan(P, d, R, K, n, sms, max_smem);
     const int slot = g_plan_count < kPlanCache ? g_plan_count++ : (g_plan_next++ % kPlanCache);
     g_plan_keys[slot] = key;
     g_plans[slot] = pl;
@@ -947,17 +995,15 @@ bool select_fused_supported(int K, int R, int d, int n) {
            d % 8 == 0 && n >= 2;
 }
 
-cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int num_sms,
-                                size_t max_smem, bool* launched) {
-    *launched = false;
+namespace {
+
+// Launches the kernel for a plan: the fused selector (tensor maps of h and W),
+// or with edges_only the edge phase alone on the caller's u (maps unused).
+cudaError_t launch_plan(const SelectArgs& a, const Plan& pl, const CUtensorMap& tmH,
+                        const CUtensorMap& tmW, int edges_only, cudaStream_t stream) {
     const int P = a.S * a.n;
-    const Plan pl = get_plan(P, a.d, a.R, a.K, a.n, num_sms, max_smem);
-    if (!pl.ok) return cudaSuccess;  // the caller falls back to the two-kernel path
-    CUtensorMap tmH, tmW;
-    if (!make_tmap_rows_bf16(&tmH, a.h, P, a.d, pl.MR) ||
-        !make_tmap_rows_bf16(&tmW, a.W, a.R, a.d, a.R))
-        return cudaErrorInvalidValue;
     SelParams p{};
+    p.edges_only = edges_only;
     p.cand_ids = a.cand_ids;
     p.unary = a.unary;
     p.A = static_cast<const __nv_bfloat16*>(a.A);
@@ -1025,12 +1071,44 @@ cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int nu
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.attrs = pl.CS > 1 ? attr : attr + 1;  // no cluster attribute for clusters of one
+    cfg.numAttrs = pl.CS > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, select_fused_kernel, tmH, tmW, p);
     if (e != cudaSuccess) return e;
-    *launched = true;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_select_fused(const SelectArgs& a, cudaStream_t stream, int num_sms,
+                                size_t max_smem, bool* launched) {
+    *launched = false;
+    const int P = a.S * a.n;
+    const Plan pl = get_plan(P, a.d, a.R, a.K, a.n, num_sms, max_smem);
+    if (!pl.ok) return cudaSuccess;  // the caller falls back to the two-kernel path
+    CUtensorMap tmH, tmW;
+    if (!make_tmap_rows_bf16(&tmH, a.h, P, a.d, pl.MR) ||
+        !make_tmap_rows_bf16(&tmW, a.W, a.R, a.d, a.R))
+        return cudaErrorInvalidValue;
+    const cudaError_t e = launch_plan(a, pl, tmH, tmW, 0, stream);
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+cudaError_t launch_select_edges(const EdgesArgs& ea, cudaStream_t stream, int num_sms,
+                                size_t max_smem, bool* launched) {
+    *launched = false;
+    if (!select_fused_supported(ea.K, ea.R, 8, ea.n)) return cudaSuccess;
+    const int P = ea.S * ea.n;
+    const Plan pl = get_plan(P, 0, ea.R, ea.K, ea.n, num_sms, max_smem);
+    if (!pl.ok) return cudaSuccess;
+    SelectArgs a{nullptr, nullptr, ea.cand_ids, ea.A, ea.B, ea.unary, ea.S, ea.n, 0, ea.K,
+                 ea.R, ea.V, const_cast<float*>(ea.u), ea.edges_out, ea.best_slot,
+                 ea.best_score, ea.err_flag};
+    const CUtensorMap none{};  // never read in edges-only mode
+    const cudaError_t e = launch_plan(a, pl, none, none, 1, stream);
+    if (e == cudaSuccess) *launched = true;
+    return e;
 }
 
 bool select_fused_plan(int S, int n, int d, int K, int R, int num_sms, size_t max_smem,
