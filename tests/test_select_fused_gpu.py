@@ -114,3 +114,20 @@ def test_fused_select_repeated_calls_are_identical():
     _, _, u1, e1, s1, _ = run(w)
     _, _, u2, e2, s2, _ = run(w)
     assert torch.equal(u1, u2) and torch.equal(e1, e2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("S,n,d,K,R,V", [
+    (256, 16, 512, 16, 128, 151936),  # the batched shape's edge work (d shortened)
+    (16, 8, 256, 64, 256, 4096),      # two units per tile (R = 256), K = 64
+    (7, 5, 256, 4, 64, 500),          # K = 4, R = 64, ragged tiles
+])
+def test_edges_call_matches_the_selectors_edge_phase(S, n, d, K, R, V):
+    """dflash2_edges on bf16 codebooks runs the selector's edge phase on the given u,
+    with its own row decomposition (one CTA per cluster): given the selector's u it
+    must reproduce the selector's edge scores, argmax and best scores exactly."""
+    w = W_(S, n, d, K, R, V)
+    cb, sel, u, e, slot, score = run(w)
+    e2, slot2, score2 = df2.edges(dev(sel["cand_ids"]), u, dev(cb["A"], "bf16"),
+                                  dev(cb["B"], "bf16"), dev(sel["unary"]), edges_out=True)
+    torch.cuda.synchronize()
+    assert torch.equal(e, e2) and torch.equal(slot, slot2) and torch.equal(score, score2)
