@@ -99,7 +99,6 @@ struct SelParams {
     int nkb_e;         // 64-rank k-blocks per edge stage (1 or 2)
     int nhalf;         // edge stages per tile (R / (64 * nkb_e))
     int n_early;       // edge units gathered while the partials are exchanged
-    int edges_only;    // u is an input: no projection, no exchange (clusters of one)
     int sorder;        // physical edge stage of ring slot i: bits [4i, 4i+4)
     uint32_t pstage_bytes;  // HTILE + R * 128
     uint32_t estage_bytes;  // 2 * nkb_e * KB_OP
@@ -160,6 +159,9 @@ __device__ __forceinline__ int trans_before(int q, int n) {
     return s * (n - 1) + (i > 0 ? i - 1 : 0);
 }
 
+// EDGES_ONLY: u is an input; no projection and no exchange (clusters of one),
+// every edge stage free from the start.
+template <bool EDGES_ONLY>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_fused_kernel(const __grid_constant__ CUtensorMap tmH,
                         const __grid_constant__ CUtensorMap tmW, const SelParams p) {
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         }
     };
     if (tid == 0) {
-        if (!p.edges_only) {
+        if constexpr (!EDGES_ONLY) {
             prefetch_tmap(&tmH);
             prefetch_tmap(&tmW);
         }
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         };
 
         // ================= phase A: projection of the row block (+ early gathers)
-        if (!p.edges_only) {
+        if constexpr (!EDGES_ONLY) {
             if (warp == 0 || warp == 8) {
                 // TMA producers: warp 0 takes the even k-blocks, warp 8 (idle until the
                 // gathers) the odd ones; each load instruction holds its issuing thread
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 reinterpret_cast<float4*>(unslice)[qd] = __ldg(src + qd);
         }
 
-        if (p.edges_only) {
+        if constexpr (EDGES_ONLY) {
             // u is the caller's: warps 0-7 copy this CTA's rows of it on chip while
             // the gather warps issue the first units (every edge stage is free)
             if (warp < 8) {
@@ -889,12 +891,12 @@ int max_active_clusters(int CS, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    bool ok = cudaFuncSetAttribute(select_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    bool ok = cudaFuncSetAttribute(select_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem) == cudaSuccess;
     if (ok && CS > 8)
-        ok = cudaFuncSetAttribute(select_fused_kernel,
+        ok = cudaFuncSetAttribute(select_fused_kernel<false>,
                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    if (ok) ok = cudaOccupancyMaxActiveClusters(&n, select_fused_kernel, &cfg) == cudaSuccess;
+    if (ok) ok = cudaOccupancyMaxActiveClusters(&n, select_fused_kernel<false>, &cfg) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();  // an unsupported cluster size is not an error of the call
         return 0;
@@ -1003,7 +1005,6 @@ cudaError_t launch_plan(const SelectArgs& a, const Plan& pl, const CUtensorMap& 
                         const CUtensorMap& tmW, int edges_only, cudaStream_t stream) {
     const int P = a.S * a.n;
     SelParams p{};
-    p.edges_only = edges_only;
     p.cand_ids = a.cand_ids;
     p.unary = a.unary;
     p.A = static_cast<const __nv_bfloat16*>(a.A);
@@ -1051,11 +1052,11 @@ cudaError_t launch_plan(const SelectArgs& a, const Plan& pl, const CUtensorMap& 
     p.n_early = pl.n_early;
     p.sorder = pl.sorder;
     p.red_stride = pl.red_stride;
-    cudaError_t e = cudaFuncSetAttribute(select_fused_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    auto kern = edges_only ? select_fused_kernel<true> : select_fused_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
     if (pl.CS > 8) {
-        e = cudaFuncSetAttribute(select_fused_kernel,
+        e = cudaFuncSetAttribute(kern,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
@@ -1073,7 +1074,7 @@ cudaError_t launch_plan(const SelectArgs& a, const Plan& pl, const CUtensorMap& 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pl.CS > 1 ? attr : attr + 1;  // no cluster attribute for clusters of one
     cfg.numAttrs = pl.CS > 1 ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, select_fused_kernel, tmH, tmW, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmH, tmW, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
