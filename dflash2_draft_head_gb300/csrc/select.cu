@@ -911,8 +911,13 @@ int max_active_clusters(int CS, size_t smem) {
 constexpr size_t kMinSmem = 120 * 1024;
 
 // Picks the cluster size and row-block height with the least modelled time per
-// CTA: HBM bytes of h and of the gathered rows, plus the L2-served slice of W
-// at a third of their weight, times the number of waves of row blocks.
+// CTA, times the number of waves of row blocks: the HBM bytes of h and of the
+// gathered rows; the L2-served slice of W at half their weight; and the
+// partials the CTA receives through distributed shared memory at 2.7 times
+// their weight (its remote stores run at about 15 GB/s per SM against about
+// 41 GB/s for the gathers).  Weights fitted to cluster-size sweeps on GB300:
+// batched 256 x 16 (CS 4 best), wide 64 x 8 with R = 256 (CS 6-8 best, 16
+// 15 % slower), one draft block (CS 16 best).
 Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
     Plan best;
     double best_cost = 0;
@@ -939,7 +944,8 @@ Plan make_plan(int P, int d, int R, int K, int n, int sms, size_t max_smem) {
         const double h_b = MR * kpc * 128.0;
         const double w_b = R * kpc * 128.0;
         const double g_b = (double)q.own_max * E_per_pos * 2.0 * K * R * 2.0;
-        const double cost = waves * (h_b + g_b + w_b / 3.0) + 1e-3 * NC * CS;
+        const double x_b = (double)(CS - 1) * q.own_max * R * 4.0;
+        const double cost = waves * (h_b + g_b + 0.5 * w_b + 2.7 * x_b) + 1e-3 * NC * CS;
         if (!best.ok || cost < best_cost) {
             best = q;
             best.ok = true;
