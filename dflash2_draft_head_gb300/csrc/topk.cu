@@ -1583,6 +1583,8 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
 //  4. the other ranks store their sorted lists into rank 0's shared memory
 //     (distributed shared memory) before one cluster barrier; rank 0 merges
 //     them pairwise and writes the row from the sorted result.
+// The cluster size is the largest in 1..8 (not only powers of two) whose
+// clusters for all rows are resident at once.
 // Keys, ties, NaN and the sign of zero follow the streaming kernels exactly.
 constexpr int kRowsMaxK = 32;
 constexpr int kRowsThreads = 512;                  // the first kNC run the exact select
@@ -1603,8 +1605,9 @@ __device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
-// Pairwise merges of n (a power of two, <= 16) descending 32-key lists held at
-// lists[32*w .. 32*w + 31] into the sorted top 32 at lists[0 .. 31];
+// Pairwise merges of n (<= 16) descending 32-key lists held at
+// lists[32*w .. 32*w + 31] into the sorted top 32 at lists[0 .. 31], as a
+// binary tree in which a list without a partner waits a round;
 // block-collective (every thread calls it).
 __device__ __forceinline__ void rows_merge_lists(uint64_t* lists, int n) {
     const int lane = threadIdx.x & 31;
@@ -1765,7 +1768,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1) topk_rows_kernel(const TopkPa
 struct DeviceInfo {
     bool ready = false;
     int max_clusters[2][2][4] = {};  // [async][bf16][log2 cs]: clusters resident at once
-    int rows_clusters[2][5][4] = {};  // few-row kernel: [bf16][VPT index][log2 cluster size]
+    int rows_clusters[2][5][9] = {};  // few-row kernel: [bf16][VPT index][cluster size 1..8]
 };
 
 std::mutex g_mu;
@@ -1799,6 +1802,36 @@ cudaError_t query_kernel(Kern kern, uint32_t smem_bytes, int threads, int (&out)
     return cudaSuccess;
 }
 
+// Clusters of the few-row kernel resident at once, for every cluster size 1..8
+// (its merge takes any size, not only powers of two).
+template <typename Kern>
+cudaError_t query_rows_kernel(Kern kern, uint32_t smem_bytes, int (&out)[9]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    out[0] = 0;
+    for (int cs = 1; cs <= 8; ++cs) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(cs, 1, 1);
+        cfg.blockDim = dim3(kRowsThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem_bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        out[cs] = n;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t query_device(DeviceInfo& d) {
     cudaError_t e = query_kernel(topk_kernel<false>, kSmem, kThreads, d.max_clusters[0][0]);
     if (e == cudaSuccess) e = query_kernel(topk_kernel<true>, kSmem, kThreads, d.max_clusters[0][1]);
@@ -1809,8 +1842,8 @@ cudaError_t query_device(DeviceInfo& d) {
     constexpr uint32_t rs = (uint32_t)sizeof(RowsSmem);
 #define DF2_ROWS_Q(BF, I)                                                                         \
     if (e == cudaSuccess)                                                                         \
-        e = query_kernel(topk_rows_kernel<BF, kRowsVpts[I]>, rs, kRowsThreads,                    \
-                         d.rows_clusters[BF ? 1 : 0][I]);
+        e = query_rows_kernel(topk_rows_kernel<BF, kRowsVpts[I]>, rs,                            \
+                              d.rows_clusters[BF ? 1 : 0][I]);
     DF2_ROWS_Q(false, 0) DF2_ROWS_Q(false, 1) DF2_ROWS_Q(false, 2) DF2_ROWS_Q(false, 3)
     DF2_ROWS_Q(false, 4) DF2_ROWS_Q(true, 0) DF2_ROWS_Q(true, 1) DF2_ROWS_Q(true, 2)
     DF2_ROWS_Q(true, 3) DF2_ROWS_Q(true, 4)
@@ -1864,14 +1897,13 @@ cudaError_t launch_any(const TopkLaunch& a, cudaStream_t stream) {
         const int esz = a.bf16 ? 2 : 4;
         if (a.K <= kRowsMaxK && (a.V * esz) % 16 == 0 &&
             reinterpret_cast<uintptr_t>(a.logits) % 16 == 0) {
-            for (int l = 3; l >= 0 && rows_cs == 0; --l) {
-                const int P = 1 << l;
+            for (int P = 8; P >= 1 && rows_cs == 0; --P) {
                 const long long vecs = ((long long)(a.V + P - 1) / P * esz + 15) / 16 + 1;
                 const long long vpt = (vecs + kRowsThreads - 1) / kRowsThreads;
                 int vi = 0;
                 while (vi < 5 && kRowsVpts[vi] < vpt) ++vi;
                 if (vi == 5) break;  // smaller clusters: longer chunks
-                if (a.rows <= d.rows_clusters[a.bf16 ? 1 : 0][vi][l]) {
+                if (a.rows <= d.rows_clusters[a.bf16 ? 1 : 0][vi][P]) {
                     rows_cs = P;
                     rows_vi = vi;
                 }
