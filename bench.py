@@ -48,12 +48,12 @@ TRAFFIC = {
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
     ("batched_256x16_d5120", "topk"): {
-        "sha": "51944453c7adcd3de91c05c4fcfa47165324136335a91958d79abf62d059e449",
-        "bytes": 8 * (311331840 + 3218176),
+        "sha": "2a7da80a81a4f70142e6369571006d546d905c8c4ad86e8c36370c2f68ca3550",
+        "bytes": 8 * (311296512 + 3386624),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "b021f08e109a6c10d045beb1c068741e8a8721fdf5f96e818ba142ebff585f54",
-        "bytes": 69800192 + 1122560,
+        "sha": "9d1f34eb8e1547391f7cfccba06cd7120f90f7b27fa698d2c978c1e568f448aa",
+        "bytes": 69796608 + 955392,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
