@@ -253,6 +253,9 @@ def test_edges_without_edge_matrix():
     dict(S=2, n=4, K=16, R=512, V=3000),   # warp path, maximum R
     dict(S=1, n=2, K=64, R=384, V=3000),   # tile path, maximum R
     dict(S=37, n=3, K=16, R=128, V=20000), # ragged last tile (74 transitions)
+    # bf16, K a power of two and R in {64, 128, 256}: the selector's edge phase alone
+    dict(S=9, n=5, K=4, R=64, V=1000),     # K = 4, R = 64
+    dict(S=1300, n=16, K=16, R=128, V=5000),  # 20800 positions: CTAs take two row blocks
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_edges_edge_shapes(kw, dtype):
@@ -269,9 +272,10 @@ def test_edges_single_position_launches_nothing():
     assert e.shape == (2, 0, 4, 4) and slot.shape == (2, 0, 4)
 
 
+@pytest.mark.parametrize("R", [32, 64])  # bf16 R = 64: the selector's edge phase
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_edges_bad_ids_are_clamped_and_flagged(dtype):
-    w = W_(S=2, n=4, K=8, R=32, V=64, dtype=dtype)
+def test_edges_bad_ids_are_clamped_and_flagged(dtype, R):
+    w = W_(S=2, n=4, K=8, R=R, V=64, dtype=dtype)
     cb = synth.codebooks(w)
     sel = synth.selector_inputs(w)
     ids = sel["cand_ids"].clone()
