@@ -437,10 +437,17 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * (uint32_t)R * 4u);
             wait(accum, (uint32_t)rbi & 1u);
             tc_fence_before();
-            if (CS > 1)
-                cluster_sync();
-            else
+            // the gather warps only arrive: their first units need this CTA's ring
+            // drained (the accumulator barrier), not the rest of the cluster, so
+            // they wait for the barrier after issuing them
+            if (CS > 1) {
+                if (warp < 8)
+                    cluster_sync();
+                else
+                    cluster_arrive();
+            } else {
                 __syncthreads();
+            }
             tc_fence_after();
             if (warp < 8) {
                 const int q = warp & 3;
@@ -515,6 +522,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 // every MMA has read its stage: the edge stages clear of the receive
                 // area are free, and the first units' rows are gathered meanwhile
                 for (int jj = 0; jj < p.n_early && jj < nunits; ++jj) issue_unit(jj);
+                if (CS > 1) cluster_wait();
             }
         }
         __syncthreads();  // u slice complete; the receive slots are free
