@@ -228,53 +228,32 @@ struct PipeParams {
 };
 
 
-// A thread's staged row segment: NP packed bf16 pairs (NP = 4: 8 channels in
-// 16 bytes; NP = 2: 4 channels in 8 bytes), converted to fp32 pairs.
+// A thread's staged row segment: NP = 4 packed bf16 pairs (8 channels in 16
+// bytes), converted to fp32 pairs.
 template <int NP>
 __device__ __forceinline__ void load_row_f2(uint32_t addr, float2 (&f)[NP]) {
-    if constexpr (NP == 4) {
-        const uint4 v = lds_v4(addr);
-        f[0] = bf16x2_to_f2(v.x);
-        f[1] = bf16x2_to_f2(v.y);
-        f[2] = bf16x2_to_f2(v.z);
-        f[3] = bf16x2_to_f2(v.w);
-    } else {
-        const uint2 v = lds_v2(addr);
-        f[0] = bf16x2_to_f2(v.x);
-        f[1] = bf16x2_to_f2(v.y);
-    }
+    static_assert(NP == 4, "8-channel threads");
+    const uint4 v = lds_v4(addr);
+    f[0] = bf16x2_to_f2(v.x);
+    f[1] = bf16x2_to_f2(v.y);
+    f[2] = bf16x2_to_f2(v.z);
+    f[3] = bf16x2_to_f2(v.w);
 }
 
 template <int NP>
 __device__ __forceinline__ void load_base_f2(const __nv_bfloat16* p, bool active, float2 (&f)[NP]) {
-    if constexpr (NP == 4) {
-        const uint4 v = active ? ldg_nc_v4(p) : make_uint4(0, 0, 0, 0);
-        f[0] = bf16x2_to_f2(v.x);
-        f[1] = bf16x2_to_f2(v.y);
-        f[2] = bf16x2_to_f2(v.z);
-        f[3] = bf16x2_to_f2(v.w);
-    } else {
-        const uint2 v = active ? __ldg(reinterpret_cast<const uint2*>(p)) : make_uint2(0, 0);
-        f[0] = bf16x2_to_f2(v.x);
-        f[1] = bf16x2_to_f2(v.y);
-    }
+    static_assert(NP == 4, "8-channel threads");
+    const uint4 v = active ? ldg_nc_v4(p) : make_uint4(0, 0, 0, 0);
+    f[0] = bf16x2_to_f2(v.x);
+    f[1] = bf16x2_to_f2(v.y);
+    f[2] = bf16x2_to_f2(v.z);
+    f[3] = bf16x2_to_f2(v.w);
 }
 
 __device__ __forceinline__ void store_pairs(__nv_bfloat16* p, const float2 (&acc)[4]) {
     store_row(p, acc);
 }
 __device__ __forceinline__ void store_pairs(float* p, const float2 (&acc)[4]) { store_row(p, acc); }
-__device__ __forceinline__ void store_pairs(__nv_bfloat16* p, const float2 (&acc)[2]) {
-    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0].x, acc[0].y);
-    __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[1].x, acc[1].y);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&b0);
-    v.y = *reinterpret_cast<uint32_t*>(&b1);
-    *reinterpret_cast<uint2*>(p) = v;
-}
-__device__ __forceinline__ void store_pairs(float* p, const float2 (&acc)[2]) {
-    *reinterpret_cast<float4*>(p) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-}
 
 // One output position: acc = sum_t (base_t + delta_t) * x_{i-t}; xw[t] holds
 // x_{i-t}; dtl[t] is delta_t of this thread's group (fp32, contiguous).
@@ -298,23 +277,9 @@ __device__ __forceinline__ void conv_point(const float2 (&bw)[T][NP], const floa
         acc[q] = make_float2(0.f, 0.f);
         odd[q] = make_float2(0.f, 0.f);
     }
-    // 4-channel threads (long filters) read a position's taps as 16-byte vectors
-    // (the tap rows are 16-byte aligned: DSTR and T are multiples of 4)
-    constexpr bool kVecTaps = NP == 2 && T % 4 == 0;
-    float dvv[T];
-    if constexpr (kVecTaps) {
-#pragma unroll
-        for (int t = 0; t < T; t += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dtl + t);
-            dvv[t] = d4.x;
-            dvv[t + 1] = d4.y;
-            dvv[t + 2] = d4.z;
-            dvv[t + 3] = d4.w;
-        }
-    }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        const float dv = kVecTaps ? dvv[t] : dtl[t];
+        const float dv = dtl[t];
         const float2 d2 = make_float2(dv, dv);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
@@ -386,10 +351,12 @@ __device__ __forceinline__ void conv_tile_ragged(uint32_t sb, uint32_t row_bytes
     }
 }
 
-// Register budget: 4 CTAs of 160 threads (8-channel threads) or 2 CTAs of 288
-// threads (4-channel threads) per SM.
+// Register budget: 4 CTAs of 160 threads per SM up to T = 4; 2 for longer
+// filters, whose window and taps need about 170 registers (8 channels per
+// thread either way: on the 8 x 32768 stream at T = 8 that measured 1.287 ms
+// against 1.297 ms for twice the threads with 4 channels each).
 template <int T, int PL, int NP, typename TOut>
-__global__ void __launch_bounds__(NP == 4 ? 160 : 288, NP == 4 ? 4 : 2)
+__global__ void __launch_bounds__(160, T <= 4 ? 4 : 2)
     dynconv_pipe_kernel(const PipeParams p) {
     constexpr int VEC = 2 * NP;  // channels per compute thread
     extern __shared__ __align__(128) uint8_t smem[];
@@ -562,9 +529,7 @@ __global__ void __launch_bounds__(NP == 4 ? 160 : 288, NP == 4 ? 4 : 2)
 
 template <int T, int PL, typename TOut>
 cudaError_t launch_pipe_t(PipeParams p, cudaStream_t stream) {
-    // 8 channels per thread up to T = 4; 4 channels (half the registers for the
-    // window and the taps, twice the threads) for longer filters
-    constexpr int NP = T <= 4 ? 4 : 2;
+    constexpr int NP = 4;      // 8 channels per thread
     p.nthr = p.nthr * 4 / NP;  // nthr arrives as the 8-channel thread count
     p.row_bytes = (uint32_t)p.nthr * (4u * NP);
     auto kern = dynconv_pipe_kernel<T, PL, NP, TOut>;
