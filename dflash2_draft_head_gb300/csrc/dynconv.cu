@@ -201,7 +201,10 @@ __global__ void __launch_bounds__(256) dynconv_kernel(const DynParams p) {
 // completing on an mbarrier:
 //   - the T-1 halo rows (from x, or from the history window for the first tile
 //     of a sequence) and the tile's rows of x, each the CTA's channel segment;
-//   - the tile's whole delta block [l][t][G] (contiguous in HBM).
+//   - the tile's whole delta block [l][t][G] (contiguous in HBM): one copy, or,
+//     when a (l, t) row of G values is a multiple of 128 bytes (every row then
+//     starts in the same shared-memory bank), one copy per position with the
+//     positions 16 bytes further apart than in HBM.
 // Compute threads consume a buffer (16-byte shared loads, a register sliding
 // window of T converted rows, packed FFMA2), store 16-byte outputs straight to
 // HBM and release the buffer with an mbarrier arrive.  The ring keeps several
@@ -224,7 +227,8 @@ struct PipeParams {
     int ng_max;            // groups a channel block can span
     int stages;
     uint32_t row_bytes;    // nthr * 16: one staged row segment
-    uint32_t stage_bytes;  // (T-1+PL) rows + PL*T*G bf16 of delta, 128-byte rounded
+    uint32_t dpos_bytes;   // staged delta bytes from one position to the next
+    uint32_t stage_bytes;  // (T-1+PL) rows + PL positions of delta, 128-byte rounded
 };
 
 
@@ -429,8 +433,14 @@ __global__ void __launch_bounds__(160, T <= 4 ? 4 : 2)
             for (int l = 0; l < nl; ++l)
                 bulk_g2s(dst + (uint32_t)(T - 1 + l) * p.row_bytes,
                          p.x + ((size_t)s * p.n + i0 + l) * p.C + c0, seg, fb);
-            bulk_g2s(dst + (uint32_t)(T - 1 + PL) * p.row_bytes,
-                     p.delta + ((size_t)s * p.n + i0) * TG, (uint32_t)(nl * TG) * 2u, fb);
+            const uint32_t ddst = dst + (uint32_t)(T - 1 + PL) * p.row_bytes;
+            const __nv_bfloat16* dsrc = p.delta + ((size_t)s * p.n + i0) * TG;
+            if (p.dpos_bytes == (uint32_t)TG * 2u)
+                bulk_g2s(ddst, dsrc, (uint32_t)(nl * TG) * 2u, fb);
+            else
+                for (int l = 0; l < nl; ++l)
+                    bulk_g2s(ddst + (uint32_t)l * p.dpos_bytes, dsrc + (size_t)l * TG,
+                             (uint32_t)TG * 2u, fb);
         }
         return;
     }
@@ -469,16 +479,22 @@ __global__ void __launch_bounds__(160, T <= 4 ? 4 : 2)
             if (p.G % 8 == 0) {
                 // 16-byte reads of 8 consecutive groups of one (l, t) row of the
                 // staged [l][t][G] block (G % 8 == 0 keeps them aligned), lanes over
-                // (l, t) so each of the 8 scattered stores hits consecutive words
+                // (l, t) so each of the 8 scattered stores hits nearby words: t
+                // fastest, or l fastest when the positions are staggered (rows of
+                // one position share banks, rows of 8 positions do not)
                 const int g8_lo = g_lo & ~7;
                 const int n8 = (g_lo + ng - g8_lo + 7) >> 3;
                 const uint32_t src0 = smem_u32(dsrc);
+                const bool stagger = p.dpos_bytes != (uint32_t)TG * 2u;
                 for (int q = tid; q < PL * T * n8; q += nthr) {
-                    const int lt = q % (PL * T);
+                    const int r = q % (PL * T);
+                    const int l = stagger ? r % PL : r / T;
+                    const int t = stagger ? r / PL : r % T;
+                    const int lt = l * T + t;
                     const int gb = g8_lo + (q / (PL * T)) * 8;
-                    const uint4 raw = (lt / T) < nl
-                                          ? lds_v4(src0 + (uint32_t)(lt * p.G + gb) * 2u)
-                                          : make_uint4(0, 0, 0, 0);
+                    const uint4 raw = l < nl ? lds_v4(src0 + (uint32_t)l * p.dpos_bytes +
+                                                      (uint32_t)(t * p.G + gb) * 2u)
+                                             : make_uint4(0, 0, 0, 0);
                     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -680,8 +696,11 @@ cudaError_t launch_dynconv(const DynconvArgs& a, cudaStream_t stream) {
         if (items <= 0x7FFFFFFFLL) {
             q.n_items = (int)items;
             q.row_bytes = (uint32_t)nthr * 16u;
+            // rows of G bf16 that are whole 128-byte lines would all start in
+            // one bank: stagger the staged positions by 16 bytes
+            q.dpos_bytes = (uint32_t)(a.T * a.G) * 2u + ((a.G * 2) % 128 == 0 ? 16u : 0u);
             const uint32_t raw = (uint32_t)(a.T - 1 + PLsel) * q.row_bytes +
-                                 (uint32_t)(PLsel * a.T * a.G) * 2u;
+                                 (uint32_t)PLsel * q.dpos_bytes;
             q.stage_bytes = (raw + 127u) & ~127u;
             q.stages = 2;
             return a.out_bf16 ? launch_pipe<PLsel, __nv_bfloat16>(q, a.T, stream)

@@ -84,6 +84,10 @@ def test_dynconv_edge_shapes(kw, dtype):
     (dict(S=100, n=13, C=5120, T=4, G=40), True),   # more tiles than resident CTAs, ragged
     (dict(S=77, n=21, C=5120, T=5, G=40), False),   # ragged tiles, no history
     (dict(S=256, n=16, C=5120, T=2, G=40), True),   # T = 2
+    # rows of G bf16 that are whole 128-byte lines: staged delta positions staggered
+    (dict(S=3, n=21, C=5120, T=8, G=64), True),     # the long-span shape, ragged tile
+    (dict(S=2, n=13, C=1024, T=3, G=128), False),   # cg = 8, no history
+    (dict(S=2, n=5, C=512, T=6, G=64), True),       # one partial tile, 64-thread block
 ])
 def test_dynconv_many_tiles(kw, hist):
     """Shapes with more (sequence, tile) items than resident CTAs (bf16 pipelined path)."""
