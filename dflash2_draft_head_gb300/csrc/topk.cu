@@ -1469,9 +1469,12 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             if (seedable && ks == 0) {
                 // First (full) stage: the K-th largest of the 256 lane maxima is at
                 // most the row's K-th best (those K maxima are distinct elements).
-                // Every warp sorts its 32 maxima; a candidate's rank among all 256
-                // is its place in its own sorted list plus the keys above it in the
-                // other seven (binary searches); the one of rank K-1 is the bound.
+                // Every warp sorts its 32 maxima.  For K <= 32 a tree of pairwise
+                // merges (warps w and w+4, then w and w+2, then 0 and 1) leaves the
+                // best 32 of all 256 in warp 0, whose lane K-1 is the bound; for
+                // larger K a candidate's rank among all 256 is its place in its own
+                // list plus the keys above it in the other seven (binary searches),
+                // and the one of rank K-1 is the bound.
                 int me = -1;
 #pragma unroll
                 for (int e = 0; e < EPT; ++e)
@@ -1482,7 +1485,25 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 sl[tid] = kk;
                 named_bar_sync(1, kNC);
                 if (tid == 0) c->seedk[slot ^ 1] = 0ull;  // the other row's readers are done
-                if (kk != 0ull && lane < p.K) {
+                if (p.K <= 32) {
+                    // each level reads lists the level before wrote and writes only
+                    // the reading warps' own slots
+                    uint64_t best = kk;
+                    if (warp < 4) {
+                        best = warp_merge_desc(best, sl[(warp + 4) * 32 + lane]);
+                        sl[tid] = best;
+                        named_bar_sync(3, 128);
+                    }
+                    if (warp < 2) {
+                        best = warp_merge_desc(best, sl[(warp + 2) * 32 + lane]);
+                        sl[tid] = best;
+                        named_bar_sync(4, 64);
+                    }
+                    if (warp == 0) {
+                        best = warp_merge_desc(best, sl[32 + lane]);
+                        if (lane == p.K - 1) c->seedk[slot] = best;  // 0: fewer than K keys
+                    }
+                } else if (kk != 0ull && lane < p.K) {
                     int rk = lane;
 #pragma unroll
                     for (int v = 0; v < kNF; ++v)
