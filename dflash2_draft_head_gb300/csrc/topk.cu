@@ -36,6 +36,7 @@
 // section header further down).
 // NaN entries never pass a test; rows with fewer than K other entries get
 // id -1 and value NaN in the remaining slots.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -313,6 +314,36 @@ __device__ __forceinline__ float stage_max(const uint32_t (&w)[kWPT]) {
 #pragma unroll
             for (int i = 0; i < h; ++i) t[i] = fmaxf(t[i], t[i + h]);
         return t[0];
+    }
+}
+
+// Bits e of gt / eq set when staged element e (as stage_elem numbers them) is
+// above / equal to t; NaN is neither.  bf16 stages compare packed pairs
+// against t as a bf16 pair (exact: every threshold is a bf16 element's value).
+template <bool BF16>
+__device__ __forceinline__ void stage_cmp_masks(const uint32_t (&w)[kWPT], float t, uint32_t& gt,
+                                                uint32_t& eq) {
+    gt = 0u;
+    eq = 0u;
+    if constexpr (BF16) {
+        const uint32_t h = __float_as_uint(t) >> 16;
+        const uint32_t t2 = h | (h << 16);
+        const __nv_bfloat162 tt = *reinterpret_cast<const __nv_bfloat162*>(&t2);
+#pragma unroll
+        for (int i = 0; i < kWPT; ++i) {
+            const __nv_bfloat162 x2 = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+            const uint32_t g = __hgt2_mask(x2, tt);  // low half: element 2i, high: 2i + 1
+            const uint32_t q = __heq2_mask(x2, tt);
+            gt |= ((g & 1u) | ((g >> 30) & 2u)) << (2 * i);
+            eq |= ((q & 1u) | ((q >> 30) & 2u)) << (2 * i);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kWPT; ++e) {
+            const float x = __uint_as_float(w[e]);
+            gt |= (x > t ? 1u : 0u) << e;
+            eq |= (x == t ? 1u : 0u) << e;
+        }
     }
 }
 
@@ -1537,13 +1568,8 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             if (__any_sync(0xffffffffu, mx >= tv)) {
                 // key > tk: value above tv, or equal to it (-0 == +0) with an
                 // index below the threshold's (complemented in the key)
-                uint32_t m = 0, mt = 0;
-#pragma unroll
-                for (int e = 0; e < EPT; ++e) {
-                    const float x = stage_elem<BF16>(w, e);
-                    m |= (x > tv ? 1u : 0u) << e;
-                    mt |= (x == tv ? 1u : 0u) << e;
-                }
+                uint32_t m, mt;
+                stage_cmp_masks<BF16>(w, tv, m, mt);
                 const uint32_t ti = ~(uint32_t)tk;
                 for (uint32_t mm = mt; mm; mm &= mm - 1u) {
                     const int e = __ffs(mm) - 1;
