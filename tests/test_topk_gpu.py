@@ -61,6 +61,7 @@ def _storage(z, dtype):
     (1, 1, 1), (3, 5, 5), (2, 7, 3), (5, 15, 4), (4, 33, 33), (2, 1000, 16), (7, 4099, 64),
     (2, 70001, 1), (3, 70001, 1024), (40, 9999, 16), (300, 5003, 8), (160, 2048, 1024),
     (17, 151937, 16), (5, 151936, 32), (12, 262144, 16), (16, 8, 8), (1, 262144, 1),
+    (6, 50021, 40), (3, 151936, 48), (150, 20011, 63),  # K in (32, 64]: two list registers
 ])
 def test_topk_shapes(rows, V, K, dtype):
     z = _storage(np.random.default_rng(rows * 7919 + V + K).standard_normal((rows, V)) * 2, dtype)
@@ -71,7 +72,8 @@ def test_topk_shapes(rows, V, K, dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("kind", ["ties", "ascending", "descending", "zeros", "nan", "ninf"])
-@pytest.mark.parametrize("rows,V,K", [(3, 20011, 16), (200, 3001, 64), (3, 20000, 16), (2, 4096, 32)])
+@pytest.mark.parametrize("rows,V,K", [(3, 20011, 16), (200, 3001, 64), (3, 20000, 16), (2, 4096, 32),
+                                      (4, 30011, 48)])
 def test_topk_degenerate(kind, rows, V, K, dtype):
     rng = np.random.default_rng(zlib.crc32(f"{kind}/{rows}/{V}".encode()))
     if kind == "ties":
