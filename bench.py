@@ -48,16 +48,16 @@ TRAFFIC = {
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
     ("batched_256x16_d5120", "topk"): {
-        "sha": "2a7da80a81a4f70142e6369571006d546d905c8c4ad86e8c36370c2f68ca3550",
-        "bytes": 8 * (311296512 + 3386624),
+        "sha": "5eff851a2690554aa4c322eb8f53d0a023a7fdccc307a417602a1bcc0ffa359e",
+        "bytes": 8 * (311341312 + 3631360),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "9d1f34eb8e1547391f7cfccba06cd7120f90f7b27fa698d2c978c1e568f448aa",
-        "bytes": 69796608 + 955392,
+        "sha": "d2ce70a25da5ac6f6466d56791640bf47b799bbec6a6ba89b6650c1fcf33eb64",
+        "bytes": 69797888 + 996352,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
-        "sha": "a8089d42b0aa0a1fcd1e5155cd243e23fc5ce4321e9f14ea019a000109fc83a1",
-        "bytes": 52396288 + 3153408,
+        "sha": "8b1254453ff647de614a550e6b7a3a920bd343bed6d783b0234df397d6484d6e",
+        "bytes": 52569856 + 3127296,
     },
 }
 
