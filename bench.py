@@ -252,6 +252,43 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------------------- host link
+
+def _host_link(pin, dst, copy_streams, split, stream, reps=5):
+    """Pinned host -> device copy rate of one step's inputs (the e2e loop's
+    tensors and copy streams), with no kernel running: all tensors on one
+    stream, then split over the two copy streams as the e2e loop splits them."""
+    import torch
+
+    nbytes = sum(v.numel() * v.element_size() for v in pin.values())
+
+    def run(groups):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for cst in copy_streams[:len(groups)]:
+            cst.wait_event(e0)
+        for _ in range(reps):
+            for cst, names in zip(copy_streams, groups):
+                with torch.cuda.stream(cst):
+                    for k in names:
+                        dst[k].copy_(pin[k], non_blocking=True)
+        for cst in copy_streams[:len(groups)]:
+            ev = torch.cuda.Event()
+            ev.record(cst)
+            stream.wait_event(ev)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
+    one = [sorted(pin)]
+    run(one)
+    t1 = run(one)
+    t2 = run(split)
+    return {"bytes": nbytes, "reps": reps, "GB/s_1stream": nbytes * reps / t1 / 1e6,
+            "GB/s_2streams": nbytes * reps / t2 / 1e6}
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -909,6 +946,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    link = _host_link(pin, d_in, copy_streams, split, stream)
 
     positions = w.S * w.n * world
     value = positions * K / (total_ms / 1000.0)
@@ -1029,7 +1067,14 @@ def main():
         "e2e": {"value": positions * E2 / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": E2,
                 "pipelining": "double-buffered inputs: step k+1's H2D copies (2 streams) overlap "
-                              "step k's kernels"},
+                              "step k's kernels",
+                # the host link alone: one step's inputs copied with no kernel running
+                "host_link": {**link,
+                              "bound_positions_per_s": positions / (
+                                  h2d / (1e9 * max(link["GB/s_1stream"], link["GB/s_2streams"]))),
+                              "frac_of_bound": (positions * E2 / (e2e_ms / 1000.0)) / (
+                                  positions / (h2d / (1e9 * max(link["GB/s_1stream"],
+                                                                link["GB/s_2streams"]))))}},
         # dynconv + the selector (one kernel, or project + edges) per timed step
         "gpu_launches": (2 if sel_plan["fused"] else 3) * K,
         "clocks": clk.summary(),
