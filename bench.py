@@ -52,8 +52,8 @@ TRAFFIC = {
         "bytes": 8 * (311341312 + 3631360),
     },
     ("batched_256x16_d5120", "select"): {
-        "sha": "d2ce70a25da5ac6f6466d56791640bf47b799bbec6a6ba89b6650c1fcf33eb64",
-        "bytes": 69797888 + 996352,
+        "sha": "6612f58bcc72d04450b131bd2958dbfd202b8042e9e5b9ea71329c420c3e2c45",
+        "bytes": 69798656 + 977408,
     },
     ("batched_256x16_d5120", "dynconv_predicted"): {
         "sha": "8b1254453ff647de614a550e6b7a3a920bd343bed6d783b0234df397d6484d6e",

@@ -76,5 +76,36 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+TRACE_LIB = os.path.join(PKG, "libdflash2_trace.so")
+
+
+def build_traced(force: bool = False) -> str:
+    """The library with the selector's phase trace compiled in (select.cu with
+    -DDF2_TRACE, every other object from the normal build): a separate
+    libdflash2_trace.so for measurement; the normal library is unchanged."""
+    build()
+    deps = _deps() + [LIB]
+    if not force and os.path.exists(TRACE_LIB) and \
+            all(os.path.getmtime(p) <= os.path.getmtime(TRACE_LIB) for p in deps):
+        return TRACE_LIB
+    nvcc = _nvcc()
+    tdir = os.path.join(BUILD, "trace")
+    os.makedirs(tdir, exist_ok=True)
+    sel = os.path.join(CSRC, "select.cu")
+    obj = os.path.join(tdir, "select.o")
+    r = subprocess.run([nvcc, *NVCC_FLAGS, "-DDF2_TRACE", "-c", sel, "-o", obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on select.cu (traced):\n{r.stderr}")
+    objs = [obj if os.path.basename(src) == "select.cu"
+            else os.path.join(BUILD, os.path.basename(src)[:-3] + ".o") for src in _sources()]
+    tmp = TRACE_LIB + f".tmp{os.getpid()}"
+    r = subprocess.run([nvcc, "-shared", *ARCH, "-o", tmp, *objs], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed (traced):\n{r.stderr}")
+    os.replace(tmp, TRACE_LIB)
+    return TRACE_LIB
+
+
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv, verbose=True))

@@ -63,6 +63,28 @@ namespace df2 {
 // Device-side fault word of the fused selector (read by dflash2_take_device_faults).
 __device__ unsigned int g_select_fault = 0;
 
+// Phase trace (compiled in only with -DDF2_TRACE; otherwise every trace point
+// is empty): global-timer stamps of CTAs 0..kTraceCTAs-1, kTraceSlots per CTA,
+// at the points include/dflash2.h lists with dflash2_trace_read.  DF2_TRACE_RB
+// records only during a CTA's first row block.
+#ifdef DF2_TRACE
+constexpr int kTraceCTAs = 512;
+constexpr int kTraceSlots = 64;
+__device__ unsigned long long g_trace[kTraceCTAs * kTraceSlots];
+#define DF2_TRACE_AT(k)                                                                   \
+    do {                                                                                  \
+        if (blockIdx.x < (unsigned)kTraceCTAs) g_trace[blockIdx.x * kTraceSlots + (k)] = global_ns(); \
+    } while (0)
+#else
+#define DF2_TRACE_AT(k) \
+    do {                \
+    } while (0)
+#endif
+#define DF2_TRACE_RB(k)                \
+    do {                               \
+        if (rbi == 0) DF2_TRACE_AT(k); \
+    } while (0)
+
 namespace {
 
 constexpr int SEL_THREADS = 512;   // 16 warps
@@ -200,6 +222,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const int nm1 = p.n - 1;
     const int gtid = tid - 8 * 32;    // gather thread index (>= 0 in warps 8..15)
     const uint32_t row_bytes = p.red_stride * 4u;
+    if (tid == 0) DF2_TRACE_AT(0);
 
     auto init_edge_bars = [&]() {
         for (int i = 0; i < p.estages; ++i) {
@@ -238,6 +261,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // previous kernel; no input is read before it has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (tid == 0) DF2_TRACE_AT(1);
 
     auto wait = [&](uint32_t bar, uint32_t parity) {
         if (*abort_flag) return;
@@ -338,6 +362,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     }
                 }
             }
+            if (gtid == 0 && j < 6) DF2_TRACE_RB(9 + j);
             cp_async_mbar_arrive_noinc(landed0 + 8 * st);
             if (half == p.nhalf - 1) id_next = raw_id(t + 1);
         };
@@ -378,6 +403,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                         const int st = it - use * p.pstages;
                         wait(full0 + 8 * st, (uint32_t)use & 1u);
                         tc_fence_after();
+                        if (kb == kb0) DF2_TRACE_RB(2);
                         const uint32_t a0 = sE + (uint32_t)st * p.pstage_bytes;
                         const uint32_t b0 = a0 + HTILE;
                         if (!*abort_flag) {
@@ -388,7 +414,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                         }
                         tc_commit(empty0 + 8 * st);
                     }
-                    tc_commit(accum);  // every issuer arrives once, with or without k-blocks
+                    tc_commit(accum); DF2_TRACE_RB(3 + 0 * q);  // every issuer arrives once, with or without k-blocks
                 }
                 __syncwarp();
             } else if (warp >= 8) {
@@ -436,6 +462,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             if (tid == 0 && CS > 1)
                 mbar_arrive_expect_tx(recv, (uint32_t)(CS - 1) * (uint32_t)(o_hi - o_lo) * (uint32_t)R * 4u);
             wait(accum, (uint32_t)rbi & 1u);
+        if (tid == 0) DF2_TRACE_RB(4);
             tc_fence_before();
             // the gather warps only arrive: their first units need this CTA's ring
             // drained (the accumulator barrier), not the rest of the cluster, so
@@ -449,6 +476,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 __syncthreads();
             }
             tc_fence_after();
+        if (tid == 0) DF2_TRACE_RB(5);
             if (warp < 8) {
                 const int q = warp & 3;
                 const int cw = R >> 1;
@@ -496,6 +524,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 named_bar_sync(3, 256);  // own rows in place
                 // ================= phase C: the owner sums its rows' partials
                 if (CS > 1) wait(recv, (uint32_t)rbi & 1u);
+            if (tid == 0) DF2_TRACE_RB(6);
                 // (row, 4-column group) items; R is a power of two, so no divides
                 const int own = o_hi - o_lo;
                 const int l2c4 = p.log2R - 2;
@@ -526,6 +555,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             }
         }
         __syncthreads();  // u slice complete; the receive slots are free
+        if (tid == 0) DF2_TRACE_RB(7);
 
         // ================= phase D: the edge tiles of this CTA's positions
         if (warp >= 8) {
@@ -533,6 +563,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             // previous unit (the first n_early units were issued in phase B)
             for (int j = p.n_early; j < nunits; ++j) issue_unit(j);
             cp_async_wait_all();
+            if (gtid == 0) DF2_TRACE_RB(8);
         } else if (warp < 4) {
             // gate: thread tid owns chunk column c of some of the unit's 32 four-row
             // groups (a row slot of cpr threads takes groups g_first, g_first +
@@ -559,6 +590,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                 const int e0 = e_lo + t * TP;
                 const int rows_valid = min(TP, e_hi - e0) << p.log2K;
                 wait(landed0 + 8 * st, (uint32_t)use & 1u);
+                if (tid == 0 && j < 6) DF2_TRACE_RB(15 + j);
+                if (tid == 64 && j < 4) DF2_TRACE_RB(56 + j);
                 const uint32_t sb = estage_base(st) + c_off;
                 const int col = half * 64 * p.nkb_e + c * 8;
                 if (!*abort_flag) {
@@ -623,6 +656,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                         }
                         tc_commit(sfree0 + 8 * st);
                         if (half == p.nhalf - 1) tc_commit(tfull0 + 8 * bb);
+                        if (j < 6) DF2_TRACE_RB(21 + j);
                     }
                     __syncwarp();
                 }
@@ -767,6 +801,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                     p.best_score[(size_t)e * K + pslot] = best;
                 }
                 tc_fence_before();
+                if (tid == 128 && t < 4) DF2_TRACE_RB(27 + t);
                 mbar_arrive(tempty0 + 8 * bb);
             }
         }
@@ -796,6 +831,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) DF2_TRACE_AT(31);
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1147,3 +1183,23 @@ cudaError_t take_select_faults(unsigned* flags) {
 }
 
 }  // namespace df2
+
+extern "C" int dflash2_trace_read(uint64_t* host, int bytes, int clear) {
+#ifdef DF2_TRACE
+    if (host == nullptr || bytes < 0 || (size_t)bytes > sizeof(df2::g_trace))
+        return DF2_ERR_INVALID_ARG;
+    if (cudaMemcpyFromSymbol(host, df2::g_trace, (size_t)bytes) != cudaSuccess) return DF2_ERR_CUDA;
+    if (clear) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, df2::g_trace) != cudaSuccess ||
+            cudaMemset(a, 0, sizeof(df2::g_trace)) != cudaSuccess)
+            return DF2_ERR_CUDA;
+    }
+    return DF2_OK;
+#else
+    (void)host;
+    (void)bytes;
+    (void)clear;
+    return DF2_ERR_UNSUPPORTED;
+#endif
+}

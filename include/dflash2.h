@@ -332,6 +332,30 @@ int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const
                          int n_ids, uint32_t* out, void* stream);
 
 /*
+ * Phase trace of dflash2_select's one-kernel path, for a library built with
+ * tracing (build.build_traced(): the selector compiled with -DDF2_TRACE; the
+ * normal build returns DF2_ERR_UNSUPPORTED and records nothing).  Copies the
+ * first `bytes` bytes of the trace table to host memory `host`, then zeroes the
+ * table when `clear` is nonzero.  The table is 512 CTAs x 64 slots of uint64
+ * global-timer readings (ns; 0 = not reached), written during each CTA's first
+ * row block (slots 0, 1 and 31: every launch), so after one launch slot k of
+ * CTA b is host[64*b + k]:
+ *   0 entry, set-up done      1 previous grid complete (griddep wait)
+ *   2 first TMA stage of h and W landed (MMA issuers)   3 last projection MMAs committed
+ *   4 accumulators complete   5 cluster barrier passed (every projection of the cluster done)
+ *   6 the CTA's partials received   7 partials summed, u slice written
+ *   8 every edge unit's gathers issued
+ *   9..14  edge units 0..5 issued (first gather warp)
+ *   15..20 edge units 0..5 landed (gate warp)   21..26 units 0..5 MMAs committed
+ *   27..30 units 0..3 scored (epilogue)   31 CTA exit
+ *   56..59 units 0..3 landed, as seen by the second gate warp
+ * Synchronises with nothing: call after the launch has completed.  Returns
+ * DF2_OK, DF2_ERR_INVALID_ARG (NULL host, bytes < 0 or larger than the
+ * table), DF2_ERR_UNSUPPORTED or DF2_ERR_CUDA.
+ */
+int dflash2_trace_read(uint64_t* host, int bytes, int clear);
+
+/*
  * Reads and clears the library's device-side fault word for the current
  * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_dynconv,
  * dflash2_dynconv_predicted, dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from

@@ -235,3 +235,10 @@ def _probe(L, tb=P[0], rows=1000, rb=256, ids=P[1], n=64, out=P[2]):
 def test_probe_gather_validation(L, kw, code):
     assert _probe(L, **kw) == code
     assert L.dflash2_last_error()
+
+
+def test_trace_read_is_unsupported_without_tracing(L):
+    """The normal library has no trace table: the call reports it and touches no device."""
+    buf = (ctypes.c_uint64 * 4)()
+    L.dflash2_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    assert L.dflash2_trace_read(ctypes.addressof(buf), 32, 0) == 2

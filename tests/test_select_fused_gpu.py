@@ -131,3 +131,46 @@ def test_edges_call_matches_the_selectors_edge_phase(S, n, d, K, R, V):
                                   dev(cb["B"], "bf16"), dev(sel["unary"]), edges_out=True)
     torch.cuda.synchronize()
     assert torch.equal(e, e2) and torch.equal(slot, slot2) and torch.equal(score, score2)
+
+
+@pytest.mark.gpu
+def test_traced_build_matches_and_records_phases():
+    """The selector built with its trace points gives the same outputs as the
+    normal library, and each CTA's stamps are ordered along the kernel."""
+    import ctypes
+    from dflash2_draft_head_gb300 import build as B
+    from dflash2_draft_head_gb300.workloads import BY_NAME
+    w = BY_NAME["qwen27b_single_block16"]
+    cb = synth.codebooks(w)
+    si = synth.selector_inputs(w)
+    bt = torch.bfloat16
+    h, W, A, Bm = (t.to(bt).cuda() for t in (si["h"], cb["W"], cb["A"], cb["B"]))
+    ids, un = si["cand_ids"].cuda(), si["unary"].cuda()
+    u0, e0, s0, c0 = df2.select(h, W, ids, A, Bm, un)
+    T = ctypes.CDLL(B.build_traced())
+    vp = ctypes.c_void_p
+    T.dflash2_trace_read.argtypes = [vp, ctypes.c_int, ctypes.c_int]
+    P, E = w.S_sel * w.n_sel, w.S_sel * (w.n_sel - 1)
+    u = torch.empty((P, w.R), dtype=torch.float32, device="cuda")
+    slot = torch.empty((E, w.K), dtype=torch.int32, device="cuda")
+    score = torch.empty((E, w.K), dtype=torch.float32, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    buf = torch.zeros(512 * 64, dtype=torch.int64)
+    torch.cuda.synchronize()
+    assert T.dflash2_trace_read(vp(buf.data_ptr()), buf.numel() * 8, 1) == 0
+    rc = T.dflash2_select(vp(h.data_ptr()), vp(W.data_ptr()), vp(ids.data_ptr()), vp(A.data_ptr()),
+                          vp(Bm.data_ptr()), vp(un.data_ptr()), w.S_sel, w.n_sel, w.d, w.K, w.R,
+                          w.V, 1, vp(u.data_ptr()), None, vp(slot.data_ptr()), vp(score.data_ptr()),
+                          vp(flag.data_ptr()), vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    assert torch.equal(u, u0.view(P, w.R))
+    assert torch.equal(slot, s0.view(E, w.K)) and torch.equal(score, c0.view(E, w.K))
+    assert T.dflash2_trace_read(vp(buf.data_ptr()), buf.numel() * 8, 0) == 0
+    st = buf.view(512, 64)
+    live = st[st[:, 0] > 0]
+    assert live.shape[0] > 0
+    for a, b in ((0, 1), (1, 4), (4, 31)):
+        ok = (live[:, a] > 0) & (live[:, b] > 0)
+        assert ok.any() and bool((live[ok, b] >= live[ok, a]).all()), (a, b)
