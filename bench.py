@@ -48,8 +48,8 @@ TRAFFIC = {
     # captured on 512 rows (same kernel, same V and K), scaled by 4096 / 512: every row
     # streams once, so DRAM traffic grows in proportion to the rows
     ("batched_256x16_d5120", "topk"): {
-        "sha": "5eff851a2690554aa4c322eb8f53d0a023a7fdccc307a417602a1bcc0ffa359e",
-        "bytes": 8 * (311341312 + 3631360),
+        "sha": "44bcef28a9e26a4fb49140d8ca8d19c39eef514ce542cdf321497360a4e547d3",
+        "bytes": 8 * (311339776 + 3530496),
     },
     ("batched_256x16_d5120", "select"): {
         "sha": "6612f58bcc72d04450b131bd2958dbfd202b8042e9e5b9ea71329c420c3e2c45",

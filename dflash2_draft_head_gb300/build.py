@@ -79,10 +79,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 TRACE_LIB = os.path.join(PKG, "libdflash2_trace.so")
 
 
+TRACED = ("select.cu", "topk.cu")
+
+
 def build_traced(force: bool = False) -> str:
-    """The library with the selector's phase trace compiled in (select.cu with
-    -DDF2_TRACE, every other object from the normal build): a separate
-    libdflash2_trace.so for measurement; the normal library is unchanged."""
+    """The library with the phase traces compiled in (the selector's and the
+    streaming top-K's sources with -DDF2_TRACE, every other object from the
+    normal build): a separate libdflash2_trace.so for measurement; the normal
+    library is unchanged."""
     build()
     deps = _deps() + [LIB]
     if not force and os.path.exists(TRACE_LIB) and \
@@ -91,14 +95,19 @@ def build_traced(force: bool = False) -> str:
     nvcc = _nvcc()
     tdir = os.path.join(BUILD, "trace")
     os.makedirs(tdir, exist_ok=True)
-    sel = os.path.join(CSRC, "select.cu")
-    obj = os.path.join(tdir, "select.o")
-    r = subprocess.run([nvcc, *NVCC_FLAGS, "-DDF2_TRACE", "-c", sel, "-o", obj],
-                       capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on select.cu (traced):\n{r.stderr}")
-    objs = [obj if os.path.basename(src) == "select.cu"
-            else os.path.join(BUILD, os.path.basename(src)[:-3] + ".o") for src in _sources()]
+
+    def compile_one(name):
+        obj = os.path.join(tdir, name[:-3] + ".o")
+        r = subprocess.run([nvcc, *NVCC_FLAGS, "-DDF2_TRACE", "-c", os.path.join(CSRC, name),
+                            "-o", obj], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {name} (traced):\n{r.stderr}")
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(TRACED)) as ex:
+        list(ex.map(compile_one, TRACED))
+    objs = [os.path.join(tdir if os.path.basename(src) in TRACED else BUILD,
+                         os.path.basename(src)[:-3] + ".o") for src in _sources()]
     tmp = TRACE_LIB + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, "-shared", *ARCH, "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:

@@ -53,6 +53,26 @@ namespace df2 {
 // gives up, DF2_FLAG_OVERFLOW if the candidate buffer bound were ever hit.
 __device__ unsigned int g_topk_fault = 0;
 
+// Row trace of the streaming kernel (compiled in only with -DDF2_TRACE;
+// otherwise every trace point is empty): global-timer stamps of CTAs
+// 0..1023, 64 slots each: 8 points for each of 8 traced rows of the CTA (its
+// rows 0-3 and 10-13), at the points include/dflash2.h lists with
+// dflash2_trace_read_topk.
+#ifdef DF2_TRACE
+__device__ unsigned long long g_trace_topk[1024 * 64];
+#define DF2_TK_ROW(r) ((r) < 4 ? (r) : ((r) >= 10 && (r) < 14 ? (r) - 6 : -1))
+#define DF2_TK_TRACE(r, k)                                                        \
+    do {                                                                          \
+        const int tr_ = DF2_TK_ROW(r);                                            \
+        if (tr_ >= 0 && blockIdx.x < 1024u)                                       \
+            g_trace_topk[blockIdx.x * 64 + tr_ * 8 + (k)] = global_ns();          \
+    } while (0)
+#else
+#define DF2_TK_TRACE(r, k) \
+    do {                   \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int kNC = 256;                   // consumer threads (8 warps)
@@ -1116,6 +1136,8 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                     mbar_arrive_expect_tx(full0 + 8 * st, bytes);
                     bulk_g2s(s0 + (uint32_t)st * kSB, reinterpret_cast<const void*>(off), bytes,
                              full0 + 8 * st);
+                    if (off == b0) DF2_TK_TRACE((row - cid) / ncl, 5);
+                    if (off + kSB >= b1) DF2_TK_TRACE((row - cid) / ncl, 6);
                 }
             }
         }
@@ -1437,6 +1459,7 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
             if (lane == 0) {
                 c->tau[slot] = 0ull;  // free for row rit + 2
                 st_release_u32(&c->sel_done, (uint32_t)(rit + 1));
+                DF2_TK_TRACE(rit, 4);
             }
         }
         __syncwarp();
@@ -1467,8 +1490,10 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
         if (tid < tail) tx = load_logit<BF16>(p.logits, rowoff + (e1 - tail) + tid);
         // At most one row ahead of the selector: it has finished the row that
         // last used this threshold slot and reset it to 0 (no threshold).
+        if (tid == 0) DF2_TK_TRACE(rit, 0);
         if (lane == 0 && rit >= 2) wait_counter(&c->sel_done, (uint32_t)(rit - 1), abort_flag);
         __syncwarp();
+        if (tid == 0) DF2_TK_TRACE(rit, 1);
         if (!seedable && warp == 0)
             push_one(tid < head && hx == hx, hx, (uint32_t)(e0 + tid), myq, qh, c, warp, abort_flag);
 
@@ -1578,8 +1603,11 @@ __global__ void __launch_bounds__(kAThreads, 1) topk_async_kernel(TopkParams p) 
                 push_keys<BF16, E>(m, sb, idx0, myq, qh, c, warp, abort_flag);
             }
             __syncwarp();
+            if (tid == 0 && ks == 0) DF2_TK_TRACE(rit, 2);
             if (lane == 0) mbar_arrive(empty0 + 8 * st);  // done with the stage
         }
+        if (tid == 0) DF2_TK_TRACE(rit, 3);
+        if (tid == 224) DF2_TK_TRACE(rit, 7);
         if (warp == 0 && tail > 0) {
             const unsigned long long tk = ld_volatile_u64(&c->tau[slot]);
             const uint32_t ti = (uint32_t)(e1 - tail + tid);
@@ -2011,3 +2039,24 @@ cudaError_t take_topk_faults(unsigned* flags) {
 }
 
 }  // namespace df2
+
+extern "C" int dflash2_trace_read_topk(uint64_t* host, int bytes, int clear) {
+#ifdef DF2_TRACE
+    if (host == nullptr || bytes < 0 || (size_t)bytes > sizeof(df2::g_trace_topk))
+        return DF2_ERR_INVALID_ARG;
+    if (cudaMemcpyFromSymbol(host, df2::g_trace_topk, (size_t)bytes) != cudaSuccess)
+        return DF2_ERR_CUDA;
+    if (clear) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, df2::g_trace_topk) != cudaSuccess ||
+            cudaMemset(a, 0, sizeof(df2::g_trace_topk)) != cudaSuccess)
+            return DF2_ERR_CUDA;
+    }
+    return DF2_OK;
+#else
+    (void)host;
+    (void)bytes;
+    (void)clear;
+    return DF2_ERR_UNSUPPORTED;
+#endif
+}

@@ -356,6 +356,23 @@ int dflash2_probe_gather(const void* table, long long rows, int row_bytes, const
 int dflash2_trace_read(uint64_t* host, int bytes, int clear);
 
 /*
+ * Row trace of dflash2_topk's streaming kernel (K <= 256, more rows than the
+ * few-row kernel takes), for a library built with tracing as above; the normal
+ * build returns DF2_ERR_UNSUPPORTED.  Same copy / clear / return conventions as
+ * dflash2_trace_read.  The table is 1024 CTAs x 64 slots of uint64 global-timer
+ * readings (ns; 0 = not reached): slot 8*j + k of CTA b is point k of the CTA's
+ * j-th traced row, the traced rows being the CTA's rows 0, 1, 2, 3, 10, 11, 12
+ * and 13 (its row iterations, in order):
+ *   0 filter warp 0 reaches the row   1 ... after waiting for the selector
+ *                                       (the filters run at most one row ahead)
+ *   2 the row's first stage (the threshold seeding) processed
+ *   3 filter warp 0 done with the row   7 filter warp 7 done with the row
+ *   4 the selector done with the row
+ *   5 the producer issued the row's first stage   6 ... its last stage
+ */
+int dflash2_trace_read_topk(uint64_t* host, int bytes, int clear);
+
+/*
  * Reads and clears the library's device-side fault word for the current
  * device (DF2_FLAG_TIMEOUT when a bounded wait inside dflash2_dynconv,
  * dflash2_dynconv_predicted, dflash2_project or dflash2_topk gave up; DF2_FLAG_OVERFLOW from

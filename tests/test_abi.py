@@ -242,3 +242,9 @@ def test_trace_read_is_unsupported_without_tracing(L):
     buf = (ctypes.c_uint64 * 4)()
     L.dflash2_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     assert L.dflash2_trace_read(ctypes.addressof(buf), 32, 0) == 2
+
+
+def test_topk_trace_read_is_unsupported_without_tracing(L):
+    buf = (ctypes.c_uint64 * 4)()
+    L.dflash2_trace_read_topk.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    assert L.dflash2_trace_read_topk(ctypes.addressof(buf), 32, 0) == 2

@@ -146,3 +146,40 @@ def test_topk_feeds_selector():
     from helpers import assert_argmax, assert_close
     assert_close(e.cpu().numpy(), re, "bf16", "chained edges")
     assert_argmax(slot.cpu().numpy(), re, rslot, "bf16", "chained argmax")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_traced_build_matches_and_records_rows(dtype):
+    """The streaming top-K built with its trace points returns the same ids and
+    values as the normal library, and each traced row's points are ordered."""
+    import ctypes
+    from dflash2_draft_head_gb300 import build as B
+    rows, V, K = 2048, 4099, 16  # 13-14 rows per CTA: rows 10-13 are traced too
+    z = _storage(np.random.default_rng(4321).standard_normal((rows, V)) * 2, dtype)
+    x = _to_dev(z, dtype)
+    ids0, vals0 = df2.topk(x, K)
+    T = ctypes.CDLL(B.build_traced())
+    vp = ctypes.c_void_p
+    T.dflash2_trace_read_topk.argtypes = [vp, ctypes.c_int, ctypes.c_int]
+    T.dflash2_topk.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+    ids = torch.empty(rows, K, dtype=torch.int32, device="cuda")
+    vals = torch.empty(rows, K, dtype=torch.float32, device="cuda")
+    buf = torch.zeros(1024 * 64, dtype=torch.int64)
+    torch.cuda.synchronize()
+    assert T.dflash2_trace_read_topk(vp(buf.data_ptr()), buf.numel() * 8, 1) == 0
+    assert T.dflash2_topk(vp(x.data_ptr()), rows, V, K, 1 if dtype == "bf16" else 0,
+                          vp(ids.data_ptr()), vp(vals.data_ptr()),
+                          vp(torch.cuda.current_stream().cuda_stream)) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids0.view(rows, K))
+    assert torch.equal(vals.view(torch.int32), vals0.view(rows, K).view(torch.int32))
+    assert T.dflash2_trace_read_topk(vp(buf.data_ptr()), buf.numel() * 8, 0) == 0
+    st = buf.view(1024, 8, 8)
+    for j in (0, 4):
+        r = st[:, j, :]
+        live = r[:, 0] > 0
+        assert live.any()
+        r = r[live]
+        for a, b in ((0, 1), (1, 2), (2, 3), (0, 4)):
+            assert bool((r[:, b] >= r[:, a]).all()), (j, a, b)
